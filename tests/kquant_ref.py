@@ -1,0 +1,92 @@
+"""Test-side k-quant encoder and a second, independently written decoder.
+
+The encoder builds super-blocks from their fields (d, dmin, s_j, m_j, q_i) with
+Python integers, so that a hand-constructed block has a value that follows from
+its fields alone. The decoder reads the packed bytes with 64-bit shifts and
+index arithmetic, a different route from the oracle's bit-stream unpacking; the
+brute-force checks use it so that they share no dequantisation code with the
+oracle.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def encode_header(d: float, dmin: float, s, m) -> bytes:
+    acc = 0
+    for j in range(8):
+        assert 0 <= s[j] < 64 and 0 <= m[j] < 64
+        acc |= int(s[j]) << (6 * j)
+        acc |= int(m[j]) << (48 + 6 * j)
+    return (np.float16(d).tobytes() + np.float16(dmin).tobytes()
+            + acc.to_bytes(12, "little"))
+
+
+def encode_q4k(d, dmin, s, m, q) -> np.ndarray:
+    assert len(q) == 256 and all(0 <= v < 16 for v in q)
+    qs = bytes(int(q[2 * b]) | (int(q[2 * b + 1]) << 4) for b in range(128))
+    return np.frombuffer(encode_header(d, dmin, s, m) + qs, dtype=np.uint8).copy()
+
+
+def encode_q5k(d, dmin, s, m, q) -> np.ndarray:
+    assert len(q) == 256 and all(0 <= v < 32 for v in q)
+    hi = 0
+    for i in range(256):
+        hi |= (int(q[i]) >> 4) << i
+    low = [int(v) & 15 for v in q]
+    qs = bytes(low[2 * b] | (low[2 * b + 1] << 4) for b in range(128))
+    return np.frombuffer(encode_header(d, dmin, s, m) + hi.to_bytes(32, "little") + qs,
+                         dtype=np.uint8).copy()
+
+
+def expected_weights(d, dmin, s, m, q) -> np.ndarray:
+    """w_i = d * s_j * q_i - dmin * m_j, j = i // 32, from the fields."""
+    d64 = float(np.float16(d))
+    m64 = float(np.float16(dmin))
+    return np.array([d64 * s[i // 32] * q[i] - m64 * m[i // 32] for i in range(256)])
+
+
+def _le_u64(b: np.ndarray) -> np.ndarray:
+    out = np.zeros(b.shape[:-1], dtype=np.uint64)
+    for n in range(b.shape[-1]):
+        out |= b[..., n].astype(np.uint64) << np.uint64(8 * n)
+    return out
+
+
+def decode(blocks: np.ndarray) -> np.ndarray:
+    """[..., 144 or 176] uint8 -> [..., 256] float64 (second implementation)."""
+    nb = blocks.shape[-1]
+    d = blocks[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    dmin = blocks[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    lo = _le_u64(blocks[..., 4:12])          # field bits 0..63
+    hi = _le_u64(blocks[..., 12:16])         # field bits 64..95
+    fields = []
+    for f in range(16):
+        p = 6 * f
+        if p + 6 <= 64:
+            v = (lo >> np.uint64(p)) & np.uint64(63)
+        elif p >= 64:
+            v = (hi >> np.uint64(p - 64)) & np.uint64(63)
+        else:
+            v = ((lo >> np.uint64(p)) | (hi << np.uint64(64 - p))) & np.uint64(63)
+        fields.append(v.astype(np.float64))
+    i = np.arange(256)
+    if nb == 144:
+        qs = blocks[..., 16:144]
+        qh = None
+    else:
+        qs = blocks[..., 48:176]
+        qh = blocks[..., 16:48]
+    q = (qs[..., i // 2].astype(np.int64) >> (4 * (i % 2))) & 15
+    if qh is not None:
+        q = q + 16 * ((qh[..., i // 8].astype(np.int64) >> (i % 8)) & 1)
+    s = np.stack(fields[0:8], axis=-1)[..., i // 32]
+    m = np.stack(fields[8:16], axis=-1)[..., i // 32]
+    return d[..., None] * s * q - dmin[..., None] * m
+
+
+def dense(W: np.ndarray) -> np.ndarray:
+    """[..., rows, nblk, bytes] -> [..., rows, nblk*256] via ``decode``."""
+    v = decode(W)
+    return v.reshape(*W.shape[:-2], W.shape[-2] * 256)
