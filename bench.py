@@ -1,0 +1,402 @@
+"""Throughput of the k-quant routed-MoE layer on GB300 (one JSON line).
+
+A step is one forward of the whole layer (router, top-k, permutation, grouped
+gate/up + SwiGLU, grouped down, slot-order combine with the shared expert and
+the residual) over one batch of T rows. The default workload is the decode row
+of the Qwen3.5-35B-A3B-shaped layer: T=1, H=2048, E=256, top-8, F=512, shared
+expert, Q4_K gate/up, Q5_K down, fp32 hidden rows, seeded synthetic weights.
+
+L2 (129 MB) is defeated with 16 distinct layer instances, rotated step by step,
+7.8 GB in total: the weights one step touches are evicted before that instance
+comes round again. Steps are CUDA-graph replays on one stream, timed with CUDA
+events; the dominant kernel is timed again with per-launch events around its
+own launches on the same stream. ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+H, E, K_TOP, F = 2048, 256, 8, 512
+EXPERT_BYTES = 2 * F * (H // 256) * 144 + H * (F // 256) * 176   # 1 900 544
+GATEUP_EXPERT_BYTES = 2 * F * (H // 256) * 144                    # 1 179 648
+WORKLOADS = {
+    "decode": dict(T=1, routing="uniform"),
+    "decode64": dict(T=64, routing="uniform"),
+    "decode64-zipf": dict(T=64, routing="zipf"),
+    "prefill512": dict(T=512, routing="uniform"),
+    "prefill4096": dict(T=4096, routing="uniform"),
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    p.add_argument("--layers", type=int, default=16)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=str, default=None, help=argparse.SUPPRESS)
+    return p.parse_args()
+
+
+def workload_config(name, T, routing, layers):
+    return {"workload": f"{name}: routed-MoE layer, T={T} rows, H={H}, E={E}, top-{K_TOP}, F={F}, "
+                        f"shared expert, Q4_K gate/up, Q5_K down, fp32 hidden, {routing} routing",
+            "T": T, "H": H, "E": E, "top_k": K_TOP, "F": F, "routing": routing,
+            "l2": f"{layers} distinct layer instances rotated ({layers * EXPERT_BYTES * 257 / 1e9:.1f} GB "
+                  f"> 129 MB L2)",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_sample_main(spec: str):
+    """Runs in a child process: times the oracle on ``n`` single-row forwards
+    of layer instance 0 and prints timings and outputs as JSON."""
+    from oracle import qmoe_oracle as oracle
+    from quantized_moe_transformer_gb300 import inputs
+    cfg = json.loads(spec)
+    arr = inputs.moe_layer(0, H, E, F, shared=True, routing=cfg["routing"])
+    X = inputs.hidden(1000, cfg["rows"], H, cfg["routing"])
+    times, outs = [], []
+    t_end = time.perf_counter() + cfg["seconds"]
+    for i in range(cfg["rows"]):
+        t0 = time.perf_counter()
+        out = oracle.moe_forward(X[i:i + 1], arr, K_TOP)
+        times.append(time.perf_counter() - t0)
+        outs.append(out[0].tolist())
+        if time.perf_counter() > t_end and i >= 2:
+            break
+    print(json.dumps({"times": times, "outs": outs}))
+
+
+def run_cpu_sample(routing, rows, seconds, threads=1):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    spec = json.dumps({"routing": routing, "rows": rows, "seconds": seconds})
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", spec],
+                       capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr)
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def reference_main(args, rank, world):
+    """The oracle as the reference arm: each step is one row through the layer."""
+    if rank != 0:
+        return
+    from oracle import qmoe_oracle as oracle
+    from quantized_moe_transformer_gb300 import inputs
+    wl = WORKLOADS[args.workload]
+    arr = inputs.moe_layer(0, H, E, F, shared=True, routing=wl["routing"])
+    n = args.warmup + args.steps
+    X = inputs.hidden(1000, n, H, wl["routing"])
+    for i in range(args.warmup):
+        oracle.moe_forward(X[i:i + 1], arr, K_TOP)
+    t0 = time.perf_counter()
+    for i in range(args.warmup, n):
+        oracle.moe_forward(X[i:i + 1], arr, K_TOP)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": workload_config(args.workload, wl["T"], wl["routing"], 1),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"one row per step of the {args.workload} workload "
+                                       f"(numpy fp64 oracle, {cores} cores visible)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class ClockSampler:
+    def __init__(self, index):
+        self.p = None
+        self.index = index
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.summary = None
+        if self.p is None:
+            return
+        time.sleep(0.2)
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if sm:
+            self.summary = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_layer_on_device(torch, seed, routing, device, from_arrays=None):
+    """Layer instance from device RNG (instances 1..N-1) or host arrays (0)."""
+    from quantized_moe_transformer_gb300 import binding as qb
+    if from_arrays is not None:
+        return qb.MoeLayer.from_arrays(from_arrays, K_TOP, device)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+
+    def blocks(n, nb):
+        b = torch.randint(0, 256, (n, nb), dtype=torch.uint8, device=device, generator=g)
+        dd = torch.empty((n, 2), device=device).uniform_(2.0**-12, 2.0**-10, generator=g)
+        b[:, 0:4] = dd.half().view(torch.uint8).reshape(n, 4)
+        return b
+
+    Wr = torch.randn((H, E), device=device, generator=g) * 0.02
+    if routing == "zipf":
+        rank = torch.randperm(E, device=device, generator=g).double()
+        Wr[0] = (-1.1 * torch.log1p(rank)).float()
+    nb = H // 256
+    Wg = blocks(E * F * nb, 144).reshape(E, F, nb, 144)
+    Wu = blocks(E * F * nb, 144).reshape(E, F, nb, 144)
+    Wd = blocks(E * H * (F // 256), 176).reshape(E, H, F // 256, 176)
+    Sg = blocks(F * nb, 144).reshape(F, nb, 144)
+    Su = blocks(F * nb, 144).reshape(F, nb, 144)
+    Sd = blocks(H * (F // 256), 176).reshape(H, F // 256, 176)
+    return qb.MoeLayer(H, E, K_TOP, F, Wr.contiguous(), Wg, Wu, Wd, Sg, Su, Sd, "q4k", "q5k")
+
+
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ours_main(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_moe_transformer_gb300 import binding as qb
+    from quantized_moe_transformer_gb300 import build, inputs
+
+    build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = WORKLOADS[args.workload]
+    T, routing = wl["T"], wl["routing"]
+    NL = args.layers
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peaks = json.load(open(pk))
+
+    arr0 = inputs.moe_layer(0, H, E, F, shared=True, routing=routing)
+    layers = [make_layer_on_device(torch, 1000 * rank + i, routing, device,
+                                   arr0 if i == 0 else None) for i in range(NL)]
+    gX = torch.Generator(device=device)
+    gX.manual_seed(7 + rank)
+    Xs = torch.randn((NL, T, H), device=device, generator=gX)
+    if routing == "zipf":
+        Xs[:, :, 0] = 1.0
+    outs = torch.empty_like(Xs)
+    ws = layers[0].workspace(T)
+    stream = torch.cuda.Stream(device=device)
+
+    def step(i, s=None):
+        qb.moe_forward(layers[i % NL], Xs[i % NL], Xs[i % NL], out=outs[i % NL], ws=ws, stream=s)
+
+    with torch.cuda.stream(stream):
+        n0 = qb.launch_count()
+        step(0, stream)
+        launches_per_step = qb.launch_count() - n0
+        for i in range(max(args.warmup, 3)):
+            step(i, stream)
+    torch.cuda.synchronize()
+    assert qb.query_status(stream) == 0
+    path = qb.last_path()
+
+    # one graph of NL steps and one graph per step
+    macro = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(macro, stream=stream):
+        for i in range(NL):
+            step(i, stream)
+    singles = []
+    for i in range(NL):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            step(i, stream)
+        singles.append(gph)
+    for _ in range(max(1, args.warmup // NL)):
+        macro.replay()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps // NL):
+            macro.replay()
+        for i in range(args.steps % NL):
+            singles[i].replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    value = T * args.steps * world / (ms / 1e3)
+
+    # dominant kernel: grouped gate/up, timed per launch on the launching stream
+    dom = "gateup"
+    prof_steps = 2 * NL
+    U = []
+    L = layers[0].workspace_layout(T)
+    with torch.cuda.stream(stream):
+        qb.profile_start(dom)
+        for i in range(prof_steps):
+            step(i, stream)
+            ids = ws[L.ids:L.ids + 4 * T * K_TOP].view(torch.int32)
+            U.append(int(torch.unique(ids).numel()))
+        dom_ms, dom_n = qb.profile_stop()
+    torch.cuda.synchronize()
+    dom_avg_ms = dom_ms / dom_n
+    # algorithmic bytes of one gate/up launch: each touched expert's packed gate and
+    # up rows once, the rows X read, h written (fp32)
+    u_mean = float(np.mean(U))
+    rows_h = T * K_TOP + T
+    alg_bytes = (u_mean + 1) * GATEUP_EXPERT_BYTES + T * H * 4 + rows_h * F * 4
+    achieved = alg_bytes / (dom_avg_ms / 1e3) / 1e9
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    kernel_sha = source_sha(["quantized_moe_transformer_gb300/csrc/moe_gemv.cu",
+                             "quantized_moe_transformer_gb300/csrc/common.cuh"])
+    if os.path.exists(tf):
+        rec = json.load(open(tf)).get(f"{dom}:{args.workload}")
+        if rec and rec.get("source_sha") == kernel_sha:
+            traffic = rec["dram_bytes_per_launch"]
+    layer_bytes = (u_mean + 1) * EXPERT_BYTES + H * E * 4 + 2 * T * H * 4
+    layer_gbs = layer_bytes / (ms / args.steps / 1e3) / 1e9
+
+    # end to end through the C ABI on host buffers (pinned), copies inside
+    e2e = None
+    if rank == 0 or True:
+        Xh = torch.randn((NL, T, H), generator=torch.Generator().manual_seed(11)).pin_memory()
+        if routing == "zipf":
+            Xh[:, :, 0] = 1.0
+        Oh = torch.empty_like(Xh).pin_memory()
+        hws = torch.empty(qb.host_workspace_bytes(layers[0], T), dtype=torch.uint8, device=device)
+        n_e2e = min(args.steps, 400)
+        for i in range(3):
+            qb.moe_forward_host(layers[i % NL], Xh[i % NL], out=Oh[i % NL], ws=hws, stream=stream)
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            qb.moe_forward_host(layers[i % NL], Xh[i % NL], out=Oh[i % NL], ws=hws, stream=stream)
+        dt = time.perf_counter() - t0
+        e2e = {"value": T * n_e2e * world / dt, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 4,
+               "d2h_bytes_per_step": T * H * 4, "steps": n_e2e,
+               "api": "qmoe_moe_forward_host (pinned host buffers, one call per step)"}
+
+    # CPU baseline and a parity spot check of instance 0 on the same rows
+    cpu = None
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res = run_cpu_sample(routing, 64, args.cpu_seconds, threads=1)
+        n = len(res["times"])
+        cpu = {"value": n / sum(res["times"]), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} single-row forwards of layer instance 0 ({args.workload} shape, "
+                         f"fp64 numpy oracle, 1 thread)"}
+        Xp = torch.from_numpy(inputs.hidden(1000, 64, H, routing)[:n]).to(device)
+        got = np.stack([qb.moe_forward(layers[0], Xp[i:i + 1]).cpu().numpy()[0] for i in range(n)])
+        ref = np.array(res["outs"])
+        parity = {"rows": n, "max_abs_err_over_max_ref": float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))}
+
+    if rank == 0:
+        line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32" if path == "gemv" else "bf16", "data": "synthetic",
+                "config": workload_config(args.workload, T, routing, NL),
+                "path": path,
+                "roofline": {"bound": "hbm", "kernel": "gateup_gemv_kernel", "achieved": achieved,
+                             "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": traffic,
+                             "alg_bytes_per_launch": alg_bytes, "avg_launch_us": dom_avg_ms * 1e3,
+                             "launches_timed": dom_n, "distinct_experts_mean": u_mean},
+                "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / peak,
+                              "alg_bytes_per_step": layer_bytes},
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+                "launches_per_step": launches_per_step, "clocks": clk.summary, "parity": parity}
+        print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.cpu_sample:
+        cpu_sample_main(args.cpu_sample)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_main(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    ours_main(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * qmoe.h -- C ABI of libqmoe.so, a GB300 (sm_103a) library for the k-quant
+ * weight-quantized routed-MoE layer of a Qwen3.5-35B-A3B-shaped transformer
+ * block and for that block.
+ *
+ * Sources (the operations; the pages describe no API):
+ *   [CKE-Zip]  "CKE Zip: From Splitting Tokens To Splitting Qwen3.5 Weights",
+ *              sections "What The First Prototype Split" (hidden rows X [T, H],
+ *              selected top-k expert indices and routing weights, routed and
+ *              shared SwiGLU branches), "What PR #382 Now Splits" (256 routed
+ *              experts, eight per token, Q4_K gate/up and Q5_K down weights,
+ *              the 256/256 intermediate split, 16 query / 2 KV heads, the
+ *              block recombination order) and "A Separate Decode Result Shows
+ *              Why Axis Choice Matters" (routes merged in selected-slot order).
+ *   [CKE-Dist] "Distributed CPU: Zip Fusion Beyond Tensor Parallelism",
+ *              "The Reduction Algebra" and "Streaming reductions" (partials are
+ *              summed in a fixed, declared order).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument except the descriptors is a DEVICE pointer on the
+ *     current CUDA device, owned by the caller. The library allocates nothing
+ *     and frees nothing; scratch lives in the caller's workspace ``ws``.
+ *   - All work is enqueued on ``stream`` (a cudaStream_t; NULL = the legacy
+ *     default stream) with no host synchronisation. Buffers must stay valid
+ *     until that work completes.
+ *   - Row-major, contiguous tensors. fp32 tensors, packed weights and the
+ *     workspace must be 16-byte aligned (the workspace 256-byte aligned).
+ *   - Return value: QMOE_OK or a negative qmoe_status; nothing is enqueued
+ *     when an argument check fails. Errors detected on the device (an expert
+ *     id out of range in caller-supplied routes, a bounded wait that ran out)
+ *     are recorded in a per-device status word read by qmoe_query_status().
+ *   - T = 0 is valid and enqueues nothing.
+ *
+ * Packed super-block formats (256 weights, 8 sub-blocks of 32; the pages name
+ * Q4_K and Q5_K only, so this byte layout is the library's own):
+ *   Q4_K, 144 bytes: [0,2) d fp16; [2,4) dmin fp16; [4,16) sixteen 6-bit
+ *     fields packed little-endian, fields 0..7 the scales s_j, 8..15 the mins
+ *     m_j; [16,144) quants, byte b = weight 2b (low nibble), 2b+1 (high).
+ *   Q5_K, 176 bytes: the same 16-byte header; [16,48) high bits, weight i is
+ *     bit i%8 of byte 16 + i/8; [48,176) low nibbles as in Q4_K.
+ *   Weight i (sub-block j = i/32): w_i = d*s_j*q_i - dmin*m_j, q_i the 4-bit
+ *   quant (Q4_K) or quant + 16*high bit (Q5_K).
+ *   Matrices are stored one output feature per row, super-blocks running
+ *   along the input (reduction) axis: a [rows][cols] matrix with cols % 256
+ *   == 0 is rows * (cols/256) consecutive super-blocks.
+ */
+#ifndef QMOE_H
+#define QMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qmoe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  QMOE_OK = 0,
+  QMOE_ERR_ARG = -1,         /* a size or type argument is out of range      */
+  QMOE_ERR_NULL = -2,        /* a required pointer is NULL                   */
+  QMOE_ERR_ALIGN = -3,       /* a pointer is not 16-byte (workspace 256) aligned */
+  QMOE_ERR_WORKSPACE = -4,   /* ws_bytes is below the queried requirement    */
+  QMOE_ERR_ARCH = -5,        /* the current device is not sm_103             */
+  QMOE_ERR_LAUNCH = -6,      /* a kernel launch failed (cudaGetLastError)    */
+  QMOE_ERR_TIMEOUT = -7,     /* device: a bounded wait ran out               */
+  QMOE_ERR_DEVICE_ARG = -8,  /* device: caller-supplied route out of range   */
+  QMOE_ERR_CUDA = -9         /* another CUDA runtime error                   */
+} qmoe_status;
+
+typedef enum { QMOE_Q4K = 0, QMOE_Q5K = 1 } qmoe_qtype;
+
+/* Execution path the last successful qmoe_moe_forward took on this thread. */
+typedef enum { QMOE_PATH_NONE = 0, QMOE_PATH_GEMV = 1, QMOE_PATH_GEMM_TC = 2 } qmoe_path;
+
+/*
+ * One routed-MoE layer ([CKE-Zip] "What PR #382 Now Splits").
+ *   H  hidden width, multiple of 256;  E routed experts, 1..1024;
+ *   k  experts per row, 1..min(E, 16); F expert intermediate, multiple of 256.
+ *   Wr       fp32 [H][E] router weights (logits = x . Wr).
+ *   Wg, Wu   gate / up, gate_type, [E][F rows][H/256 blocks].
+ *   Wd       down, down_type, [E][H rows][F/256 blocks].
+ *   Sg,Su,Sd the shared expert, same per-expert shapes and types, or all NULL.
+ */
+typedef struct {
+  int H, E, k, F;
+  int gate_type, down_type; /* qmoe_qtype */
+  const float *Wr;
+  const void *Wg, *Wu, *Wd;
+  const void *Sg, *Su, *Sd;
+} qmoe_moe_desc;
+
+/*
+ * Router: logits = X . Wr (fp32), then per row the k largest logits (equal
+ * logits: the lower expert index first), in descending-logit slot order, with
+ * weights w_s = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0), which is the
+ * softmax over all E renormalised over the selected k.
+ * ([CKE-Zip] "What The First Prototype Split": selected top-k indices and
+ * routing weights; "What PR #382 Now Splits": one synchronised router decision.)
+ *   X [T][H] fp32, Wr [H][E] fp32 -> ids [T][k] int32, w [T][k] fp32.
+ *   ws: qmoe_moe_route_workspace_bytes(T, H, E, k) bytes.
+ */
+size_t qmoe_moe_route_workspace_bytes(int T, int H, int E, int k);
+int qmoe_moe_route(const float *X, const float *Wr, int T, int H, int E, int k,
+                   int32_t *ids, float *w, void *ws, size_t ws_bytes,
+                   qmoe_stream_t stream);
+
+/*
+ * The routed-MoE layer on rows X [T][H] fp32:
+ *   out_t = R_t + y_shared,t + sum_{s=0}^{k-1} w_{t,s} * y_{t,s}
+ * with y = down(silu(gate(x)) * up(x)) per selected expert and for the shared
+ * expert (weight 1, no gate), the slot sum taken in slot order s = 0..k-1
+ * without atomics, so the result is run-to-run bit-identical.
+ * ([CKE-Zip] "What The First Prototype Split", "What PR #382 Now Splits",
+ * "A Separate Decode Result Shows Why Axis Choice Matters".)
+ *   R    [T][H] fp32 residual, or NULL for none (R may equal out).
+ *   ids, w  [T][k] int32 / fp32 precomputed routes (e.g. one synchronised
+ *        decision shared by two rank partials), or both NULL to route X here.
+ *   out  [T][H] fp32; may alias R but not X.
+ *   ws   qmoe_moe_workspace_bytes(d, T) bytes, 256-byte aligned.
+ * Small T takes the dequant-fused grouped GEMV path (fp32 accumulation);
+ * large T the grouped dequant + bf16 tcgen05 GEMM path (fp32 accumulation in
+ * tensor memory); qmoe_last_path() tells which ran.
+ * A rank partial of the intermediate split is computed by passing that
+ * rank's slices of the packed tensors with F halved.
+ */
+size_t qmoe_moe_workspace_bytes(const qmoe_moe_desc *d, int T);
+int qmoe_moe_forward(const qmoe_moe_desc *d, const float *X, const float *R,
+                     const int32_t *ids, const float *w, float *out, int T,
+                     void *ws, size_t ws_bytes, qmoe_stream_t stream);
+
+/* Path selection threshold: rows above it take the tensor-core path.
+ * qmoe_set_gemm_threshold(-1) restores the built-in value. */
+int qmoe_get_gemm_threshold(void);
+void qmoe_set_gemm_threshold(int rows);
+int qmoe_last_path(void);
+
+/*
+ * Byte offsets of the intermediates inside a moe_forward workspace, for
+ * stagewise checks: ids [T][k] int32, w [T][k] fp32, offsets [E+2] int32
+ * (row ranges per expert, the shared expert last), perm [T*k + T] int32 (pair
+ * index t*k+s grouped by expert, stable), y [T*k + T][H] fp32 (per pair,
+ * shared rows last). Valid after the forward has completed.
+ */
+typedef struct {
+  size_t ids, w, offsets, perm, y;
+} qmoe_moe_ws_layout;
+int qmoe_moe_workspace_layout(const qmoe_moe_desc *d, int T, qmoe_moe_ws_layout *out);
+
+/*
+ * End-to-end variant of qmoe_moe_forward on HOST buffers: copies X_host (and
+ * R_host, if not NULL) into the workspace, runs the layer on ``stream``,
+ * copies the result to out_host and waits for the stream. X_host, R_host and
+ * out_host are [T][H] fp32 host arrays (pinned memory makes the copies
+ * asynchronous DMA; pageable memory works too). ws is a DEVICE workspace of
+ * qmoe_moe_forward_host_workspace_bytes(d, T) bytes. Routing is internal.
+ */
+size_t qmoe_moe_forward_host_workspace_bytes(const qmoe_moe_desc *d, int T);
+int qmoe_moe_forward_host(const qmoe_moe_desc *d, const float *X_host, const float *R_host,
+                          float *out_host, int T, void *ws, size_t ws_bytes,
+                          qmoe_stream_t stream);
+
+/* Number of kernels this library has enqueued since it was loaded (a CUDA
+ * graph replay of captured launches does not add to it). */
+long long qmoe_launch_count(void);
+
+/*
+ * Stage timing. After qmoe_profile_start(stage), every launch of that stage
+ * by this thread (outside stream capture) is bracketed with a pair of CUDA
+ * events on its stream, up to 4096 launches; qmoe_profile_stop waits for them
+ * and returns the summed kernel time in milliseconds and the launch count.
+ * stage 0 turns profiling off. Do not profile while a stream is capturing.
+ */
+typedef enum {
+  QMOE_STAGE_ROUTER = 1,  /* router logits                          */
+  QMOE_STAGE_ROUTE = 2,   /* top-k, histogram, scan, permutation    */
+  QMOE_STAGE_GATEUP = 3,  /* grouped gate/up + SwiGLU               */
+  QMOE_STAGE_DOWN = 4,    /* grouped down projection                */
+  QMOE_STAGE_COMBINE = 5  /* slot-order combine + shared + residual */
+} qmoe_stage;
+int qmoe_profile_start(int stage);
+int qmoe_profile_stop(double *total_ms, int *launches);
+
+/* Human-readable text of a status code (static storage). */
+const char *qmoe_status_str(int status);
+
+/* Waits for ``stream``, then returns and clears the device status word of the
+ * current device (QMOE_OK if no kernel recorded an error). */
+int qmoe_query_status(qmoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMOE_H */

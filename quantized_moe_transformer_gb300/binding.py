@@ -1,0 +1,232 @@
+"""Thin ctypes binding of libqmoe.so (argument marshalling only).
+
+Every step of the layer runs in the library's CUDA kernels; PyTorch supplies
+device memory and the current stream. There is no fallback: if the library is
+missing or the device is not a GB300, the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqmoe.so")
+
+Q4K, Q5K = 0, 1
+QTYPE = {"q4k": Q4K, "q5k": Q5K}
+PATH_NAMES = {0: "none", 1: "gemv", 2: "gemm_tc"}
+
+_c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+
+
+class MoeDesc(ctypes.Structure):
+    _fields_ = [("H", _c_int), ("E", _c_int), ("k", _c_int), ("F", _c_int),
+                ("gate_type", _c_int), ("down_type", _c_int),
+                ("Wr", _vp), ("Wg", _vp), ("Wu", _vp), ("Wd", _vp),
+                ("Sg", _vp), ("Su", _vp), ("Sd", _vp)]
+
+
+class MoeWsLayout(ctypes.Structure):
+    _fields_ = [("ids", _c_size), ("w", _c_size), ("offsets", _c_size), ("perm", _c_size),
+                ("y", _c_size)]
+
+
+class QmoeError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libqmoe.so (built in-tree by ``quantized_moe_transformer_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise QmoeError(f"{LIB_PATH} is not built; run quantized_moe_transformer_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER
+        L.qmoe_status_str.restype = ctypes.c_char_p
+        L.qmoe_status_str.argtypes = [_c_int]
+        L.qmoe_query_status.argtypes = [_vp]
+        L.qmoe_get_gemm_threshold.argtypes = []
+        L.qmoe_set_gemm_threshold.argtypes = [_c_int]
+        L.qmoe_set_gemm_threshold.restype = None
+        L.qmoe_last_path.argtypes = []
+        L.qmoe_moe_route_workspace_bytes.restype = _c_size
+        L.qmoe_moe_route_workspace_bytes.argtypes = [_c_int] * 4
+        L.qmoe_moe_route.argtypes = [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
+                                     _c_size, _vp]
+        L.qmoe_moe_workspace_bytes.restype = _c_size
+        L.qmoe_moe_workspace_bytes.argtypes = [P(MoeDesc), _c_int]
+        L.qmoe_moe_workspace_layout.argtypes = [P(MoeDesc), _c_int, P(MoeWsLayout)]
+        L.qmoe_moe_forward.argtypes = [P(MoeDesc), _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_size,
+                                       _vp]
+        L.qmoe_moe_forward_host_workspace_bytes.restype = _c_size
+        L.qmoe_moe_forward_host_workspace_bytes.argtypes = [P(MoeDesc), _c_int]
+        L.qmoe_moe_forward_host.argtypes = [P(MoeDesc), _vp, _vp, _vp, _c_int, _vp, _c_size, _vp]
+        L.qmoe_launch_count.restype = ctypes.c_longlong
+        L.qmoe_launch_count.argtypes = []
+        L.qmoe_profile_start.argtypes = [_c_int]
+        L.qmoe_profile_stop.argtypes = [P(ctypes.c_double), P(_c_int)]
+        _lib = L
+    return _lib
+
+
+def exported_symbols() -> list[str]:
+    """Names of the entry points include/qmoe.h declares."""
+    return ["qmoe_status_str", "qmoe_query_status", "qmoe_get_gemm_threshold",
+            "qmoe_set_gemm_threshold", "qmoe_last_path", "qmoe_moe_route_workspace_bytes",
+            "qmoe_moe_route", "qmoe_moe_workspace_bytes", "qmoe_moe_workspace_layout",
+            "qmoe_moe_forward", "qmoe_moe_forward_host_workspace_bytes", "qmoe_moe_forward_host",
+            "qmoe_launch_count", "qmoe_profile_start", "qmoe_profile_stop"]
+
+
+def _check(status: int):
+    if status != 0:
+        raise QmoeError(f"qmoe status {status}: {lib().qmoe_status_str(status).decode()}")
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise QmoeError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise QmoeError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class MoeLayer:
+    """Device-resident weights of one routed-MoE layer plus its descriptor."""
+
+    def __init__(self, H, E, k, F, Wr, Wg, Wu, Wd, Sg=None, Su=None, Sd=None,
+                 gate_type="q4k", down_type="q5k"):
+        self.H, self.E, self.k, self.F = H, E, k, F
+        self.gate_type, self.down_type = gate_type, down_type
+        self.Wr, self.Wg, self.Wu, self.Wd = Wr, Wg, Wu, Wd
+        self.Sg, self.Su, self.Sd = Sg, Su, Sd
+        self._desc = MoeDesc(H, E, k, F, QTYPE[gate_type], QTYPE[down_type],
+                             _ptr(Wr), _ptr(Wg), _ptr(Wu), _ptr(Wd),
+                             _ptr(Sg), _ptr(Su), _ptr(Sd))
+
+    @classmethod
+    def from_arrays(cls, layer: dict, k: int, device="cuda"):
+        """From the numpy dict of ``inputs.moe_layer``."""
+        dev = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        return cls(layer["H"], layer["E"], k, layer["F"], dev(layer["Wr"]), dev(layer["Wg"]),
+                   dev(layer["Wu"]), dev(layer["Wd"]), dev(layer.get("Sg")), dev(layer.get("Su")),
+                   dev(layer.get("Sd")), layer["gate_type"], layer["down_type"])
+
+    @property
+    def desc(self) -> MoeDesc:
+        return self._desc
+
+    def workspace_bytes(self, T: int) -> int:
+        return int(lib().qmoe_moe_workspace_bytes(ctypes.byref(self._desc), T))
+
+    def workspace_layout(self, T: int) -> MoeWsLayout:
+        out = MoeWsLayout()
+        _check(lib().qmoe_moe_workspace_layout(ctypes.byref(self._desc), T, ctypes.byref(out)))
+        return out
+
+    def workspace(self, T: int) -> torch.Tensor:
+        return torch.empty(max(self.workspace_bytes(T), 256), dtype=torch.uint8,
+                           device=self.Wr.device)
+
+
+def moe_route(X: torch.Tensor, Wr: torch.Tensor, k: int, ws: torch.Tensor | None = None,
+              stream=None):
+    """ids [T,k] int32 and w [T,k] fp32 of rows X [T,H] under router Wr [H,E]."""
+    T, H = X.shape
+    E = Wr.shape[1]
+    ids = torch.empty((T, k), dtype=torch.int32, device=X.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=X.device)
+    need = int(lib().qmoe_moe_route_workspace_bytes(T, H, E, k))
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=X.device)
+    _check(lib().qmoe_moe_route(_ptr(X), _ptr(Wr), T, H, E, k, _ptr(ids), _ptr(w), _ptr(ws),
+                                ws.numel(), _stream(stream)))
+    return ids, w
+
+
+def moe_forward(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = None,
+                ids: torch.Tensor | None = None, w: torch.Tensor | None = None,
+                out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """out = R + shared(X) + sum_s w_s expert_{ids_s}(X), enqueued on ``stream``."""
+    T = X.shape[0]
+    if out is None:
+        out = torch.empty_like(X)
+    if ws is None:
+        ws = layer.workspace(T)
+    _check(lib().qmoe_moe_forward(ctypes.byref(layer.desc), _ptr(X), _ptr(R), _ptr(ids), _ptr(w),
+                                  _ptr(out), T, _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def query_status(stream=None) -> int:
+    return int(lib().qmoe_query_status(_stream(stream)))
+
+
+def last_path() -> str:
+    return PATH_NAMES[int(lib().qmoe_last_path())]
+
+
+def set_gemm_threshold(rows: int):
+    lib().qmoe_set_gemm_threshold(int(rows))
+
+
+def get_gemm_threshold() -> int:
+    return int(lib().qmoe_get_gemm_threshold())
+
+
+STAGES = {"router": 1, "route": 2, "gateup": 3, "down": 4, "combine": 5}
+
+
+def moe_forward_host(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """The layer on HOST tensors (pinned for asynchronous copies): the library
+    copies X (and R) in, runs the layer and copies the result back, then waits."""
+    if X.is_cuda:
+        raise QmoeError("moe_forward_host takes host tensors")
+    T = X.shape[0]
+    if out is None:
+        out = torch.empty_like(X)
+    if ws is None:
+        n = int(lib().qmoe_moe_forward_host_workspace_bytes(ctypes.byref(layer.desc), T))
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=layer.Wr.device)
+    hp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    _check(lib().qmoe_moe_forward_host(ctypes.byref(layer.desc), hp(X), hp(R), hp(out), T,
+                                       _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def host_workspace_bytes(layer: MoeLayer, T: int) -> int:
+    return int(lib().qmoe_moe_forward_host_workspace_bytes(ctypes.byref(layer.desc), T))
+
+
+def launch_count() -> int:
+    return int(lib().qmoe_launch_count())
+
+
+def profile_start(stage: str):
+    _check(lib().qmoe_profile_start(STAGES[stage]))
+
+
+def profile_stop():
+    """(summed kernel milliseconds, launches) of the profiled stage."""
+    ms = ctypes.c_double()
+    n = _c_int()
+    _check(lib().qmoe_profile_stop(ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value

@@ -1,0 +1,376 @@
+// C ABI of libqmoe.so: argument checks, workspace carving and launch order.
+// The operations are defined in include/qmoe.h.
+#include <atomic>
+#include <climits>
+#include <cstdio>
+
+#include "kernels.cuh"
+
+using namespace qmoe;
+
+namespace {
+
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_arch_ok[kMaxDevices];     // 0 unknown, 1 sm_103, -1 other
+std::atomic<int*> g_status_ptr[kMaxDevices];
+std::atomic<int> g_gemm_threshold{INT_MAX};
+thread_local int g_last_path = QMOE_PATH_NONE;
+std::atomic<long long> g_launches{0};
+
+// Opt-in per-stage timing: events recorded around every launch of one stage.
+constexpr int kProfCap = 4096;
+struct StageProfile {
+  int stage = 0;
+  int n = 0;
+  cudaEvent_t start[kProfCap];
+  cudaEvent_t stop[kProfCap];
+  int created = 0;
+};
+thread_local StageProfile g_prof;
+
+// Runs ``launch`` (a kernel launch on ``st``), counting it and, when its stage
+// is being profiled, bracketing it with a pair of events.
+template <typename F>
+cudaError_t staged(int stage, int n_kernels, cudaStream_t st, F&& launch) {
+  const bool prof = g_prof.stage == stage && g_prof.n < kProfCap;
+  if (prof) {
+    if (g_prof.n >= g_prof.created) {
+      if (cudaEventCreate(&g_prof.start[g_prof.n]) != cudaSuccess ||
+          cudaEventCreate(&g_prof.stop[g_prof.n]) != cudaSuccess)
+        return cudaErrorMemoryAllocation;
+      g_prof.created = g_prof.n + 1;
+    }
+    cudaEventRecord(g_prof.start[g_prof.n], st);
+  }
+  cudaError_t e = launch();
+  g_launches.fetch_add(n_kernels);
+  if (prof) {
+    cudaEventRecord(g_prof.stop[g_prof.n], st);
+    ++g_prof.n;
+  }
+  return e;
+}
+
+// Checks the current device once (sm_103) and finds the status word's address.
+int device_ready(int** status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMOE_ERR_CUDA;
+  int ok = g_arch_ok[dev].load();
+  if (ok == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return QMOE_ERR_CUDA;
+    ok = (major == 10 && minor == 3) ? 1 : -1;
+    g_arch_ok[dev].store(ok);
+  }
+  if (ok != 1) return QMOE_ERR_ARCH;
+  int* p = g_status_ptr[dev].load();
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status_word) != cudaSuccess)
+      return QMOE_ERR_CUDA;
+    g_status_ptr[dev].store(p);
+  }
+  *status = p;
+  return QMOE_OK;
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace carve-up (every piece 256-byte aligned).
+struct MoeWs {
+  size_t part, ids, w, offsets, perm, active, n_active, chunk, h, y, total;
+  int nsplit;
+};
+
+MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
+  MoeWs L{};
+  const size_t P = (size_t)T * k, rows = P + T;
+  L.nsplit = router_splits(T, H, E);
+  size_t o = 0;
+  L.part = o;     o += up256(sizeof(float) * (size_t)L.nsplit * T * E);
+  L.ids = o;      o += up256(sizeof(int32_t) * P);
+  L.w = o;        o += up256(sizeof(float) * P);
+  L.offsets = o;  o += up256(sizeof(int32_t) * (E + 2));
+  L.perm = o;     o += up256(sizeof(int32_t) * rows);
+  L.active = o;   o += up256(sizeof(int32_t) * (E + 1));
+  L.n_active = o; o += 256;
+  L.chunk = o;    o += up256(sizeof(int32_t) * (size_t)perm_chunks((int)P) * E);
+  L.h = o;        o += up256(sizeof(float) * rows * F);
+  L.y = o;        o += up256(sizeof(float) * rows * H);
+  L.total = o;
+  return L;
+}
+
+bool supported_width(int n) { return n == 256 || n == 512 || n == 1024 || n == 2048 || n == 4096; }
+
+int check_desc(const qmoe_moe_desc* d) {
+  if (!d) return QMOE_ERR_NULL;
+  if (!supported_width(d->H) || !supported_width(d->F)) return QMOE_ERR_ARG;
+  if (d->E < 1 || d->E > 1024 || d->k < 1 || d->k > 16 || d->k > d->E) return QMOE_ERR_ARG;
+  if ((d->gate_type != QMOE_Q4K && d->gate_type != QMOE_Q5K) ||
+      (d->down_type != QMOE_Q4K && d->down_type != QMOE_Q5K))
+    return QMOE_ERR_ARG;
+  if (!d->Wr || !d->Wg || !d->Wu || !d->Wd) return QMOE_ERR_NULL;
+  const bool any_shared = d->Sg || d->Su || d->Sd;
+  const bool all_shared = d->Sg && d->Su && d->Sd;
+  if (any_shared && !all_shared) return QMOE_ERR_NULL;
+  const void* ptrs[] = {d->Wr, d->Wg, d->Wu, d->Wd, d->Sg, d->Su, d->Sd};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return QMOE_ERR_ALIGN;
+  return QMOE_OK;
+}
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? QMOE_OK : QMOE_ERR_LAUNCH; }
+
+}  // namespace
+
+extern "C" {
+
+const char* qmoe_status_str(int s) {
+  switch (s) {
+    case QMOE_OK: return "ok";
+    case QMOE_ERR_ARG: return "argument out of range";
+    case QMOE_ERR_NULL: return "required pointer is NULL";
+    case QMOE_ERR_ALIGN: return "pointer not aligned (16 B; workspace 256 B)";
+    case QMOE_ERR_WORKSPACE: return "workspace too small";
+    case QMOE_ERR_ARCH: return "current device is not sm_103 (GB300)";
+    case QMOE_ERR_LAUNCH: return "kernel launch failed";
+    case QMOE_ERR_TIMEOUT: return "device wait timed out";
+    case QMOE_ERR_DEVICE_ARG: return "device: route id out of range";
+    case QMOE_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+int qmoe_query_status(qmoe_stream_t stream) {
+  int* p = nullptr;
+  int r = device_ready(&p);
+  if (r != QMOE_OK) return r;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return QMOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QMOE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return QMOE_ERR_CUDA;
+  return v;
+}
+
+int qmoe_get_gemm_threshold(void) { return g_gemm_threshold.load(); }
+void qmoe_set_gemm_threshold(int rows) { g_gemm_threshold.store(rows < 0 ? INT_MAX : rows); }
+int qmoe_last_path(void) { return g_last_path; }
+
+size_t qmoe_moe_route_workspace_bytes(int T, int H, int E, int k) {
+  (void)k;
+  if (T <= 0 || H <= 0 || E <= 0) return 0;
+  return up256(sizeof(float) * (size_t)router_splits(T, H, E) * T * E);
+}
+
+int qmoe_moe_route(const float* X, const float* Wr, int T, int H, int E, int k, int32_t* ids,
+                   float* w, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+  if (T < 0 || !supported_width(H) || E < 1 || E > 1024 || k < 1 || k > 16 || k > E)
+    return QMOE_ERR_ARG;
+  if (T == 0) return QMOE_OK;
+  if (!X || !Wr || !ids || !w || !ws) return QMOE_ERR_NULL;
+  if (!aligned(X, 16) || !aligned(Wr, 16) || !aligned(ws, 256)) return QMOE_ERR_ALIGN;
+  if (ws_bytes < qmoe_moe_route_workspace_bytes(T, H, E, k)) return QMOE_ERR_WORKSPACE;
+  int* status = nullptr;
+  int r = device_ready(&status);
+  if (r != QMOE_OK) return r;
+  const int ns = router_splits(T, H, E);
+  float* part = static_cast<float*>(ws);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = staged(QMOE_STAGE_ROUTER, 1, st,
+                         [&] { return launch_router_logits(X, Wr, part, T, H, E, ns, st); });
+  if (e == cudaSuccess)
+    e = staged(QMOE_STAGE_ROUTE, 1, st, [&] { return launch_topk(part, ns, T, E, k, ids, w, st); });
+  return launch_status(e);
+}
+
+size_t qmoe_moe_workspace_bytes(const qmoe_moe_desc* d, int T) {
+  if (check_desc(d) != QMOE_OK || T < 0) return 0;
+  if (T == 0) return 0;
+  return moe_ws_layout(T, d->H, d->E, d->k, d->F).total;
+}
+
+int qmoe_moe_workspace_layout(const qmoe_moe_desc* d, int T, qmoe_moe_ws_layout* out) {
+  int r = check_desc(d);
+  if (r != QMOE_OK) return r;
+  if (!out) return QMOE_ERR_NULL;
+  if (T < 0) return QMOE_ERR_ARG;
+  MoeWs L = moe_ws_layout(T, d->H, d->E, d->k, d->F);
+  out->ids = L.ids;
+  out->w = L.w;
+  out->offsets = L.offsets;
+  out->perm = L.perm;
+  out->y = L.y;
+  return QMOE_OK;
+}
+
+int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, const int32_t* ids,
+                     const float* w, float* out, int T, void* ws, size_t ws_bytes,
+                     qmoe_stream_t stream) {
+  int r = check_desc(d);
+  if (r != QMOE_OK) return r;
+  if (T < 0) return QMOE_ERR_ARG;
+  if ((ids == nullptr) != (w == nullptr)) return QMOE_ERR_NULL;
+  if (T == 0) {
+    g_last_path = QMOE_PATH_NONE;
+    return QMOE_OK;
+  }
+  if (!X || !out || !ws) return QMOE_ERR_NULL;
+  if (!aligned(X, 16) || !aligned(out, 16) || (R && !aligned(R, 16)) || !aligned(ws, 256) ||
+      (ids && !aligned(ids, 4)) || (w && !aligned(w, 4)))
+    return QMOE_ERR_ALIGN;
+  if (X == out) return QMOE_ERR_ARG;
+  const int H = d->H, E = d->E, k = d->k, F = d->F;
+  const MoeWs L = moe_ws_layout(T, H, E, k, F);
+  if (ws_bytes < L.total) return QMOE_ERR_WORKSPACE;
+  int* status = nullptr;
+  r = device_ready(&status);
+  if (r != QMOE_OK) return r;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  float* part = reinterpret_cast<float*>(base + L.part);
+  int32_t* ws_ids = reinterpret_cast<int32_t*>(base + L.ids);
+  float* ws_w = reinterpret_cast<float*>(base + L.w);
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+  int32_t* active = reinterpret_cast<int32_t*>(base + L.active);
+  int32_t* n_active = reinterpret_cast<int32_t*>(base + L.n_active);
+  int32_t* chunk = reinterpret_cast<int32_t*>(base + L.chunk);
+  float* hbuf = reinterpret_cast<float*>(base + L.h);
+  float* y = reinterpret_cast<float*>(base + L.y);
+  const int has_shared = d->Sg != nullptr;
+  const int P = T * k;
+
+  cudaError_t e = cudaSuccess;
+  const bool small = P <= 2048;
+  if (ids == nullptr) {
+    e = staged(QMOE_STAGE_ROUTER, 1, st,
+               [&] { return launch_router_logits(X, d->Wr, part, T, H, E, L.nsplit, st); });
+    if (e == cudaSuccess) {
+      if (small) {
+        e = staged(QMOE_STAGE_ROUTE, 1, st, [&] {
+          return launch_route_small(part, L.nsplit, nullptr, T, E, k, has_shared, ws_ids, ws_w,
+                                    offsets, perm, active, n_active, status, st);
+        });
+      } else {
+        e = staged(QMOE_STAGE_ROUTE, 4, st, [&] {
+          cudaError_t e2 = launch_topk(part, L.nsplit, T, E, k, ws_ids, ws_w, st);
+          if (e2 != cudaSuccess) return e2;
+          return launch_perm_large(ws_ids, T, E, k, has_shared, chunk, offsets, perm, active,
+                                   n_active, status, st);
+        });
+      }
+    }
+  } else {
+    if (small)
+      e = staged(QMOE_STAGE_ROUTE, 1, st, [&] {
+        return launch_route_small(nullptr, 0, ids, T, E, k, has_shared, ws_ids, ws_w, offsets,
+                                  perm, active, n_active, status, st);
+      });
+    else
+      e = staged(QMOE_STAGE_ROUTE, 3, st, [&] {
+        return launch_perm_large(ids, T, E, k, has_shared, chunk, offsets, perm, active,
+                                 n_active, status, st);
+      });
+  }
+  if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+  const float* w_use = ids ? w : ws_w;
+
+  GroupedArgs g;
+  g.offsets = offsets;
+  g.perm = perm;
+  g.active = active;
+  g.n_active = n_active;
+  g.T = T;
+  g.k = k;
+  g.E = E;
+  g.max_active = (P < E ? P : E) + has_shared;
+
+  g.W = static_cast<const uint8_t*>(d->Wg);
+  g.S = static_cast<const uint8_t*>(d->Sg);
+  e = staged(QMOE_STAGE_GATEUP, 1, st, [&] {
+    return launch_gateup_gemv(g, static_cast<const uint8_t*>(d->Wu),
+                              static_cast<const uint8_t*>(d->Su), d->gate_type, X, H, F, hbuf, st);
+  });
+  if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+  g.W = static_cast<const uint8_t*>(d->Wd);
+  g.S = static_cast<const uint8_t*>(d->Sd);
+  e = staged(QMOE_STAGE_DOWN, 1, st,
+             [&] { return launch_down_gemv(g, d->down_type, hbuf, F, H, y, st); });
+  if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+  e = staged(QMOE_STAGE_COMBINE, 1, st,
+             [&] { return launch_combine(y, w_use, R, out, T, H, k, has_shared, st); });
+  if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+  g_last_path = QMOE_PATH_GEMV;
+  return QMOE_OK;
+}
+
+size_t qmoe_moe_forward_host_workspace_bytes(const qmoe_moe_desc* d, int T) {
+  const size_t base = qmoe_moe_workspace_bytes(d, T);
+  if (base == 0) return 0;
+  return base + 3 * up256(sizeof(float) * (size_t)T * d->H);
+}
+
+int qmoe_moe_forward_host(const qmoe_moe_desc* d, const float* X_host, const float* R_host,
+                          float* out_host, int T, void* ws, size_t ws_bytes,
+                          qmoe_stream_t stream) {
+  int r = check_desc(d);
+  if (r != QMOE_OK) return r;
+  if (T < 0) return QMOE_ERR_ARG;
+  if (T == 0) return QMOE_OK;
+  if (!X_host || !out_host || !ws) return QMOE_ERR_NULL;
+  if (!aligned(ws, 256)) return QMOE_ERR_ALIGN;
+  const size_t base = qmoe_moe_workspace_bytes(d, T);
+  const size_t rows = up256(sizeof(float) * (size_t)T * d->H);
+  if (ws_bytes < base + 3 * rows) return QMOE_ERR_WORKSPACE;
+  char* p = static_cast<char*>(ws);
+  float* Xd = reinterpret_cast<float*>(p + base);
+  float* Rd = R_host ? reinterpret_cast<float*>(p + base + rows) : nullptr;
+  float* Od = reinterpret_cast<float*>(p + base + 2 * rows);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t nbytes = sizeof(float) * (size_t)T * d->H;
+  if (cudaMemcpyAsync(Xd, X_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return QMOE_ERR_CUDA;
+  if (R_host && cudaMemcpyAsync(Rd, R_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return QMOE_ERR_CUDA;
+  r = qmoe_moe_forward(d, Xd, Rd, nullptr, nullptr, Od, T, ws, base, stream);
+  if (r != QMOE_OK) return r;
+  if (cudaMemcpyAsync(out_host, Od, nbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return QMOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QMOE_ERR_CUDA;
+  return QMOE_OK;
+}
+
+long long qmoe_launch_count(void) { return g_launches.load(); }
+
+int qmoe_profile_start(int stage) {
+  if (stage < 0 || stage > QMOE_STAGE_COMBINE) return QMOE_ERR_ARG;
+  g_prof.stage = stage;
+  g_prof.n = 0;
+  return QMOE_OK;
+}
+
+int qmoe_profile_stop(double* total_ms, int* launches) {
+  if (!total_ms || !launches) return QMOE_ERR_NULL;
+  double tot = 0.0;
+  for (int i = 0; i < g_prof.n; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.stop[i]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.start[i], g_prof.stop[i]) != cudaSuccess)
+      return QMOE_ERR_CUDA;
+    tot += ms;
+  }
+  *total_ms = tot;
+  *launches = g_prof.n;
+  g_prof.stage = 0;
+  g_prof.n = 0;
+  return QMOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// Shared device helpers for the k-quant MoE kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qmoe.h"
+
+namespace qmoe {
+
+constexpr int QK = 256;          // weights per super-block
+constexpr int SUBK = 32;         // weights per sub-block
+constexpr int Q4K_BYTES = 144;
+constexpr int Q5K_BYTES = 176;
+
+__host__ __device__ inline int qtype_bytes(int qt) { return qt == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES; }
+
+// One super-block header: d, dmin and the sixteen 6-bit fields. The header is
+// the first 16 bytes of both formats, loaded as one 16-byte vector.
+struct KHeader {
+  float d, dmin;
+  uint32_t f0, f1, f2;  // bytes 4..15 as three little-endian words
+};
+
+__device__ __forceinline__ KHeader load_header(const uint8_t* blk) {
+  uint4 v = __ldg(reinterpret_cast<const uint4*>(blk));
+  KHeader h;
+  __half2 dd = *reinterpret_cast<const __half2*>(&v.x);
+  float2 f = __half22float2(dd);
+  h.d = f.x;
+  h.dmin = f.y;
+  h.f0 = v.y;
+  h.f1 = v.z;
+  h.f2 = v.w;
+  return h;
+}
+
+// 6-bit field f (0..15) of the 96-bit little-endian field stream.
+__device__ __forceinline__ uint32_t field6(const KHeader& h, int f) {
+  const int p = 6 * f;
+  const uint32_t lo = p < 32 ? h.f0 : (p < 64 ? h.f1 : h.f2);
+  const uint32_t hi = p < 32 ? h.f1 : (p < 64 ? h.f2 : 0u);
+  return __funnelshift_r(lo, hi, p & 31) & 63u;
+}
+
+// Sub-block j's effective scale d*s_j and offset dmin*m_j.
+__device__ __forceinline__ float2 sub_scale(const KHeader& h, int j) {
+  return make_float2(h.d * (float)field6(h, j), h.dmin * (float)field6(h, 8 + j));
+}
+
+// Byte offset of sub-block j's 16 quant bytes inside a super-block.
+__host__ __device__ constexpr int quant_offset(int qt, int j) {
+  return (qt == QMOE_Q5K ? 48 : 16) + 16 * j;
+}
+
+// Sum over the 32 weights of one sub-block of q_i * x_i, where the quants are
+// the 16 bytes ``qv`` (weight 2b low nibble, 2b+1 high nibble of byte b) plus,
+// for Q5_K, 16 times bit i of ``hb``.
+template <int QT>
+__device__ __forceinline__ float dot_sub(const uint4 qv, uint32_t hb, const float* x) {
+  const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int i = 8 * n + b;  // weight index within the sub-block
+      uint32_t q = (w[n] >> (4 * b)) & 15u;
+      if (QT == QMOE_Q5K) q |= ((hb >> i) & 1u) << 4;
+      acc = fmaf((float)q, x[i], acc);
+    }
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g / (1.f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace qmoe

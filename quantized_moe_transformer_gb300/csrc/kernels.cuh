@@ -1,0 +1,42 @@
+// Launchers of the library's kernels (host side), one translation unit each.
+#pragma once
+
+#include "common.cuh"
+
+namespace qmoe {
+
+// router.cu
+int router_splits(int T, int H, int E);
+cudaError_t launch_router_logits(const float* X, const float* Wr, float* part, int T, int H, int E,
+                                 int nsplit, cudaStream_t st);
+cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k, int32_t* ids, float* w,
+                        cudaStream_t st);
+size_t route_small_smem(int T, int E, int k);
+cudaError_t launch_route_small(const float* part, int nsplit, const int32_t* ids_in, int T, int E,
+                               int k, int has_shared, int32_t* ids, float* w, int32_t* offsets,
+                               int32_t* perm, int32_t* active, int32_t* n_active, int* status,
+                               cudaStream_t st);
+int perm_chunks(int P);
+cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_shared,
+                              int32_t* chunk_cnt, int32_t* offsets, int32_t* perm,
+                              int32_t* active, int32_t* n_active, int* status, cudaStream_t st);
+
+// moe_gemv.cu: grouped dequant-fused GEMV kernels and the combine.
+struct GroupedArgs {
+  const uint8_t* W;        // routed experts, [E][rows][cols/256] super-blocks
+  const uint8_t* S;        // shared expert (expert index E) or nullptr
+  const int32_t* offsets;  // [E+2]
+  const int32_t* perm;     // [T*k + T]
+  const int32_t* active;   // [E+1]
+  const int32_t* n_active; // [1]
+  int T, k, E;
+  int max_active;          // grid bound on the active-expert count
+};
+cudaError_t launch_gateup_gemv(const GroupedArgs& g, const uint8_t* Wu, const uint8_t* Su, int qt,
+                               const float* X, int H, int F, float* hbuf, cudaStream_t st);
+cudaError_t launch_down_gemv(const GroupedArgs& g, int qt, const float* hbuf, int F, int H,
+                             float* y, cudaStream_t st);
+cudaError_t launch_combine(const float* y, const float* w, const float* R, float* out, int T,
+                           int H, int k, int has_shared, cudaStream_t st);
+
+}  // namespace qmoe

@@ -1,0 +1,419 @@
+// Router and token-to-expert permutation.
+//
+// "CKE Zip: From Splitting Tokens To Splitting Qwen3.5 Weights", "What The
+// First Prototype Split": every row carries its selected top-k expert indices
+// and routing weights; "A Separate Decode Result Shows Why Axis Choice
+// Matters": the selected routes are independent work items whose outputs are
+// merged in slot order. Here the routes are grouped by expert with a histogram
+// and an exclusive prefix scan so that each expert's packed weights are read
+// once for all the rows that selected it.
+#include "kernels.cuh"
+
+namespace qmoe {
+
+// ---------------------------------------------------------------------------
+// Router logits, split along H: part[s][t][e] = sum_{h in slice s} X[t][h] Wr[h][e].
+// Tile: 32 rows x 64 experts per CTA, 256 threads, each thread 2 rows x 4
+// experts, K staged through shared memory in chunks of 32.
+// ---------------------------------------------------------------------------
+constexpr int RL_BT = 32, RL_BE = 64, RL_BK = 32;
+
+__global__ void __launch_bounds__(256) router_logits_kernel(const float* __restrict__ X,
+                                                            const float* __restrict__ Wr,
+                                                            float* __restrict__ part, int T, int H,
+                                                            int E, int h_per_split) {
+  __shared__ float xs[RL_BK][RL_BT + 1];
+  __shared__ __align__(16) float ws[RL_BK][RL_BE];
+  const int t0 = blockIdx.y * RL_BT, e0 = blockIdx.x * RL_BE;
+  const int hs0 = blockIdx.z * h_per_split;
+  const int tid = threadIdx.x;
+  const int ty = tid / 16, tx = tid % 16;
+  float acc[2][4] = {};
+  for (int hk = hs0; hk < hs0 + h_per_split; hk += RL_BK) {
+    // X tile: 32 rows x 32 h (transposed into xs[h][t])
+    for (int i = tid; i < RL_BT * RL_BK; i += 256) {
+      int r = i / RL_BK, c = i % RL_BK;
+      int t = t0 + r;
+      xs[c][r] = (t < T) ? __ldg(&X[(size_t)t * H + hk + c]) : 0.f;
+    }
+    // Wr tile: 32 h x 64 experts
+    for (int i = tid; i < RL_BK * RL_BE; i += 256) {
+      int r = i / RL_BE, c = i % RL_BE;
+      int e = e0 + c;
+      ws[r][c] = (e < E) ? __ldg(&Wr[(size_t)(hk + r) * E + e]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < RL_BK; ++kk) {
+      float a0 = xs[kk][ty * 2], a1 = xs[kk][ty * 2 + 1];
+      float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+      acc[0][0] = fmaf(a0, b.x, acc[0][0]);
+      acc[0][1] = fmaf(a0, b.y, acc[0][1]);
+      acc[0][2] = fmaf(a0, b.z, acc[0][2]);
+      acc[0][3] = fmaf(a0, b.w, acc[0][3]);
+      acc[1][0] = fmaf(a1, b.x, acc[1][0]);
+      acc[1][1] = fmaf(a1, b.y, acc[1][1]);
+      acc[1][2] = fmaf(a1, b.z, acc[1][2]);
+      acc[1][3] = fmaf(a1, b.w, acc[1][3]);
+    }
+    __syncthreads();
+  }
+  float* dst = part + (size_t)blockIdx.z * T * E;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    int t = t0 + ty * 2 + r;
+    if (t >= T) continue;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      int e = e0 + tx * 4 + c;
+      if (e < E) dst[(size_t)t * E + e] = acc[r][c];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Top-k of one row by one warp. Lane l holds experts l, l+32, ...; each round
+// takes the largest remaining logit, the lower index on ties.
+// ---------------------------------------------------------------------------
+template <int EPL>
+__device__ __forceinline__ void warp_topk_row(const float* part, int nsplit, int T, int E, int k,
+                                              int t, int32_t* ids_out, float* w_out,
+                                              int32_t* ids_smem) {
+  const int lane = threadIdx.x & 31;
+  float v[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    int e = lane + 32 * j;
+    float s = 0.f;
+    if (e < E) {
+      for (int sp = 0; sp < nsplit; ++sp) s += part[((size_t)sp * T + t) * E + e];
+    }
+    v[j] = (e < E) ? s : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float l0 = 0.f, denom = 0.f;
+  float sel_l[16];
+  int sel_e[16];
+  for (int r = 0; r < k; ++r) {
+    // local best: highest value, lowest index (j ascending = index ascending)
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      int e = lane + 32 * j;
+      bool ok = (e < E) && !((taken >> j) & 1u);
+      if (ok && (v[j] > bv || (v[j] == bv && e < be))) {
+        bv = v[j];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be >= E) be = 0;  // only if every remaining logit is NaN: keep the id in range
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    sel_l[r] = bv;
+    sel_e[r] = be;
+    if (r == 0) l0 = bv;
+  }
+  if (lane == 0) {
+    for (int r = 0; r < k; ++r) denom += expf(sel_l[r] - l0);
+    for (int r = 0; r < k; ++r) {
+      ids_out[(size_t)t * k + r] = sel_e[r];
+      w_out[(size_t)t * k + r] = expf(sel_l[r] - l0) / denom;
+      if (ids_smem) ids_smem[(size_t)t * k + r] = sel_e[r];
+    }
+  }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int nsplit,
+                                                   int T, int E, int k, int32_t* __restrict__ ids,
+                                                   float* __restrict__ w) {
+  int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  warp_topk_row<EPL>(part, nsplit, T, E, k, t, ids, w, nullptr);
+}
+
+// ---------------------------------------------------------------------------
+// Permutation for small T (one CTA): optional top-k, histogram, exclusive scan,
+// stable scatter in (t, slot) order, active-expert list. Expert index E is the
+// shared expert, which takes every row (pairs T*k + t).
+// Workspace outputs: offsets[E+2], perm[T*k+T], active[E+1], n_active[1].
+// ---------------------------------------------------------------------------
+template <int EPL>
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const float* __restrict__ part, int nsplit, const int32_t* __restrict__ ids_in, int T, int E,
+    int k, int has_shared, int32_t* __restrict__ ids, float* __restrict__ w,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ active,
+    int32_t* __restrict__ n_active, int* status) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;                 // [E+1]
+  int32_t* cur = sm + (E + 1);       // [E+1] running cursor / scan scratch
+  int32_t* sid = sm + 2 * (E + 1);   // [T*k] ids of this batch
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = T * k;
+  for (int i = tid; i <= E; i += blockDim.x) cnt[i] = 0;
+  if (ids_in == nullptr) {
+    for (int t = warp; t < T; t += blockDim.x / 32)
+      warp_topk_row<EPL>(part, nsplit, T, E, k, t, ids, w, sid);
+  } else {
+    for (int p = tid; p < P; p += blockDim.x) {
+      int e = ids_in[p];
+      if (e < 0 || e >= E) {
+        record_status(status, QMOE_ERR_DEVICE_ARG);
+        e = 0;
+      }
+      sid[p] = e;
+    }
+  }
+  __syncthreads();
+  for (int p = tid; p < P; p += blockDim.x) atomicAdd(&cnt[sid[p]], 1);
+  if (tid == 0) cnt[E] = has_shared ? T : 0;
+  __syncthreads();
+  // exclusive scan over E+1 counts, and the compacted active list (serial in
+  // one warp: E+1 <= 1025 entries, 33 steps of a warp scan)
+  if (warp == 0) {
+    int run = 0, arun = 0;
+    for (int base = 0; base <= E; base += 32) {
+      int e = base + lane;
+      int c = (e <= E) ? cnt[e] : 0;
+      int a = (c > 0) ? 1 : 0;
+      int incl = c, aincl = a;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, incl, off);
+        int oa = __shfl_up_sync(0xffffffffu, aincl, off);
+        if (lane >= off) {
+          incl += o;
+          aincl += oa;
+        }
+      }
+      if (e <= E) {
+        offsets[e] = run + incl - c;
+        cur[e] = run + incl - c;
+        if (a) active[arun + aincl - 1] = e;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+      arun += __shfl_sync(0xffffffffu, aincl, 31);
+    }
+    if (lane == 0) {
+      offsets[E + 1] = run;
+      n_active[0] = arun;
+    }
+  }
+  __syncthreads();
+  // stable scatter: one warp walks the pairs in order, 32 at a time
+  if (warp == 0) {
+    for (int base = 0; base < P; base += 32) {
+      int p = base + lane;
+      int e = (p < P) ? sid[p] : -1;
+      unsigned mask = __match_any_sync(0xffffffffu, e);
+      int rank = __popc(mask & ((1u << lane) - 1u));
+      int pos = 0;
+      if (p < P) pos = cur[e] + rank;
+      __syncwarp();
+      if (p < P) {
+        perm[pos] = p;
+        if ((mask >> lane) == 1u) cur[e] += __popc(mask);  // highest lane of the group
+      }
+      __syncwarp();
+    }
+  } else if (has_shared) {
+    for (int t = tid - 32; t < T; t += blockDim.x - 32) perm[P + t] = P + t;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Permutation for large T: per-chunk histogram, one-CTA scan, per-chunk
+// stable scatter. Chunks are PERM_CHUNK consecutive pairs handled by one warp.
+// chunk_cnt is [n_chunks][E] int32 scratch.
+// ---------------------------------------------------------------------------
+constexpr int PERM_CHUNK = 512;
+
+__global__ void perm_count_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                  int32_t* __restrict__ chunk_cnt, int* status) {
+  extern __shared__ int32_t cnt[];
+  const int c = blockIdx.x;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  int p0 = c * PERM_CHUNK, p1 = min(P, p0 + PERM_CHUNK);
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    int e = ids[p];
+    if (e < 0 || e >= E) {
+      record_status(status, QMOE_ERR_DEVICE_ARG);
+      e = 0;
+    }
+    atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) chunk_cnt[(size_t)c * E + i] = cnt[i];
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_cnt,
+                                                         int n_chunks, int T, int E, int k,
+                                                         int has_shared,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ perm,
+                                                         int32_t* __restrict__ active,
+                                                         int32_t* __restrict__ n_active) {
+  extern __shared__ int32_t tot[];  // [E+1]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // per expert: exclusive running sum over chunks (in place), total
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      int v = chunk_cnt[(size_t)c * E + e];
+      chunk_cnt[(size_t)c * E + e] = run;
+      run += v;
+    }
+    tot[e] = run;
+  }
+  if (tid == 0) tot[E] = has_shared ? T : 0;
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0, arun = 0;
+    for (int base = 0; base <= E; base += 32) {
+      int e = base + lane;
+      int c = (e <= E) ? tot[e] : 0;
+      int a = c > 0;
+      int incl = c, aincl = a;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, incl, off);
+        int oa = __shfl_up_sync(0xffffffffu, aincl, off);
+        if (lane >= off) {
+          incl += o;
+          aincl += oa;
+        }
+      }
+      if (e <= E) {
+        offsets[e] = run + incl - c;
+        if (a) active[arun + aincl - 1] = e;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+      arun += __shfl_sync(0xffffffffu, aincl, 31);
+    }
+    if (lane == 0) {
+      offsets[E + 1] = run;
+      n_active[0] = arun;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int base = offsets[e];
+    for (int c = 0; c < n_chunks; ++c) chunk_cnt[(size_t)c * E + e] += base;
+  }
+  const int P = T * k;
+  if (has_shared)
+    for (int t = tid; t < T; t += blockDim.x) perm[P + t] = P + t;
+}
+
+__global__ void perm_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                    const int32_t* __restrict__ chunk_base,
+                                    int32_t* __restrict__ perm) {
+  extern __shared__ int32_t cur[];
+  const int c = blockIdx.x, lane = threadIdx.x;
+  for (int i = lane; i < E; i += 32) cur[i] = chunk_base[(size_t)c * E + i];
+  __syncwarp();
+  int p0 = c * PERM_CHUNK, p1 = min(P, p0 + PERM_CHUNK);
+  for (int base = p0; base < p1; base += 32) {
+    int p = base + lane;
+    int e = (p < p1) ? ids[p] : -1;
+    if (p < p1 && (e < 0 || e >= E)) e = 0;  // already recorded by the count pass
+    unsigned mask = __match_any_sync(0xffffffffu, e);
+    int rank = __popc(mask & ((1u << lane) - 1u));
+    int pos = (p < p1) ? cur[e] + rank : 0;
+    __syncwarp();
+    if (p < p1) {
+      perm[pos] = p;
+      if ((mask >> lane) == 1u) cur[e] += __popc(mask);
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers
+// ---------------------------------------------------------------------------
+int router_splits(int T, int H, int E) {
+  // enough CTAs to spread the read of Wr at small T; one split at large T
+  int tiles = ((E + RL_BE - 1) / RL_BE) * ((T + RL_BT - 1) / RL_BT);
+  int s = 1;
+  while (tiles * s * 2 <= 256 && (H / (s * 2)) % RL_BK == 0 && H / (s * 2) >= 64) s *= 2;
+  return s;
+}
+
+cudaError_t launch_router_logits(const float* X, const float* Wr, float* part, int T, int H, int E,
+                                 int nsplit, cudaStream_t st) {
+  dim3 grid((E + RL_BE - 1) / RL_BE, (T + RL_BT - 1) / RL_BT, nsplit);
+  router_logits_kernel<<<grid, 256, 0, st>>>(X, Wr, part, T, H, E, H / nsplit);
+  return cudaGetLastError();
+}
+
+template <int EPL>
+static cudaError_t topk_dispatch(const float* part, int nsplit, int T, int E, int k, int32_t* ids,
+                                 float* w, cudaStream_t st) {
+  topk_kernel<EPL><<<(T + 7) / 8, 256, 0, st>>>(part, nsplit, T, E, k, ids, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k, int32_t* ids, float* w,
+                        cudaStream_t st) {
+  if (E <= 32) return topk_dispatch<1>(part, nsplit, T, E, k, ids, w, st);
+  if (E <= 64) return topk_dispatch<2>(part, nsplit, T, E, k, ids, w, st);
+  if (E <= 128) return topk_dispatch<4>(part, nsplit, T, E, k, ids, w, st);
+  if (E <= 256) return topk_dispatch<8>(part, nsplit, T, E, k, ids, w, st);
+  if (E <= 512) return topk_dispatch<16>(part, nsplit, T, E, k, ids, w, st);
+  return topk_dispatch<32>(part, nsplit, T, E, k, ids, w, st);
+}
+
+size_t route_small_smem(int T, int E, int k) { return sizeof(int32_t) * (2 * (E + 1) + T * k); }
+
+template <int EPL>
+static cudaError_t route_small_dispatch(const float* part, int nsplit, const int32_t* ids_in, int T,
+                                        int E, int k, int has_shared, int32_t* ids, float* w,
+                                        int32_t* offsets, int32_t* perm, int32_t* active,
+                                        int32_t* n_active, int* status, cudaStream_t st) {
+  size_t smem = route_small_smem(T, E, k);
+  route_small_kernel<EPL><<<1, 1024, smem, st>>>(part, nsplit, ids_in, T, E, k, has_shared, ids, w,
+                                                 offsets, perm, active, n_active, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_small(const float* part, int nsplit, const int32_t* ids_in, int T, int E,
+                               int k, int has_shared, int32_t* ids, float* w, int32_t* offsets,
+                               int32_t* perm, int32_t* active, int32_t* n_active, int* status,
+                               cudaStream_t st) {
+#define QMOE_RS(EPL) \
+  route_small_dispatch<EPL>(part, nsplit, ids_in, T, E, k, has_shared, ids, w, offsets, perm, \
+                            active, n_active, status, st)
+  if (E <= 32) return QMOE_RS(1);
+  if (E <= 64) return QMOE_RS(2);
+  if (E <= 128) return QMOE_RS(4);
+  if (E <= 256) return QMOE_RS(8);
+  if (E <= 512) return QMOE_RS(16);
+  return QMOE_RS(32);
+#undef QMOE_RS
+}
+
+int perm_chunks(int P) { return (P + PERM_CHUNK - 1) / PERM_CHUNK; }
+
+cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_shared,
+                              int32_t* chunk_cnt, int32_t* offsets, int32_t* perm,
+                              int32_t* active, int32_t* n_active, int* status, cudaStream_t st) {
+  const int P = T * k, nc = perm_chunks(P);
+  perm_count_kernel<<<nc, 256, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, status);
+  perm_scan_kernel<<<1, 1024, sizeof(int32_t) * (E + 1), st>>>(chunk_cnt, nc, T, E, k, has_shared,
+                                                               offsets, perm, active, n_active);
+  perm_scatter_kernel<<<nc, 32, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, perm);
+  return cudaGetLastError();
+}
+
+}  // namespace qmoe
