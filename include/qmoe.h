@@ -130,8 +130,8 @@ int qmoe_moe_forward(const qmoe_moe_desc *d, const float *X, const float *R,
                      const int32_t *ids, const float *w, float *out, int T,
                      void *ws, size_t ws_bytes, qmoe_stream_t stream);
 
-/* Path selection threshold: rows above it take the tensor-core path.
- * qmoe_set_gemm_threshold(-1) restores the built-in value. */
+/* Path selection threshold: T above it takes the tensor-core path (built-in
+ * value 64 rows). qmoe_set_gemm_threshold(-1) restores the built-in value. */
 int qmoe_get_gemm_threshold(void);
 void qmoe_set_gemm_threshold(int rows);
 int qmoe_last_path(void);
@@ -140,8 +140,9 @@ int qmoe_last_path(void);
  * Byte offsets of the intermediates inside a moe_forward workspace, for
  * stagewise checks: ids [T][k] int32, w [T][k] fp32, offsets [E+2] int32
  * (row ranges per expert, the shared expert last), perm [T*k + T] int32 (pair
- * index t*k+s grouped by expert, stable), y [T*k + T][H] fp32 (per pair,
- * shared rows last). Valid after the forward has completed.
+ * index t*k+s grouped by expert, stable), y [T*k + T][H] (per pair, shared
+ * rows last; fp32 on the GEMV path, bf16 on the tensor-core path). Valid after
+ * the forward has completed.
  */
 typedef struct {
   size_t ids, w, offsets, perm, y;

@@ -15,7 +15,8 @@ __device__ int g_status_word;
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_arch_ok[kMaxDevices];     // 0 unknown, 1 sm_103, -1 other
 std::atomic<int*> g_status_ptr[kMaxDevices];
-std::atomic<int> g_gemm_threshold{INT_MAX};
+constexpr int kDefaultGemmThreshold = 64;
+std::atomic<int> g_gemm_threshold{kDefaultGemmThreshold};
 thread_local int g_last_path = QMOE_PATH_NONE;
 std::atomic<long long> g_launches{0};
 
@@ -82,7 +83,7 @@ inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace carve-up (every piece 256-byte aligned).
 struct MoeWs {
-  size_t part, ids, w, offsets, perm, active, n_active, chunk, h, y, total;
+  size_t part, ids, w, offsets, perm, active, n_active, chunk, mtiles, n_mtiles, h, y, total;
   int nsplit;
 };
 
@@ -99,6 +100,8 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   L.active = o;   o += up256(sizeof(int32_t) * (E + 1));
   L.n_active = o; o += 256;
   L.chunk = o;    o += up256(sizeof(int32_t) * (size_t)perm_chunks((int)P) * E);
+  L.mtiles = o;   o += up256(sizeof(int2) * (size_t)tc_max_mtiles(T, k, E, 1));
+  L.n_mtiles = o; o += 256;
   L.h = o;        o += up256(sizeof(float) * rows * F);
   L.y = o;        o += up256(sizeof(float) * rows * H);
   L.total = o;
@@ -159,7 +162,7 @@ int qmoe_query_status(qmoe_stream_t stream) {
 }
 
 int qmoe_get_gemm_threshold(void) { return g_gemm_threshold.load(); }
-void qmoe_set_gemm_threshold(int rows) { g_gemm_threshold.store(rows < 0 ? INT_MAX : rows); }
+void qmoe_set_gemm_threshold(int rows) { g_gemm_threshold.store(rows < 0 ? kDefaultGemmThreshold : rows); }
 int qmoe_last_path(void) { return g_last_path; }
 
 size_t qmoe_moe_route_workspace_bytes(int T, int H, int E, int k) {
@@ -281,6 +284,51 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
   }
   if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
   const float* w_use = ids ? w : ws_w;
+
+  if (T > g_gemm_threshold.load()) {
+    // grouped dequant + bf16 tcgen05 GEMM path: h and y are bf16
+    int2* mtiles = reinterpret_cast<int2*>(base + L.mtiles);
+    int32_t* n_mtiles = reinterpret_cast<int32_t*>(base + L.n_mtiles);
+    __nv_bfloat16* h16 = reinterpret_cast<__nv_bfloat16*>(hbuf);
+    __nv_bfloat16* y16 = reinterpret_cast<__nv_bfloat16*>(y);
+    e = staged(QMOE_STAGE_ROUTE, 1, st, [&] { return launch_build_mtiles(offsets, E, mtiles, n_mtiles, st); });
+    if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+    GroupedTcArgs p{};
+    p.offsets = offsets;
+    p.perm = perm;
+    p.mtiles = mtiles;
+    p.n_mtiles = n_mtiles;
+    p.max_mtiles = tc_max_mtiles(T, k, E, has_shared);
+    p.T = T;
+    p.k = k;
+    p.E = E;
+    p.H = H;
+    p.F = F;
+    p.status = status;
+    p.W = static_cast<const uint8_t*>(d->Wg);
+    p.W2 = static_cast<const uint8_t*>(d->Wu);
+    p.S = static_cast<const uint8_t*>(d->Sg);
+    p.S2 = static_cast<const uint8_t*>(d->Su);
+    p.qt = d->gate_type;
+    p.X = X;
+    p.hout = h16;
+    e = staged(QMOE_STAGE_GATEUP, 1, st, [&] { return launch_gateup_tc(p, st); });
+    if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+    p.W = static_cast<const uint8_t*>(d->Wd);
+    p.W2 = nullptr;
+    p.S = static_cast<const uint8_t*>(d->Sd);
+    p.S2 = nullptr;
+    p.qt = d->down_type;
+    p.hin = h16;
+    p.yout = y16;
+    e = staged(QMOE_STAGE_DOWN, 1, st, [&] { return launch_down_tc(p, st); });
+    if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+    e = staged(QMOE_STAGE_COMBINE, 1, st,
+               [&] { return launch_combine_bf16(y16, w_use, R, out, T, H, k, has_shared, st); });
+    if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+    g_last_path = QMOE_PATH_GEMM_TC;
+    return QMOE_OK;
+  }
 
   GroupedArgs g;
   g.offsets = offsets;

@@ -39,4 +39,28 @@ cudaError_t launch_down_gemv(const GroupedArgs& g, int qt, const float* hbuf, in
 cudaError_t launch_combine(const float* y, const float* w, const float* R, float* out, int T,
                            int H, int k, int has_shared, cudaStream_t st);
 
+// moe_gemm_tc.cu: grouped dequant + bf16 tcgen05 GEMM path.
+struct GroupedTcArgs {
+  const uint8_t *W, *W2, *S, *S2;  // (gate, up, shared gate, shared up) or (down, -, shared down, -)
+  int qt;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int2* mtiles;
+  const int32_t* n_mtiles;
+  int max_mtiles;
+  const float* X;
+  const __nv_bfloat16* hin;
+  __nv_bfloat16* hout;
+  __nv_bfloat16* yout;
+  int T, k, E, H, F;
+  int* status;
+};
+int tc_max_mtiles(int T, int k, int E, int has_shared);
+cudaError_t launch_build_mtiles(const int32_t* offsets, int E, int2* mtiles, int32_t* n_mtiles,
+                                cudaStream_t st);
+cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st);
+cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st);
+cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* w, const float* R, float* out,
+                                int T, int H, int k, int has_shared, cudaStream_t st);
+
 }  // namespace qmoe

@@ -1,0 +1,466 @@
+// Grouped dequant + bf16 tcgen05 GEMM for large T (prefill).
+//
+// "Distributed CPU: Zip Fusion Beyond Tensor Parallelism", "Prefill First, Then
+// One Matrix-Work Scheduler": with many rows per weight region each packed
+// weight is reused across the rows and the region becomes GEMM-bound. Here the
+// rows routed to one expert (contiguous in permutation order) form the M side
+// of a tile; the expert's packed Q4_K/Q5_K rows are dequantised to bf16 in
+// shared memory and fed to tcgen05.mma with the fp32 accumulator in tensor
+// memory ("What PR #382 Now Splits" in "CKE Zip: From Splitting Tokens To
+// Splitting Qwen3.5 Weights": gate, up, SwiGLU and down per expert).
+//
+// One persistent CTA per SM walks work items (m-tile of 128 rows of one expert,
+// n-tile of 256 output columns). Warp roles (288 threads):
+//   warps 0-3  epilogue: TMEM -> registers (warp w reads lanes 32w..32w+31),
+//              fused SwiGLU (gate/up) or bf16 store (down);
+//   warps 4-7  producers: gather the 128 activation rows of the k-tile as
+//              bf16 and dequantise the 256 weight rows, both written in the
+//              128-byte-swizzled K-major layout the MMA descriptors describe;
+//   warp 8     allocates 512 TMEM columns (two 256-column accumulators) and
+//              issues the MMAs from one lane.
+// A 4-stage shared-memory ring (48 KB per stage) decouples producers and the
+// MMA issuer; the two accumulators let the epilogue of one tile overlap the
+// main loop of the next. Every wait is bounded: on time-out the CTA records
+// QMOE_ERR_TIMEOUT, drains its MMAs, frees its TMEM and returns.
+#include "kernels.cuh"
+#include "tc.cuh"
+
+namespace qmoe {
+
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_THREADS = 288;
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
+constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 32 KB
+constexpr int TC_SMEM = TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
+
+struct TcArgs {
+  const uint8_t* W;   // gate (gate/up pass) or down weights of the routed experts
+  const uint8_t* W2;  // up weights (gate/up pass)
+  const uint8_t* S;   // shared expert counterpart of W
+  const uint8_t* S2;  // shared expert counterpart of W2
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int2* mtiles;  // (expert, first row) per m-tile
+  const int32_t* n_mtiles;
+  const float* X;               // gate/up A source, [T][H] fp32
+  const __nv_bfloat16* hin;     // down A source, [P+T][F] bf16
+  __nv_bfloat16* hout;          // gate/up output, [P+T][F] bf16
+  __nv_bfloat16* yout;          // down output, [P+T][H] bf16
+  int T, k, E, H, F;
+  int* status;
+};
+
+__device__ __forceinline__ int tc_pair_row(int p, int T, int k) { return p < T * k ? p / k : p - T * k; }
+
+// Dequantises 8 consecutive weights (word ``w`` of a sub-block's quants, high
+// bits ``hb8`` for Q5_K) as d*s*q - dmin*m and packs them as 4 bf16x2 words.
+template <int QT>
+__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t hb8, float ds, float dm) {
+  float v[8];
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    uint32_t q = (w >> (4 * b)) & 15u;
+    if (QT == QMOE_Q5K) q |= ((hb8 >> b) & 1u) << 4;
+    v[b] = fmaf(ds, (float)q, -dm);
+  }
+  uint4 o;
+  o.x = tc::pack_bf16x2(v[0], v[1]);
+  o.y = tc::pack_bf16x2(v[2], v[3]);
+  o.z = tc::pack_bf16x2(v[4], v[5]);
+  o.w = tc::pack_bf16x2(v[6], v[7]);
+  return o;
+}
+
+// Writes the 64 dequantised weights of k-tile ``kt`` of one packed row into
+// row ``r`` of a swizzled B stage.
+template <int QT>
+__device__ __forceinline__ void produce_b_row(const uint8_t* row, int kt, uint8_t* stage, int r) {
+  constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
+  const uint8_t* blk = row + (size_t)(kt >> 2) * BYTES;
+  const int j0 = (kt & 3) * 2;
+  const KHeader h = load_header(blk);
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int j = j0 + s;
+    const float2 sc = sub_scale(h, j);
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(blk + quant_offset(QT, j)));
+    const uint32_t hb = QT == QMOE_Q5K ? __ldg(reinterpret_cast<const uint32_t*>(blk + 16 + 4 * j)) : 0u;
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 o = dequant8<QT>(w[c], hb >> (8 * c), sc.x, sc.y);
+      *reinterpret_cast<uint4*>(stage + tc::sw128_offset(r, 4 * s + c)) = o;
+    }
+  }
+}
+
+template <bool GATEUP, int QT>
+__global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + TC_STAGES * TC_A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + TC_STAGES * TC_B_BYTES);
+  uint64_t* full = bars;                     // [STAGES]
+  uint64_t* empty = bars + TC_STAGES;        // [STAGES]
+  uint64_t* acc_full = bars + 2 * TC_STAGES; // [2]
+  uint64_t* acc_empty = acc_full + 2;        // [2]
+  uint64_t* drain = acc_empty + 2;           // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NT = GATEUP ? g.F / 128 : g.H / TC_BN;      // n-tiles per m-tile
+  const int KT = GATEUP ? g.H / TC_BK : g.F / TC_BK;    // k-tiles
+  const int total = g.n_mtiles[0] * NT;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TC_STAGES; ++i) {
+      tc::mbar_init(&full[i], 128);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_empty[i], 128);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 8) tc::tmem_alloc(tmem_slot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ epilogue
+    int it = 0;
+    for (int wi = blockIdx.x; wi < total; wi += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!tc::mbar_wait(&acc_full[acc], ph, abort_flag)) break;
+      tc::tc_fence_after();
+      const int2 mt = g.mtiles[wi / NT];
+      const int nt = wi % NT;
+      const int e = mt.x, m0 = mt.y;
+      const int row = 32 * warp + lane;
+      const int base = g.offsets[e];
+      const int Me = g.offsets[e + 1] - base;
+      const bool valid = m0 + row < Me;
+      const int pos = base + m0 + row;
+      const uint32_t tq = tmem + (uint32_t)(acc * 256) + ((uint32_t)(32 * warp) << 16);
+      if (GATEUP) {
+        __nv_bfloat16* dst = g.hout + (size_t)pos * g.F + nt * 128;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 16) {
+          uint32_t gr[16], ur[16];
+          tc::tmem_ld16x2(tq + c, tq + 128 + c, gr, ur);
+          uint32_t o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o[i] = tc::pack_bf16x2(silu_mul(__uint_as_float(gr[2 * i]), __uint_as_float(ur[2 * i])),
+                                   silu_mul(__uint_as_float(gr[2 * i + 1]), __uint_as_float(ur[2 * i + 1])));
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+            d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+      } else {
+        const int pair = valid ? g.perm[pos] : 0;
+        __nv_bfloat16* dst = g.yout + (size_t)pair * g.H + nt * TC_BN;
+#pragma unroll 1
+        for (int c = 0; c < TC_BN; c += 32) {
+          uint32_t a[16], b[16];
+          tc::tmem_ld16x2(tq + c, tq + c + 16, a, b);
+          uint32_t o[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[i] = tc::pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+            o[8 + i] = tc::pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+          }
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+            d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            d4[2] = make_uint4(o[8], o[9], o[10], o[11]);
+            d4[3] = make_uint4(o[12], o[13], o[14], o[15]);
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&acc_empty[acc]);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ producers
+    const int p = threadIdx.x - 128;  // A row and B rows p, p + 128
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int wi = blockIdx.x; wi < total; wi += gridDim.x) {
+      const int2 mt = g.mtiles[wi / NT];
+      const int nt = wi % NT;
+      const int e = mt.x, m0 = mt.y;
+      const int base = g.offsets[e];
+      const int Me = g.offsets[e + 1] - base;
+      const bool valid = m0 + p < Me;
+      const int pos = base + m0 + p;
+      const float* xa = nullptr;
+      const __nv_bfloat16* ha = nullptr;
+      if (valid) {
+        if (GATEUP) xa = g.X + (size_t)tc_pair_row(g.perm[pos], g.T, g.k) * g.H;
+        else ha = g.hin + (size_t)pos * g.F;
+      }
+      const uint8_t *b0, *b1;
+      if (GATEUP) {
+        const size_t rb = (size_t)(g.H / QK) * (QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES);
+        const uint8_t* wg = e < g.E ? g.W + (size_t)e * g.F * rb : g.S;
+        const uint8_t* wu = e < g.E ? g.W2 + (size_t)e * g.F * rb : g.S2;
+        b0 = wg + (size_t)(nt * 128 + p) * rb;
+        b1 = wu + (size_t)(nt * 128 + p) * rb;
+      } else {
+        const size_t rb = (size_t)(g.F / QK) * (QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES);
+        const uint8_t* wd = e < g.E ? g.W + (size_t)e * g.H * rb : g.S;
+        b0 = wd + (size_t)(nt * TC_BN + p) * rb;
+        b1 = wd + (size_t)(nt * TC_BN + 128 + p) * rb;
+      }
+      bool ok = true;
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_st = sA + stage * TC_A_BYTES;
+        uint8_t* b_st = sB + stage * TC_B_BYTES;
+        // A row p: 64 activations of k-tile kt as bf16
+        if (GATEUP) {
+          const float4* src = reinterpret_cast<const float4*>(xa + kt * TC_BK);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (valid) {
+              float4 u = __ldg(src + 2 * c), v = __ldg(src + 2 * c + 1);
+              o = make_uint4(tc::pack_bf16x2(u.x, u.y), tc::pack_bf16x2(u.z, u.w),
+                             tc::pack_bf16x2(v.x, v.y), tc::pack_bf16x2(v.z, v.w));
+            }
+            *reinterpret_cast<uint4*>(a_st + tc::sw128_offset(p, c)) = o;
+          }
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(ha + kt * TC_BK);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 o = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(a_st + tc::sw128_offset(p, c)) = o;
+          }
+        }
+        produce_b_row<QT>(b0, kt, b_st, p);
+        produce_b_row<QT>(b1, kt, b_st, p + 128);
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&full[stage]);
+        if (++stage == TC_STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = tc::idesc_bf16_f32(TC_BM, TC_BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!tc::mbar_wait(&acc_empty[acc], ph ^ 1, abort_flag)) break;
+      tc::tc_fence_after();
+      const uint32_t d_tmem = tmem + (uint32_t)(acc * 256);
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = tc::smem_u32(sA + stage * TC_A_BYTES);
+          const uint32_t b_addr = tc::smem_u32(sB + stage * TC_B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk) {
+            tc::mma_bf16(d_tmem, tc::sw128_desc(a_addr + 32 * kk), tc::sw128_desc(b_addr + 32 * kk), idesc,
+                         (kt | kk) != 0);
+          }
+          tc::mma_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == TC_STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (ok && lane == 0) tc::mma_commit(&acc_full[acc]);
+      __syncwarp();
+    }
+    // drain: every MMA this thread issued has completed before TMEM is freed
+    if (lane == 0) {
+      tc::mma_commit(drain);
+      volatile int never = 0;
+      tc::mbar_wait(drain, 0, &never);
+    }
+    __syncwarp();
+  }
+
+  if (*abort_flag && threadIdx.x == 0) record_status(g.status, QMOE_ERR_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 8) tc::tmem_dealloc(tmem, 512);
+}
+
+// Builds the m-tile list: for every expert with rows (the shared expert last),
+// one entry per 128 rows. One CTA; the scan runs in warp 0.
+__global__ void __launch_bounds__(1024) build_mtiles_kernel(const int32_t* __restrict__ offsets, int E,
+                                                            int2* __restrict__ mtiles,
+                                                            int32_t* __restrict__ n_mtiles) {
+  extern __shared__ int32_t start[];  // [E+1] exclusive scan of tile counts
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    int run = 0;
+    for (int b = 0; b <= E; b += 32) {
+      const int e = b + lane;
+      const int c = e <= E ? (offsets[e + 1] - offsets[e] + TC_BM - 1) / TC_BM : 0;
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (e <= E) start[e] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) n_mtiles[0] = run;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    const int Me = offsets[e + 1] - offsets[e];
+    int s = start[e];
+    for (int m0 = 0; m0 < Me; m0 += TC_BM) mtiles[s++] = make_int2(e, m0);
+  }
+}
+
+// out_t = R_t + y_shared,t + sum_s w_{t,s} y_{t,s} with bf16 y, in slot order.
+__global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* __restrict__ y,
+                                                           const float* __restrict__ w, const float* R,
+                                                           float* out, int T, int H, int k,
+                                                           int has_shared) {
+  const int H8 = H / 8;
+  const size_t n = (size_t)T * H8;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H8), c = (int)(i % H8);
+    float acc[8];
+    if (R) {
+      const float4* r4 = reinterpret_cast<const float4*>(R + (size_t)t * H) + 2 * c;
+      float4 a = r4[0], b = r4[1];
+      acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+      acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    }
+    if (has_shared) {
+      uint4 v = reinterpret_cast<const uint4*>(y + ((size_t)T * k + t) * H)[c];
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float2 f = __bfloat1622float2(h2[j]);
+        acc[2 * j] += f.x;
+        acc[2 * j + 1] += f.y;
+      }
+    }
+    for (int s = 0; s < k; ++s) {
+      const float ws = w[(size_t)t * k + s];
+      uint4 v = reinterpret_cast<const uint4*>(y + ((size_t)t * k + s) * H)[c];
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float2 f = __bfloat1622float2(h2[j]);
+        acc[2 * j] = fmaf(ws, f.x, acc[2 * j]);
+        acc[2 * j + 1] = fmaf(ws, f.y, acc[2 * j + 1]);
+      }
+    }
+    float4* o4 = reinterpret_cast<float4*>(out + (size_t)t * H) + 2 * c;
+    o4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+int tc_num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n = v > 0 ? v : 1;
+  }
+  return n;
+}
+
+int tc_max_mtiles(int T, int k, int E, int has_shared) {
+  const int P = T * k;
+  return (P + (has_shared ? T : 0)) / TC_BM + E + 1;
+}
+
+cudaError_t launch_build_mtiles(const int32_t* offsets, int E, int2* mtiles, int32_t* n_mtiles,
+                                cudaStream_t st) {
+  build_mtiles_kernel<<<1, 1024, sizeof(int32_t) * (E + 1), st>>>(offsets, E, mtiles, n_mtiles);
+  return cudaGetLastError();
+}
+
+template <bool GATEUP, int QT>
+static cudaError_t tc_launch_t(const TcArgs& a, int max_items, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(moe_tc_kernel<GATEUP, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TC_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  int grid = tc_num_sms();
+  if (grid > max_items) grid = max_items;
+  if (grid < 1) grid = 1;
+  moe_tc_kernel<GATEUP, QT><<<grid, TC_THREADS, TC_SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st) {
+  TcArgs a{};
+  a.W = p.W; a.W2 = p.W2; a.S = p.S; a.S2 = p.S2;
+  a.offsets = p.offsets; a.perm = p.perm; a.mtiles = p.mtiles; a.n_mtiles = p.n_mtiles;
+  a.X = p.X; a.hout = p.hout;
+  a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
+  const int items = p.max_mtiles * (p.F / 128);
+  return p.qt == QMOE_Q5K ? tc_launch_t<true, QMOE_Q5K>(a, items, st) : tc_launch_t<true, QMOE_Q4K>(a, items, st);
+}
+
+cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
+  TcArgs a{};
+  a.W = p.W; a.S = p.S;
+  a.offsets = p.offsets; a.perm = p.perm; a.mtiles = p.mtiles; a.n_mtiles = p.n_mtiles;
+  a.hin = p.hin; a.yout = p.yout;
+  a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
+  const int items = p.max_mtiles * (p.H / TC_BN);
+  return p.qt == QMOE_Q5K ? tc_launch_t<false, QMOE_Q5K>(a, items, st) : tc_launch_t<false, QMOE_Q4K>(a, items, st);
+}
+
+cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* w, const float* R, float* out, int T, int H,
+                                int k, int has_shared, cudaStream_t st) {
+  const size_t n = (size_t)T * (H / 8);
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  combine_bf16_kernel<<<blocks, 256, 0, st>>>(y, w, R, out, T, H, k, has_shared);
+  return cudaGetLastError();
+}
+
+}  // namespace qmoe

@@ -13,7 +13,7 @@ import torch
 
 from quantized_moe_transformer_gb300 import binding as qb
 from quantized_moe_transformer_gb300 import inputs
-from tests.parity import TOL_GEMV, TOL_TC, assert_close, check_routes
+from tests.parity import GAP, TOL_GEMV, TOL_TC, assert_close, check_routes
 
 pytestmark = pytest.mark.gpu
 
@@ -221,3 +221,38 @@ def test_argument_errors():
         qb.moe_forward(lay, X, ws=ws[1:])
     with pytest.raises(qb.QmoeError):
         qb.moe_forward(lay, X, out=X)
+
+
+@pytest.mark.parametrize("T", [65, 200])
+def test_gemv_and_tensor_core_paths_agree(oracle, T):
+    """The same rows through both paths (threshold forced each way)."""
+    arr, lay, k = layer_pair(0)
+    X = inputs.hidden(21, T, 2048)
+    Xd = torch.from_numpy(X).cuda()
+    old = qb.get_gemm_threshold()
+    try:
+        qb.set_gemm_threshold(10**9)
+        a = qb.moe_forward(lay, Xd)
+        assert qb.last_path() == "gemv"
+        qb.set_gemm_threshold(0)
+        b = qb.moe_forward(lay, Xd)
+        assert qb.last_path() == "gemm_tc"
+    finally:
+        qb.set_gemm_threshold(old)
+    torch.cuda.synchronize()
+    assert_close(b.cpu().numpy(), a.cpu().numpy(), TOL_TC)
+    rows = np.array([0, T // 2, T - 1])
+    ref, parts = oracle.moe_forward_rows(X, arr, k, rows)
+    ok = parts["gap"] >= GAP
+    assert_close(a.cpu().numpy()[rows], ref, TOL_GEMV, rows=ok)
+    assert_close(b.cpu().numpy()[rows], ref, TOL_TC, rows=ok)
+
+
+def test_tensor_core_path_bit_identical():
+    arr, lay, k = layer_pair(1)
+    X = torch.from_numpy(inputs.hidden(4, 512, 2048)).cuda()
+    a = qb.moe_forward(lay, X)
+    assert qb.last_path() == "gemm_tc"
+    b = qb.moe_forward(lay, X)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
