@@ -75,6 +75,45 @@ __device__ __forceinline__ float dot_sub(const uint4 qv, uint32_t hb, const floa
   return acc;
 }
 
+// Spreads four bits of ``h`` (bits b, b+2, b+4, b+6) to bit 4 of bytes 0..3.
+__device__ __forceinline__ uint32_t spread4(uint32_t h, int b) {
+  return (((h >> b) & 1u) << 4) | (((h >> (b + 2)) & 1u) << 12) | (((h >> (b + 4)) & 1u) << 20) |
+         (((h >> (b + 6)) & 1u) << 28);
+}
+
+// S = sum over the 32 weights of one sub-block of (0.5 + q_i/256) * x_i.
+// Each quant byte (0..31) is placed by one byte permute into the mantissa of
+// a float whose exponent makes it 0.5 + q/256 exactly, so the unpacking costs
+// one integer instruction per weight and no int->float conversion. The caller
+// recovers sum q_i x_i = 256 * (S - 0.5 * sum x_i).
+template <int QT>
+__device__ __forceinline__ float dot_sub_prmt(const uint4 qv, uint32_t hb, const float* x) {
+  const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    uint32_t ev = w[n] & 0x0F0F0F0Fu;          // weights 8n + 2k
+    uint32_t od = (w[n] >> 4) & 0x0F0F0F0Fu;   // weights 8n + 2k + 1
+    if (QT == QMOE_Q5K) {
+      ev |= spread4(hb >> (8 * n), 0);
+      od |= spread4(hb >> (8 * n), 1);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t sel = 0x7044u | ((uint32_t)k << 8);
+      acc0 = fmaf(__uint_as_float(__byte_perm(ev, 0x3F000000u, sel)), x[8 * n + 2 * k], acc0);
+      acc1 = fmaf(__uint_as_float(__byte_perm(od, 0x3F000000u, sel)), x[8 * n + 2 * k + 1], acc1);
+    }
+  }
+  return acc0 + acc1;
+}
+
+// Contribution of one sub-block: d*s_j * sum q x - dmin*m_j * sum x, from the
+// byte-permute sum S of dot_sub_prmt and xs = sum x.
+__device__ __forceinline__ float sub_contrib(float S, float xs, float2 sc) {
+  return fmaf(256.f * sc.x, S, -(128.f * sc.x + sc.y) * xs);
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.f + __expf(-g)) * u;
 }
