@@ -66,7 +66,8 @@ typedef enum {
   QMOE_ERR_LAUNCH = -6,      /* a kernel launch failed (cudaGetLastError)    */
   QMOE_ERR_TIMEOUT = -7,     /* device: a bounded wait ran out               */
   QMOE_ERR_DEVICE_ARG = -8,  /* device: caller-supplied route out of range   */
-  QMOE_ERR_CUDA = -9         /* another CUDA runtime error                   */
+  QMOE_ERR_CUDA = -9,        /* another CUDA runtime error                   */
+  QMOE_ERR_TOO_LARGE = -10   /* the problem needs more than the library's fixed scratch */
 } qmoe_status;
 
 typedef enum { QMOE_Q4K = 0, QMOE_Q5K = 1 } qmoe_qtype;
@@ -161,6 +162,33 @@ size_t qmoe_moe_forward_host_workspace_bytes(const qmoe_moe_desc *d, int T);
 int qmoe_moe_forward_host(const qmoe_moe_desc *d, const float *X_host, const float *R_host,
                           float *out_host, int T, void *ws, size_t ws_bytes,
                           qmoe_stream_t stream);
+
+/*
+ * qmoe_moe_forward for callers that cannot allocate device memory (the paper
+ * has no counterpart; it is an interface convenience). Some callers have no
+ * way to hand over a workspace: plugin interfaces that give an operator only
+ * its input and output buffers, or threads that must not call cudaMalloc
+ * because it may synchronise the whole device. This entry point allocates
+ * nothing and calls no allocating routine; its scratch is a fixed array of
+ * QMOE_NOALLOC_SCRATCH_BYTES (8 MiB) in device memory that the library
+ * declares, which every GPU that loads the library holds until the process
+ * exits.
+ *   Same arguments and result as qmoe_moe_forward with internal routing
+ *   (no ids/w): X [T][H] fp32, R [T][H] fp32 or NULL, out [T][H] fp32.
+ *   Returns QMOE_ERR_TOO_LARGE, enqueuing nothing, when
+ *   qmoe_moe_workspace_bytes(d, T) exceeds the scratch size (at the
+ *   Qwen3.5-35B-A3B layer shape that is T > 64 rows).
+ *   The first call on each device looks up the scratch array's device
+ *   address with that device current; make that first call before any
+ *   stream capture. Every call on a device shares the one array and leaves
+ *   its contents behind; nothing in it needs to start at zero, because every
+ *   byte a call reads is written earlier in the same call. Calls whose work
+ *   overlaps on the GPU (other streams, other host threads) race on the
+ *   array: serialise them.
+ */
+#define QMOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int qmoe_moe_forward_noalloc(const qmoe_moe_desc *d, const float *X, const float *R,
+                             float *out, int T, qmoe_stream_t stream);
 
 /* Number of kernels this library has enqueued since it was loaded (a CUDA
  * graph replay of captured launches does not add to it). */

@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
         L.qmoe_launch_count.argtypes = []
         L.qmoe_profile_start.argtypes = [_c_int]
         L.qmoe_profile_stop.argtypes = [P(ctypes.c_double), P(_c_int)]
+        L.qmoe_moe_forward_noalloc.argtypes = [P(MoeDesc), _vp, _vp, _vp, _c_int, _vp]
         _lib = L
     return _lib
 
@@ -83,7 +84,8 @@ def exported_symbols() -> list[str]:
             "qmoe_set_gemm_threshold", "qmoe_last_path", "qmoe_moe_route_workspace_bytes",
             "qmoe_moe_route", "qmoe_moe_workspace_bytes", "qmoe_moe_workspace_layout",
             "qmoe_moe_forward", "qmoe_moe_forward_host_workspace_bytes", "qmoe_moe_forward_host",
-            "qmoe_launch_count", "qmoe_profile_start", "qmoe_profile_stop"]
+            "qmoe_launch_count", "qmoe_profile_start", "qmoe_profile_stop",
+            "qmoe_moe_forward_noalloc"]
 
 
 def _check(status: int):
@@ -230,3 +232,15 @@ def profile_stop():
     n = _c_int()
     _check(lib().qmoe_profile_stop(ctypes.byref(ms), ctypes.byref(n)))
     return ms.value, n.value
+
+
+def moe_forward_noalloc(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = None,
+                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The layer with the library's fixed device scratch instead of a caller
+    workspace (for callers that cannot allocate); raises for T beyond it."""
+    T = X.shape[0]
+    if out is None:
+        out = torch.empty_like(X)
+    _check(lib().qmoe_moe_forward_noalloc(ctypes.byref(layer.desc), _ptr(X), _ptr(R), _ptr(out), T,
+                                          _stream(stream)))
+    return out

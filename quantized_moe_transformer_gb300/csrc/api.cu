@@ -145,6 +145,7 @@ const char* qmoe_status_str(int s) {
     case QMOE_ERR_TIMEOUT: return "device wait timed out";
     case QMOE_ERR_DEVICE_ARG: return "device: route id out of range";
     case QMOE_ERR_CUDA: return "CUDA runtime error";
+    case QMOE_ERR_TOO_LARGE: return "problem exceeds the library's fixed scratch (use a workspace)";
     default: return "unknown status";
   }
 }
