@@ -33,12 +33,25 @@ sys.path.insert(0, ROOT)
 H, E, K_TOP, F = 2048, 256, 8, 512
 EXPERT_BYTES = 2 * F * (H // 256) * 144 + H * (F // 256) * 176   # 1 900 544
 GATEUP_EXPERT_BYTES = 2 * F * (H // 256) * 144                    # 1 179 648
+KERNEL_SOURCES = {
+    "decode": ["quantized_moe_transformer_gb300/csrc/moe_decode.cu",
+               "quantized_moe_transformer_gb300/csrc/common.cuh",
+               "quantized_moe_transformer_gb300/csrc/tc.cuh"],
+    "gemv": ["quantized_moe_transformer_gb300/csrc/moe_gemv.cu",
+             "quantized_moe_transformer_gb300/csrc/common.cuh"],
+    "gemm_tc": ["quantized_moe_transformer_gb300/csrc/moe_gemm_tc.cu",
+                "quantized_moe_transformer_gb300/csrc/common.cuh",
+                "quantized_moe_transformer_gb300/csrc/tc.cuh"],
+}
 WORKLOADS = {
     "decode": dict(T=1, routing="uniform"),
     "decode64": dict(T=64, routing="uniform"),
     "decode64-zipf": dict(T=64, routing="zipf"),
     "prefill512": dict(T=512, routing="uniform"),
     "prefill4096": dict(T=4096, routing="uniform"),
+    # the whole attention + MoE block (16 query heads, 2 KV heads, head_dim 128)
+    "block1": dict(T=1, routing="uniform", block=True, pos0=4095),
+    "block4096": dict(T=4096, routing="uniform", block=True, pos0=0),
 }
 
 
@@ -50,6 +63,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     p.add_argument("--layers", type=int, default=16)
+    p.add_argument("--gemm-threshold", type=int, default=None,
+                   help="rows above which the tensor-core path is taken (library default if unset)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=str, default=None, help=argparse.SUPPRESS)
@@ -57,7 +72,9 @@ def parse():
 
 
 def workload_config(name, T, routing, layers):
-    return {"workload": f"{name}: routed-MoE layer, T={T} rows, H={H}, E={E}, top-{K_TOP}, F={F}, "
+    what = ("attention (16 q heads, 2 kv heads, hd 128, bf16 cache of 4096) + routed-MoE block"
+            if WORKLOADS[name].get("block") else "routed-MoE layer")
+    return {"workload": f"{name}: {what}, T={T} rows, H={H}, E={E}, top-{K_TOP}, F={F}, "
                         f"shared expert, Q4_K gate/up, Q5_K down, fp32 hidden, {routing} routing",
             "T": T, "H": H, "E": E, "top_k": K_TOP, "F": F, "routing": routing,
             "l2": f"{layers} distinct layer instances rotated ({layers * EXPERT_BYTES * 257 / 1e9:.1f} GB "
@@ -204,6 +221,33 @@ def make_layer_on_device(torch, seed, routing, device, from_arrays=None):
     return qb.MoeLayer(H, E, K_TOP, F, Wr.contiguous(), Wg, Wu, Wd, Sg, Su, Sd, "q4k", "q5k")
 
 
+CTX = 4096
+
+
+def make_block_on_device(torch, qb, seed, moe_layer, device):
+    """Attention weights (Q4_K) and RMSNorm gains of one block instance."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+
+    def blocks(rows, nb):
+        b = torch.randint(0, 256, (rows * nb, 144), dtype=torch.uint8, device=device, generator=g)
+        dd = torch.empty((rows * nb, 2), device=device).uniform_(2.0**-12, 2.0**-10, generator=g)
+        b[:, 0:4] = dd.half().view(torch.uint8).reshape(rows * nb, 4)
+        return b.reshape(rows, nb, 144)
+
+    g1 = 1.0 + 0.1 * torch.randn(H, device=device, generator=g)
+    g2 = 1.0 + 0.1 * torch.randn(H, device=device, generator=g)
+    return qb.Block(H, 16, 2, 128, g1, g2, blocks(2048, 8), blocks(256, 8), blocks(256, 8), blocks(H, 8),
+                    moe_layer)
+
+
+def block_moe_ws_offset(qb, blk, T, pos0):
+    """Byte offset of the MoE layer's workspace inside a block workspace."""
+    a = int(qb._block_lib().qmoe_attn_workspace_bytes(__import__("ctypes").byref(blk.desc), T, pos0))
+    row = (4 * T * H + 255) // 256 * 256
+    return a + 2 * row
+
+
 def source_sha(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -220,6 +264,8 @@ def ours_main(args, rank, world, local_rank):
     from quantized_moe_transformer_gb300 import build, inputs
 
     build.build()
+    if args.gemm_threshold is not None:
+        qb.set_gemm_threshold(args.gemm_threshold)
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     wl = WORKLOADS[args.workload]
@@ -230,6 +276,8 @@ def ours_main(args, rank, world, local_rank):
     if os.path.exists(pk):
         peaks = json.load(open(pk))
 
+    is_block = wl.get("block", False)
+    pos0 = wl.get("pos0", 0)
     arr0 = inputs.moe_layer(0, H, E, F, shared=True, routing=routing)
     layers = [make_layer_on_device(torch, 1000 * rank + i, routing, device,
                                    arr0 if i == 0 else None) for i in range(NL)]
@@ -239,11 +287,23 @@ def ours_main(args, rank, world, local_rank):
     if routing == "zipf":
         Xs[:, :, 0] = 1.0
     outs = torch.empty_like(Xs)
-    ws = layers[0].workspace(T)
     stream = torch.cuda.Stream(device=device)
+    if is_block:
+        blocks_ = [make_block_on_device(torch, qb, 5000 * rank + i, layers[i], device) for i in range(NL)]
+        kcs = [torch.randn((CTX, 2, 128), device=device, generator=gX).to(torch.bfloat16) for _ in range(NL)]
+        vcs = [torch.randn((CTX, 2, 128), device=device, generator=gX).to(torch.bfloat16) for _ in range(NL)]
+        ws = blocks_[0].workspace(T, pos0)
+        moe_ws_off = block_moe_ws_offset(qb, blocks_[0], T, pos0)
 
-    def step(i, s=None):
-        qb.moe_forward(layers[i % NL], Xs[i % NL], Xs[i % NL], out=outs[i % NL], ws=ws, stream=s)
+        def step(i, s=None):
+            j = i % NL
+            qb.block_forward(blocks_[j], Xs[j], kcs[j], vcs[j], pos0, out=outs[j], ws=ws, stream=s)
+    else:
+        ws = layers[0].workspace(T)
+        moe_ws_off = 0
+
+        def step(i, s=None):
+            qb.moe_forward(layers[i % NL], Xs[i % NL], Xs[i % NL], out=outs[i % NL], ws=ws, stream=s)
 
     with torch.cuda.stream(stream):
         n0 = qb.launch_count()
@@ -290,8 +350,10 @@ def ours_main(args, rank, world, local_rank):
         dist.barrier()
     value = T * args.steps * world / (ms / 1e3)
 
-    # dominant kernel: grouped gate/up, timed per launch on the launching stream
-    dom = "gateup"
+    # dominant kernel, timed per launch with events the library records on the
+    # launching stream: the decode path's chained kernels as one unit, else the
+    # grouped gate/up kernel (GEMV or tcgen05)
+    dom = "decode" if path == "decode" else "gateup"
     prof_steps = 2 * NL
     U = []
     L = layers[0].workspace_layout(T)
@@ -299,34 +361,67 @@ def ours_main(args, rank, world, local_rank):
         qb.profile_start(dom)
         for i in range(prof_steps):
             step(i, stream)
-            ids = ws[L.ids:L.ids + 4 * T * K_TOP].view(torch.int32)
+            o_ids = moe_ws_off + L.ids
+            ids = ws[o_ids:o_ids + 4 * T * K_TOP].view(torch.int32)
             U.append(int(torch.unique(ids).numel()))
         dom_ms, dom_n = qb.profile_stop()
     torch.cuda.synchronize()
     dom_avg_ms = dom_ms / dom_n
-    # algorithmic bytes of one gate/up launch: each touched expert's packed gate and
-    # up rows once, the rows X read, h written (fp32)
     u_mean = float(np.mean(U))
     rows_h = T * K_TOP + T
-    alg_bytes = (u_mean + 1) * GATEUP_EXPERT_BYTES + T * H * 4 + rows_h * F * 4
-    achieved = alg_bytes / (dom_avg_ms / 1e3) / 1e9
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = peak or 6800.0
-    traffic = None
-    tf = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    kernel_sha = source_sha(["quantized_moe_transformer_gb300/csrc/moe_gemv.cu",
-                             "quantized_moe_transformer_gb300/csrc/common.cuh"])
-    if os.path.exists(tf):
-        rec = json.load(open(tf)).get(f"{dom}:{args.workload}")
-        if rec and rec.get("source_sha") == kernel_sha:
-            traffic = rec["dram_bytes_per_launch"]
     layer_bytes = (u_mean + 1) * EXPERT_BYTES + H * E * 4 + 2 * T * H * 4
     layer_gbs = layer_bytes / (ms / args.steps / 1e3) / 1e9
+    hbm_peak = peaks.get("hbm_gbs")
+    hbm_src = "measured hbm_gbs (burst copy)" if hbm_peak else "fallback 6.8 TB/s"
+    hbm_peak = hbm_peak or 6800.0
+    if path == "gemm_tc":
+        # FLOPs of one gate/up launch: gate and up for every routed pair and the shared rows
+        alg = 2.0 * rows_h * H * 2 * F
+        achieved = alg / (dom_avg_ms / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops")
+        peak_src = "measured bf16_tflops (burst cuBLAS)" if peak else "fallback 1.9 PFLOP/s"
+        peak = peak or 1900.0
+        bound, unit, kname = "tensor", "TFLOP/s", "moe_tc_kernel<gate/up> (tcgen05)"
+    else:
+        if path == "decode":
+            alg = layer_bytes
+            kname = "decode chain: router + gate/up + down/combine kernels (PDL-overlapped, timed as one unit)"
+        else:
+            # each touched expert's packed gate and up rows once, X read, h written (fp32)
+            alg = (u_mean + 1) * GATEUP_EXPERT_BYTES + T * H * 4 + rows_h * F * 4
+            kname = "gateup_gemv_kernel"
+        achieved = alg / (dom_avg_ms / 1e3) / 1e9
+        peak, peak_src, bound, unit = hbm_peak, hbm_src, "hbm", "GB/s"
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    kernel_sha = source_sha(KERNEL_SOURCES[path])
+    if os.path.exists(tf):
+        rec = json.load(open(tf)).get(f"{path}:{args.workload}")
+        if rec and rec.get("source_sha") == kernel_sha:
+            traffic = rec["dram_bytes_per_launch"]
 
     # end to end through the C ABI on host buffers (pinned), copies inside
     e2e = None
-    if rank == 0 or True:
+    if is_block:
+        Xh = torch.randn((NL, T, H), generator=torch.Generator().manual_seed(11)).pin_memory()
+        Oh = torch.empty_like(Xh).pin_memory()
+        Xd = torch.empty((T, H), device=device)
+        n_e2e = min(args.steps, 200)
+        with torch.cuda.stream(stream):
+            for i in range(3 + n_e2e):
+                if i == 3:
+                    torch.cuda.synchronize()
+                    t0 = time.perf_counter()
+                j = i % NL
+                Xd.copy_(Xh[j], non_blocking=True)
+                qb.block_forward(blocks_[j], Xd, kcs[j], vcs[j], pos0, out=outs[j], ws=ws, stream=stream)
+                Oh[j].copy_(outs[j], non_blocking=True)
+                stream.synchronize()
+        dt = time.perf_counter() - t0
+        e2e = {"value": T * n_e2e * world / dt, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 4,
+               "d2h_bytes_per_step": T * H * 4, "steps": n_e2e,
+               "api": "binding.block_forward with pinned host copies on the same stream"}
+    else:
         Xh = torch.randn((NL, T, H), generator=torch.Generator().manual_seed(11)).pin_memory()
         if routing == "zipf":
             Xh[:, :, 0] = 1.0
@@ -346,7 +441,7 @@ def ours_main(args, rank, world, local_rank):
     # CPU baseline and a parity spot check of instance 0 on the same rows
     cpu = None
     parity = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not is_block:
         res = run_cpu_sample(routing, 64, args.cpu_seconds, threads=1)
         n = len(res["times"])
         cpu = {"value": n / sum(res["times"]), "unit": "tokens/s", "cores": 1, "kind": "oracle",
@@ -361,16 +456,18 @@ def ours_main(args, rank, world, local_rank):
         line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32" if path == "gemv" else "bf16", "data": "synthetic",
+                "dtype": "bf16" if path == "gemm_tc" else "f32", "data": "synthetic",
                 "config": workload_config(args.workload, T, routing, NL),
                 "path": path,
-                "roofline": {"bound": "hbm", "kernel": "gateup_gemv_kernel", "achieved": achieved,
-                             "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                "roofline": {"bound": bound, "kernel": kname, "achieved": achieved,
+                             "peak": peak, "peak_source": peak_src, "unit": unit,
                              "frac": achieved / peak, "traffic": traffic,
-                             "alg_bytes_per_launch": alg_bytes, "avg_launch_us": dom_avg_ms * 1e3,
-                             "launches_timed": dom_n, "distinct_experts_mean": u_mean},
-                "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / peak,
+                             "algorithmic_per_launch": alg, "avg_launch_us": dom_avg_ms * 1e3,
+                             "launches_timed": dom_n, "distinct_experts_mean": u_mean,
+                             "kernel_source_sha": kernel_sha},
+                "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / hbm_peak,
                               "alg_bytes_per_step": layer_bytes},
+                "layer_tflops": 2.0 * T * (H * E + 3 * H * F * (K_TOP + 1)) / (ms / args.steps / 1e3) / 1e12,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
                 "launches_per_step": launches_per_step, "clocks": clk.summary, "parity": parity}
         print(json.dumps(line))

@@ -73,7 +73,12 @@ typedef enum {
 typedef enum { QMOE_Q4K = 0, QMOE_Q5K = 1 } qmoe_qtype;
 
 /* Execution path the last successful qmoe_moe_forward took on this thread. */
-typedef enum { QMOE_PATH_NONE = 0, QMOE_PATH_GEMV = 1, QMOE_PATH_GEMM_TC = 2 } qmoe_path;
+typedef enum {
+  QMOE_PATH_NONE = 0,
+  QMOE_PATH_GEMV = 1,     /* grouped dequant-fused GEMV kernels        */
+  QMOE_PATH_GEMM_TC = 2,  /* grouped dequant + bf16 tcgen05 GEMM       */
+  QMOE_PATH_DECODE = 3    /* T <= 4: three kernels chained with PDL    */
+} qmoe_path;
 
 /*
  * One routed-MoE layer ([CKE-Zip] "What PR #382 Now Splits").
@@ -120,9 +125,10 @@ int qmoe_moe_route(const float *X, const float *Wr, int T, int H, int E, int k,
  *        decision shared by two rank partials), or both NULL to route X here.
  *   out  [T][H] fp32; may alias R but not X.
  *   ws   qmoe_moe_workspace_bytes(d, T) bytes, 256-byte aligned.
- * Small T takes the dequant-fused grouped GEMV path (fp32 accumulation);
- * large T the grouped dequant + bf16 tcgen05 GEMM path (fp32 accumulation in
- * tensor memory); qmoe_last_path() tells which ran.
+ * T <= 4 (internal routing) takes the decode path, other small T the
+ * dequant-fused grouped GEMV path (both fp32 accumulation); large T the
+ * grouped dequant + bf16 tcgen05 GEMM path (fp32 accumulation in tensor
+ * memory); qmoe_last_path() tells which ran.
  * A rank partial of the intermediate split is computed by passing that
  * rank's slices of the packed tensors with F halved.
  */
@@ -136,6 +142,14 @@ int qmoe_moe_forward(const qmoe_moe_desc *d, const float *X, const float *R,
 int qmoe_get_gemm_threshold(void);
 void qmoe_set_gemm_threshold(int rows);
 int qmoe_last_path(void);
+
+/* Rows up to this count (at most 4, the built-in value) take the decode path
+ * when the layer's routes are computed internally: router, gate/up and down
+ * kernels chained with programmatic dependent launch, each CTA taking the
+ * top-k itself and the down kernel forming the slot-order combine. 0 turns it
+ * off; -1 restores the built-in value. */
+int qmoe_get_decode_max_rows(void);
+void qmoe_set_decode_max_rows(int rows);
 
 /*
  * Byte offsets of the intermediates inside a moe_forward workspace, for
@@ -206,10 +220,56 @@ typedef enum {
   QMOE_STAGE_ROUTE = 2,   /* top-k, histogram, scan, permutation    */
   QMOE_STAGE_GATEUP = 3,  /* grouped gate/up + SwiGLU               */
   QMOE_STAGE_DOWN = 4,    /* grouped down projection                */
-  QMOE_STAGE_COMBINE = 5  /* slot-order combine + shared + residual */
+  QMOE_STAGE_COMBINE = 5, /* slot-order combine + shared + residual */
+  QMOE_STAGE_DECODE = 6   /* the decode path's three chained kernels, as one unit */
 } qmoe_stage;
 int qmoe_profile_start(int stage);
 int qmoe_profile_stop(double *total_ms, int *launches);
+
+/*
+ * One transformer block around the MoE layer ([CKE-Zip] "What PR #382 Now
+ * Splits": full attention with 16 query heads and 2 KV heads, then the MoE
+ * layer, each with its residual):
+ *   h1  = X + O( attention( RoPE(Q(r1)), RoPE(K(r1)), V(r1) ) ),  r1 = RMSNorm(X; g1)
+ *   out = h1 + moe( RMSNorm(h1; g2) )
+ * RMSNorm(x; g) = x / sqrt(mean(x^2) + eps) * g. RoPE rotates pairs (i, i+hd/2)
+ * by pos * theta^(-2i/hd). Query head h reads KV head h / (n_heads/n_kv);
+ * scores are scaled by 1/sqrt(hd), causal. Keys and values are rounded to
+ * bf16 (nearest even) when written to the cache. No biases, no QK-norm.
+ *   Wq [n_heads*hd][H/256], Wk, Wv [n_kv*hd][H/256], Wo [H][n_heads*hd/256]:
+ *   Q4_K super-blocks (formats above). g1, g2: fp32 [H].
+ *   moe: the MoE layer (moe.H == H).
+ */
+typedef struct {
+  int H, n_heads, n_kv, head_dim;
+  float rope_theta, eps;
+  const float *g1, *g2;
+  const void *Wq, *Wk, *Wv, *Wo;
+  qmoe_moe_desc moe;
+} qmoe_block_desc;
+
+/* y = RMSNorm(X; gamma) for X, y [T][H] fp32 (y may equal X). */
+int qmoe_rmsnorm(const float *X, const float *gamma, float eps, float *y, int T, int H,
+                 qmoe_stream_t stream);
+
+/*
+ * The attention branch: out = R + O(attention(...)) for rows X [T][H] at
+ * positions pos0 .. pos0+T-1 (R [T][H] or NULL). k_cache, v_cache: bf16 bit
+ * patterns [ctx_cap][n_kv][hd]; positions 0..pos0-1 must hold earlier keys and
+ * values, positions pos0..pos0+T-1 are written. pos0 + T <= ctx_cap.
+ * A rank partial of the head split is this call with that rank's query heads,
+ * KV head(s), cache and O-projection input columns, and R = NULL.
+ */
+size_t qmoe_attn_workspace_bytes(const qmoe_block_desc *b, int T, int pos0);
+int qmoe_attn_forward(const qmoe_block_desc *b, const float *X, const float *R, float *out, int T,
+                      uint16_t *k_cache, uint16_t *v_cache, int pos0, int ctx_cap, void *ws,
+                      size_t ws_bytes, qmoe_stream_t stream);
+
+/* The whole block (out [T][H] fp32, may not alias X). */
+size_t qmoe_block_workspace_bytes(const qmoe_block_desc *b, int T, int pos0);
+int qmoe_block_forward(const qmoe_block_desc *b, const float *X, float *out, int T,
+                       uint16_t *k_cache, uint16_t *v_cache, int pos0, int ctx_cap, void *ws,
+                       size_t ws_bytes, qmoe_stream_t stream);
 
 /* Human-readable text of a status code (static storage). */
 const char *qmoe_status_str(int status);

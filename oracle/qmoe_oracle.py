@@ -305,13 +305,16 @@ def attention_shard_stats(q: np.ndarray, K: np.ndarray, V: np.ndarray):
 
 def attn_sublayer(X: np.ndarray, blk: dict, pos0: int, k_cache: np.ndarray,
                   v_cache: np.ndarray, theta: float = 1e7, eps: float = 1e-6,
-                  rank: int | None = None, n_ranks: int = 2) -> np.ndarray:
+                  rank: int | None = None, n_ranks: int = 2,
+                  rows: np.ndarray | None = None) -> np.ndarray:
     """Attention branch of the block without its residual: O(attn(RoPE(QKV(rms(X))))).
 
     Writes the rows' bf16-rounded keys and values into the float64 caches
     (positions pos0..pos0+T-1). With ``rank`` set, computes that rank's partial:
     query heads [rank*nh/n_ranks, ...), its KV heads, and the matching input
-    columns of the O projection ([CKE-Zip] "What PR #382 Now Splits")."""
+    columns of the O projection ([CKE-Zip] "What PR #382 Now Splits"). With
+    ``rows``, keys and values are still computed and cached for every row but
+    the output is formed only for those query rows."""
     T, H = X.shape
     nh, nkv, d = blk["n_heads"], blk["n_kv"], blk["head_dim"]
     r = rmsnorm(X, blk["g1"], eps)
@@ -325,19 +328,21 @@ def attn_sublayer(X: np.ndarray, blk: dict, pos0: int, k_cache: np.ndarray,
         heads = heads[rank * nh // n_ranks:(rank + 1) * nh // n_ranks]
         kvh = kvh[rank * nkv // n_ranks:(rank + 1) * nkv // n_ranks]
     group = nh // nkv
-    q = (r @ Wq.T).reshape(T, nh, d)[:, heads]
+    if rows is None:
+        rows = np.arange(T)
+    q = (r[rows] @ Wq.T).reshape(len(rows), nh, d)[:, heads]
     kk = (r @ Wk.T).reshape(T, nkv, d)[:, kvh]
     vv = (r @ Wv.T).reshape(T, nkv, d)[:, kvh]
     pos = pos0 + np.arange(T)
-    q = rope(q, pos, theta)
+    q = rope(q, pos[rows], theta)
     kk = rope(kk, pos, theta)
     k_cache[pos0:pos0 + T, kvh] = round_bf16(kk)
     v_cache[pos0:pos0 + T, kvh] = round_bf16(vv)
     # local KV head index for each local query head
     kv_local = np.array([list(kvh).index(h // group) for h in heads])
-    o = attention(q, k_cache[:pos0 + T, kvh], v_cache[:pos0 + T, kvh], pos, kv_local)
+    o = attention(q, k_cache[:pos0 + T, kvh], v_cache[:pos0 + T, kvh], pos[rows], kv_local)
     cols = np.concatenate([np.arange(h * d, (h + 1) * d) for h in heads])
-    return o.reshape(T, len(heads) * d) @ Wo[:, cols].T
+    return o.reshape(len(rows), len(heads) * d) @ Wo[:, cols].T
 
 
 def block_forward(X: np.ndarray, blk: dict, k: int, pos0: int, k_cache: np.ndarray,
@@ -365,3 +370,16 @@ def block_forward(X: np.ndarray, blk: dict, k: int, pos0: int, k_cache: np.ndarr
         m_parts = [moe_forward(r2, blk["moe"], k)]
         out = h1 + m_parts[0]
     return out, {"attn": a_parts, "moe": m_parts, "h1": h1}
+
+
+def block_forward_rows(X: np.ndarray, blk: dict, k: int, pos0: int, k_cache: np.ndarray,
+                       v_cache: np.ndarray, rows: np.ndarray, theta: float = 1e7,
+                       eps: float = 1e-6):
+    """block_forward for the listed query rows only (every row's keys and values
+    still enter the cache; given the cache, rows are independent). Returns
+    (out[rows], moe parts of those rows incl. the routing gap)."""
+    a = attn_sublayer(X, blk, pos0, k_cache, v_cache, theta, eps, rows=rows)
+    h1 = X[rows].astype(np.float64) + a
+    r2 = rmsnorm(h1, blk["g2"], eps)
+    m, parts = moe_forward(r2, blk["moe"], k, return_parts=True)
+    return h1 + m, parts

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libqmoe.so")
 
 Q4K, Q5K = 0, 1
 QTYPE = {"q4k": Q4K, "q5k": Q5K}
-PATH_NAMES = {0: "none", 1: "gemv", 2: "gemm_tc"}
+PATH_NAMES = {0: "none", 1: "gemv", 2: "gemm_tc", 3: "decode"}
 
 _c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 
@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.qmoe_profile_start.argtypes = [_c_int]
         L.qmoe_profile_stop.argtypes = [P(ctypes.c_double), P(_c_int)]
         L.qmoe_moe_forward_noalloc.argtypes = [P(MoeDesc), _vp, _vp, _vp, _c_int, _vp]
+        L.qmoe_get_decode_max_rows.argtypes = []
+        L.qmoe_set_decode_max_rows.argtypes = [_c_int]
+        L.qmoe_set_decode_max_rows.restype = None
         _lib = L
     return _lib
 
@@ -85,7 +88,9 @@ def exported_symbols() -> list[str]:
             "qmoe_moe_route", "qmoe_moe_workspace_bytes", "qmoe_moe_workspace_layout",
             "qmoe_moe_forward", "qmoe_moe_forward_host_workspace_bytes", "qmoe_moe_forward_host",
             "qmoe_launch_count", "qmoe_profile_start", "qmoe_profile_stop",
-            "qmoe_moe_forward_noalloc"]
+            "qmoe_moe_forward_noalloc", "qmoe_get_decode_max_rows", "qmoe_set_decode_max_rows",
+            "qmoe_rmsnorm", "qmoe_attn_workspace_bytes", "qmoe_attn_forward", "qmoe_block_workspace_bytes",
+            "qmoe_block_forward"]
 
 
 def _check(status: int):
@@ -192,7 +197,15 @@ def get_gemm_threshold() -> int:
     return int(lib().qmoe_get_gemm_threshold())
 
 
-STAGES = {"router": 1, "route": 2, "gateup": 3, "down": 4, "combine": 5}
+def set_decode_max_rows(rows: int):
+    lib().qmoe_set_decode_max_rows(int(rows))
+
+
+def get_decode_max_rows() -> int:
+    return int(lib().qmoe_get_decode_max_rows())
+
+
+STAGES = {"router": 1, "route": 2, "gateup": 3, "down": 4, "combine": 5, "decode": 6}
 
 
 def moe_forward_host(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = None,
@@ -243,4 +256,101 @@ def moe_forward_noalloc(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None
         out = torch.empty_like(X)
     _check(lib().qmoe_moe_forward_noalloc(ctypes.byref(layer.desc), _ptr(X), _ptr(R), _ptr(out), T,
                                           _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- block
+
+class BlockDesc(ctypes.Structure):
+    _fields_ = [("H", _c_int), ("n_heads", _c_int), ("n_kv", _c_int), ("head_dim", _c_int),
+                ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float),
+                ("g1", _vp), ("g2", _vp), ("Wq", _vp), ("Wk", _vp), ("Wv", _vp), ("Wo", _vp),
+                ("moe", MoeDesc)]
+
+
+def _block_lib():
+    L = lib()
+    if not getattr(L, "_block_declared", False):
+        P = ctypes.POINTER
+        L.qmoe_rmsnorm.argtypes = [_vp, _vp, ctypes.c_float, _vp, _c_int, _c_int, _vp]
+        L.qmoe_attn_workspace_bytes.restype = _c_size
+        L.qmoe_attn_workspace_bytes.argtypes = [P(BlockDesc), _c_int, _c_int]
+        L.qmoe_attn_forward.argtypes = [P(BlockDesc), _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _vp,
+                                        _c_size, _vp]
+        L.qmoe_block_workspace_bytes.restype = _c_size
+        L.qmoe_block_workspace_bytes.argtypes = [P(BlockDesc), _c_int, _c_int]
+        L.qmoe_block_forward.argtypes = [P(BlockDesc), _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _vp,
+                                         _c_size, _vp]
+        L._block_declared = True
+    return L
+
+
+class Block:
+    """Device-resident weights of one attention + MoE block and its descriptor."""
+
+    def __init__(self, H, n_heads, n_kv, head_dim, g1, g2, Wq, Wk, Wv, Wo, moe: MoeLayer,
+                 rope_theta=1e7, eps=1e-6):
+        self.H, self.n_heads, self.n_kv, self.head_dim = H, n_heads, n_kv, head_dim
+        self.g1, self.g2, self.Wq, self.Wk, self.Wv, self.Wo = g1, g2, Wq, Wk, Wv, Wo
+        self.moe = moe
+        self._desc = BlockDesc(H, n_heads, n_kv, head_dim, rope_theta, eps, _ptr(g1), _ptr(g2), _ptr(Wq),
+                               _ptr(Wk), _ptr(Wv), _ptr(Wo), moe.desc)
+
+    @classmethod
+    def from_arrays(cls, blk: dict, k: int, device="cuda"):
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        moe = MoeLayer.from_arrays(blk["moe"], k, device)
+        return cls(blk["H"], blk["n_heads"], blk["n_kv"], blk["head_dim"], dev(blk["g1"]), dev(blk["g2"]),
+                   dev(blk["Wq"]), dev(blk["Wk"]), dev(blk["Wv"]), dev(blk["Wo"]), moe)
+
+    @property
+    def desc(self) -> BlockDesc:
+        return self._desc
+
+    def attn_workspace(self, T, pos0):
+        n = int(_block_lib().qmoe_attn_workspace_bytes(ctypes.byref(self._desc), T, pos0))
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=self.Wq.device)
+
+    def workspace(self, T, pos0):
+        n = int(_block_lib().qmoe_block_workspace_bytes(ctypes.byref(self._desc), T, pos0))
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=self.Wq.device)
+
+
+def cache_from_bits(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """bf16 cache tensor from uint16 bit patterns (same bytes)."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def rmsnorm(X: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, out=None, stream=None):
+    T, H = X.shape
+    if out is None:
+        out = torch.empty_like(X)
+    _check(_block_lib().qmoe_rmsnorm(_ptr(X), _ptr(gamma), eps, _ptr(out), T, H, _stream(stream)))
+    return out
+
+
+def attn_forward(block: Block, X: torch.Tensor, R: torch.Tensor | None, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, pos0: int, out=None, ws=None, stream=None):
+    """out = R + O(attention(...)) for rows at positions pos0..pos0+T-1 (R may be None)."""
+    T = X.shape[0]
+    if out is None:
+        out = torch.empty_like(X)
+    if ws is None:
+        ws = block.attn_workspace(T, pos0)
+    _check(_block_lib().qmoe_attn_forward(ctypes.byref(block.desc), _ptr(X), _ptr(R), _ptr(out), T,
+                                          _ptr(k_cache), _ptr(v_cache), pos0, k_cache.shape[0], _ptr(ws),
+                                          ws.numel(), _stream(stream)))
+    return out
+
+
+def block_forward(block: Block, X: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pos0: int,
+                  out=None, ws=None, stream=None):
+    T = X.shape[0]
+    if out is None:
+        out = torch.empty_like(X)
+    if ws is None:
+        ws = block.workspace(T, pos0)
+    _check(_block_lib().qmoe_block_forward(ctypes.byref(block.desc), _ptr(X), _ptr(out), T, _ptr(k_cache),
+                                           _ptr(v_cache), pos0, k_cache.shape[0], _ptr(ws), ws.numel(),
+                                           _stream(stream)))
     return out

@@ -17,6 +17,8 @@ std::atomic<int> g_arch_ok[kMaxDevices];     // 0 unknown, 1 sm_103, -1 other
 std::atomic<int*> g_status_ptr[kMaxDevices];
 constexpr int kDefaultGemmThreshold = 64;
 std::atomic<int> g_gemm_threshold{kDefaultGemmThreshold};
+constexpr int kDefaultDecodeRows = 4;
+std::atomic<int> g_decode_max_rows{kDefaultDecodeRows};
 thread_local int g_last_path = QMOE_PATH_NONE;
 std::atomic<long long> g_launches{0};
 
@@ -83,7 +85,7 @@ inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace carve-up (every piece 256-byte aligned).
 struct MoeWs {
-  size_t part, ids, w, offsets, perm, active, n_active, chunk, mtiles, n_mtiles, h, y, total;
+  size_t part, ids, w, offsets, perm, active, n_active, chunk, mtiles, n_mtiles, xb, h, y, total;
   int nsplit;
 };
 
@@ -92,7 +94,9 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   const size_t P = (size_t)T * k, rows = P + T;
   L.nsplit = router_splits(T, H, E);
   size_t o = 0;
-  L.part = o;     o += up256(sizeof(float) * (size_t)L.nsplit * T * E);
+  const int ns_alloc = T <= kDefaultDecodeRows && decode_router_splits(H, E) > L.nsplit
+                           ? decode_router_splits(H, E) : L.nsplit;
+  L.part = o;     o += up256(sizeof(float) * (size_t)ns_alloc * T * E);
   L.ids = o;      o += up256(sizeof(int32_t) * P);
   L.w = o;        o += up256(sizeof(float) * P);
   L.offsets = o;  o += up256(sizeof(int32_t) * (E + 2));
@@ -102,6 +106,7 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   L.chunk = o;    o += up256(sizeof(int32_t) * (size_t)perm_chunks((int)P) * E);
   L.mtiles = o;   o += up256(sizeof(int2) * (size_t)tc_max_mtiles(T, k, E, 1));
   L.n_mtiles = o; o += 256;
+  L.xb = o;       o += up256(sizeof(uint16_t) * (size_t)T * H);
   L.h = o;        o += up256(sizeof(float) * rows * F);
   L.y = o;        o += up256(sizeof(float) * rows * H);
   L.total = o;
@@ -129,9 +134,214 @@ int check_desc(const qmoe_moe_desc* d) {
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? QMOE_OK : QMOE_ERR_LAUNCH; }
 
+// ---------------------------------------------------------------- block
+struct AttnWs {
+  size_t r, q, k, v, o, part, offsets, perm, active, n_active, mtiles, n_mtiles, xb, total;
+  bool chunked;
+};
+
+constexpr int kChunkedAttnRows = 16;
+
+AttnWs attn_ws_layout(const qmoe_block_desc* b, int T, int pos0) {
+  AttnWs L{};
+  const int H = b->H, nh = b->n_heads, nkv = b->n_kv, hd = b->head_dim;
+  const size_t Q = (size_t)nh * hd, KV = (size_t)nkv * hd;
+  L.chunked = T <= kChunkedAttnRows;
+  size_t o = 0;
+  L.r = o;        o += up256(sizeof(float) * T * (size_t)H);
+  L.q = o;        o += up256(sizeof(float) * T * Q);
+  L.k = o;        o += up256(sizeof(float) * T * KV);
+  L.v = o;        o += up256(sizeof(float) * T * KV);
+  L.o = o;        o += up256(sizeof(float) * T * Q);
+  L.part = o;     o += L.chunked ? up256(sizeof(float) * T * (size_t)nh * attn_nchunks(T, pos0) * (hd + 2)) : 0;
+  L.offsets = o;  o += 256;
+  L.perm = o;     o += up256(sizeof(int32_t) * T);
+  L.active = o;   o += 256;
+  L.n_active = o; o += 256;
+  L.mtiles = o;   o += up256(sizeof(int2) * (size_t)tc_max_mtiles(T, 1, 1, 0));
+  L.n_mtiles = o; o += 256;
+  L.xb = o;       o += up256(sizeof(uint16_t) * T * (Q > (size_t)H ? Q : (size_t)H));
+  L.total = o;
+  return L;
+}
+
+int check_block(const qmoe_block_desc* b) {
+  if (!b) return QMOE_ERR_NULL;
+  const int H = b->H, nh = b->n_heads, nkv = b->n_kv, hd = b->head_dim;
+  if (!supported_width(H) || nh < 1 || nkv < 1 || nh % nkv != 0) return QMOE_ERR_ARG;
+  if (hd < 8 || hd > 256 || hd % 8 != 0) return QMOE_ERR_ARG;
+  if (!supported_width(nh * hd) || (nkv * hd) % 16 != 0) return QMOE_ERR_ARG;
+  if (!(b->eps >= 0.f) || !(b->rope_theta > 0.f)) return QMOE_ERR_ARG;
+  if (!b->g1 || !b->g2 || !b->Wq || !b->Wk || !b->Wv || !b->Wo) return QMOE_ERR_NULL;
+  const void* ptrs[] = {b->g1, b->g2, b->Wq, b->Wk, b->Wv, b->Wo};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return QMOE_ERR_ALIGN;
+  return QMOE_OK;
+}
+
+// y [T][N] fp32 = x [T][K] fp32 . W^T for a packed Q4_K/Q5_K matrix W [N][K/256]:
+// the grouped kernels with one "expert" holding all rows.
+cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int N, float* y, char* base,
+                       const AttnWs& L, int* status, cudaStream_t st) {
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+  int32_t* active = reinterpret_cast<int32_t*>(base + L.active);
+  int32_t* n_active = reinterpret_cast<int32_t*>(base + L.n_active);
+  cudaError_t e = launch_dense_route(offsets, perm, active, n_active, T, st);
+  g_launches.fetch_add(1);
+  if (e != cudaSuccess) return e;
+  if (T > g_gemm_threshold.load() && N % 256 == 0) {
+    int2* mtiles = reinterpret_cast<int2*>(base + L.mtiles);
+    int32_t* n_mtiles = reinterpret_cast<int32_t*>(base + L.n_mtiles);
+    __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
+    if ((e = launch_build_mtiles(offsets, 1, mtiles, n_mtiles, st)) != cudaSuccess) return e;
+    if ((e = launch_to_bf16(x, xb, (size_t)T * K, st)) != cudaSuccess) return e;
+    GroupedTcArgs p{};
+    p.W = static_cast<const uint8_t*>(W);
+    p.qt = qt;
+    p.offsets = offsets;
+    p.perm = perm;
+    p.mtiles = mtiles;
+    p.n_mtiles = n_mtiles;
+    p.max_mtiles = tc_max_mtiles(T, 1, 1, 0);
+    p.hin = xb;
+    p.yout_f32 = y;
+    p.T = T;
+    p.k = 1;
+    p.E = 1;
+    p.H = N;
+    p.F = K;
+    p.status = status;
+    g_launches.fetch_add(3);
+    return launch_down_tc(p, st);
+  }
+  GroupedArgs g{};
+  g.W = static_cast<const uint8_t*>(W);
+  g.S = nullptr;
+  g.offsets = offsets;
+  g.perm = perm;
+  g.active = active;
+  g.n_active = n_active;
+  g.T = T;
+  g.k = 1;
+  g.E = 1;
+  g.max_active = 1;
+  g_launches.fetch_add(1);
+  return launch_down_gemv(g, qt, x, K, N, y, st);
+}
+
+int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* out, int T, uint16_t* kc, uint16_t* vc,
+              int pos0, int ctx_cap, void* ws, size_t ws_bytes, cudaStream_t st) {
+  int r = check_block(b);
+  if (r != QMOE_OK) return r;
+  if (T < 0 || pos0 < 0) return QMOE_ERR_ARG;
+  if (T == 0) return QMOE_OK;
+  if ((long long)pos0 + T > ctx_cap) return QMOE_ERR_ARG;
+  if (!X || !out || !kc || !vc || !ws) return QMOE_ERR_NULL;
+  if (!aligned(X, 16) || !aligned(out, 16) || (R && !aligned(R, 16)) || !aligned(kc, 16) || !aligned(vc, 16) ||
+      !aligned(ws, 256))
+    return QMOE_ERR_ALIGN;
+  if (T > kChunkedAttnRows && b->head_dim != 128) return QMOE_ERR_ARG;
+  const AttnWs L = attn_ws_layout(b, T, pos0);
+  if (ws_bytes < L.total) return QMOE_ERR_WORKSPACE;
+  int* status = nullptr;
+  r = device_ready(&status);
+  if (r != QMOE_OK) return r;
+  char* base = static_cast<char*>(ws);
+  float* rr = reinterpret_cast<float*>(base + L.r);
+  float* q = reinterpret_cast<float*>(base + L.q);
+  float* k = reinterpret_cast<float*>(base + L.k);
+  float* v = reinterpret_cast<float*>(base + L.v);
+  float* o = reinterpret_cast<float*>(base + L.o);
+  float* part = reinterpret_cast<float*>(base + L.part);
+  const int H = b->H, nh = b->n_heads, nkv = b->n_kv, hd = b->head_dim;
+  __nv_bfloat16* kcb = reinterpret_cast<__nv_bfloat16*>(kc);
+  __nv_bfloat16* vcb = reinterpret_cast<__nv_bfloat16*>(vc);
+  cudaError_t e = launch_rmsnorm(X, b->g1, b->eps, rr, T, H, st);
+  g_launches.fetch_add(1);
+  if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wq, QMOE_Q4K, nh * hd, q, base, L, status, st);
+  if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wk, QMOE_Q4K, nkv * hd, k, base, L, status, st);
+  if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wv, QMOE_Q4K, nkv * hd, v, base, L, status, st);
+  if (e == cudaSuccess) {
+    e = launch_rope_cache(q, k, v, kcb, vcb, T, pos0, nh, nkv, hd, (double)b->rope_theta, st);
+    g_launches.fetch_add(1);
+  }
+  if (e == cudaSuccess) {
+    e = launch_attention(q, kcb, vcb, part, o, T, pos0, nh, nkv, hd, L.chunked, st);
+    g_launches.fetch_add(L.chunked ? 2 : 1);
+  }
+  float* proj_out = R ? rr : out;  // rr is free once Q, K, V exist
+  if (e == cudaSuccess) e = dense_proj(o, T, nh * hd, b->Wo, QMOE_Q4K, H, proj_out, base, L, status, st);
+  if (e == cudaSuccess && R) {
+    e = launch_add(R, proj_out, out, (size_t)T * H, st);
+    g_launches.fetch_add(1);
+  }
+  return e == cudaSuccess ? QMOE_OK : QMOE_ERR_LAUNCH;
+}
+
 }  // namespace
 
 extern "C" {
+
+int qmoe_rmsnorm(const float* X, const float* gamma, float eps, float* y, int T, int H, qmoe_stream_t stream) {
+  if (T < 0 || H < 1 || !(eps >= 0.f)) return QMOE_ERR_ARG;
+  if (T == 0) return QMOE_OK;
+  if (!X || !gamma || !y) return QMOE_ERR_NULL;
+  int* status = nullptr;
+  int r = device_ready(&status);
+  if (r != QMOE_OK) return r;
+  g_launches.fetch_add(1);
+  return launch_status(launch_rmsnorm(X, gamma, eps, y, T, H, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qmoe_attn_workspace_bytes(const qmoe_block_desc* b, int T, int pos0) {
+  if (check_block(b) != QMOE_OK || T <= 0 || pos0 < 0) return 0;
+  return attn_ws_layout(b, T, pos0).total;
+}
+
+int qmoe_attn_forward(const qmoe_block_desc* b, const float* X, const float* R, float* out, int T,
+                      uint16_t* k_cache, uint16_t* v_cache, int pos0, int ctx_cap, void* ws, size_t ws_bytes,
+                      qmoe_stream_t stream) {
+  return attn_impl(b, X, R, out, T, k_cache, v_cache, pos0, ctx_cap, ws, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t qmoe_block_workspace_bytes(const qmoe_block_desc* b, int T, int pos0) {
+  if (check_block(b) != QMOE_OK || T <= 0 || pos0 < 0) return 0;
+  const size_t moe = qmoe_moe_workspace_bytes(&b->moe, T);
+  if (moe == 0) return 0;
+  return attn_ws_layout(b, T, pos0).total + 2 * up256(sizeof(float) * (size_t)T * b->H) + moe;
+}
+
+int qmoe_block_forward(const qmoe_block_desc* b, const float* X, float* out, int T, uint16_t* k_cache,
+                       uint16_t* v_cache, int pos0, int ctx_cap, void* ws, size_t ws_bytes, qmoe_stream_t stream) {
+  int r = check_block(b);
+  if (r != QMOE_OK) return r;
+  r = check_desc(&b->moe);
+  if (r != QMOE_OK) return r;
+  if (b->moe.H != b->H) return QMOE_ERR_ARG;
+  if (T < 0 || pos0 < 0) return QMOE_ERR_ARG;
+  if (T == 0) return QMOE_OK;
+  if (X == out) return QMOE_ERR_ARG;
+  if (!ws) return QMOE_ERR_NULL;
+  if (!aligned(ws, 256)) return QMOE_ERR_ALIGN;
+  const size_t need = qmoe_block_workspace_bytes(b, T, pos0);
+  if (ws_bytes < need) return QMOE_ERR_WORKSPACE;
+  const size_t a_bytes = attn_ws_layout(b, T, pos0).total;
+  const size_t row_bytes = up256(sizeof(float) * (size_t)T * b->H);
+  char* base = static_cast<char*>(ws);
+  float* h1 = reinterpret_cast<float*>(base + a_bytes);
+  float* r2 = reinterpret_cast<float*>(base + a_bytes + row_bytes);
+  char* moe_ws = base + a_bytes + 2 * row_bytes;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  r = attn_impl(b, X, X, h1, T, k_cache, v_cache, pos0, ctx_cap, base, a_bytes, st);
+  if (r != QMOE_OK) return r;
+  g_launches.fetch_add(1);
+  if (launch_rmsnorm(h1, b->g2, b->eps, r2, T, b->H, st) != cudaSuccess) return QMOE_ERR_LAUNCH;
+  return qmoe_moe_forward(&b->moe, r2, h1, nullptr, nullptr, out, T, moe_ws, ws_bytes - a_bytes - 2 * row_bytes,
+                          stream);
+}
+
 
 const char* qmoe_status_str(int s) {
   switch (s) {
@@ -165,6 +375,10 @@ int qmoe_query_status(qmoe_stream_t stream) {
 int qmoe_get_gemm_threshold(void) { return g_gemm_threshold.load(); }
 void qmoe_set_gemm_threshold(int rows) { g_gemm_threshold.store(rows < 0 ? kDefaultGemmThreshold : rows); }
 int qmoe_last_path(void) { return g_last_path; }
+int qmoe_get_decode_max_rows(void) { return g_decode_max_rows.load(); }
+void qmoe_set_decode_max_rows(int rows) {
+  g_decode_max_rows.store(rows < 0 ? kDefaultDecodeRows : (rows > kDefaultDecodeRows ? kDefaultDecodeRows : rows));
+}
 
 size_t qmoe_moe_route_workspace_bytes(int T, int H, int E, int k) {
   (void)k;
@@ -252,6 +466,37 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
   const int P = T * k;
 
   cudaError_t e = cudaSuccess;
+  if (ids == nullptr && T <= g_decode_max_rows.load() &&
+      decode_path_supported(T, H, E, k, F, d->gate_type, d->down_type)) {
+    DecodeLaunch D{};
+    D.X = X;
+    D.R = R;
+    D.out = out;
+    D.Wr = d->Wr;
+    D.Wg = static_cast<const uint8_t*>(d->Wg);
+    D.Wu = static_cast<const uint8_t*>(d->Wu);
+    D.Wd = static_cast<const uint8_t*>(d->Wd);
+    D.Sg = static_cast<const uint8_t*>(d->Sg);
+    D.Su = static_cast<const uint8_t*>(d->Su);
+    D.Sd = static_cast<const uint8_t*>(d->Sd);
+    D.T = T;
+    D.H = H;
+    D.E = E;
+    D.k = k;
+    D.F = F;
+    D.gate_qt = d->gate_type;
+    D.down_qt = d->down_type;
+    D.part = part;
+    D.hbuf = hbuf;
+    D.ybuf = y;
+    D.ids = ws_ids;
+    D.w = ws_w;
+    D.status = status;
+    e = staged(QMOE_STAGE_DECODE, 3, st, [&] { return launch_decode(D, st); });
+    if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
+    g_last_path = QMOE_PATH_DECODE;
+    return QMOE_OK;
+  }
   const bool small = P <= 2048;
   if (ids == nullptr) {
     e = staged(QMOE_STAGE_ROUTER, 1, st,
@@ -292,7 +537,12 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     int32_t* n_mtiles = reinterpret_cast<int32_t*>(base + L.n_mtiles);
     __nv_bfloat16* h16 = reinterpret_cast<__nv_bfloat16*>(hbuf);
     __nv_bfloat16* y16 = reinterpret_cast<__nv_bfloat16*>(y);
-    e = staged(QMOE_STAGE_ROUTE, 1, st, [&] { return launch_build_mtiles(offsets, E, mtiles, n_mtiles, st); });
+    __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
+    e = staged(QMOE_STAGE_ROUTE, 2, st, [&] {
+      cudaError_t e2 = launch_build_mtiles(offsets, E, mtiles, n_mtiles, st);
+      if (e2 != cudaSuccess) return e2;
+      return launch_to_bf16(X, xb, (size_t)T * H, st);
+    });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
     GroupedTcArgs p{};
     p.offsets = offsets;
@@ -312,6 +562,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     p.S2 = static_cast<const uint8_t*>(d->Su);
     p.qt = d->gate_type;
     p.X = X;
+    p.xb = xb;
     p.hout = h16;
     e = staged(QMOE_STAGE_GATEUP, 1, st, [&] { return launch_gateup_tc(p, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
@@ -399,7 +650,7 @@ int qmoe_moe_forward_host(const qmoe_moe_desc* d, const float* X_host, const flo
 long long qmoe_launch_count(void) { return g_launches.load(); }
 
 int qmoe_profile_start(int stage) {
-  if (stage < 0 || stage > QMOE_STAGE_COMBINE) return QMOE_ERR_ARG;
+  if (stage < 0 || stage > QMOE_STAGE_DECODE) return QMOE_ERR_ARG;
   g_prof.stage = stage;
   g_prof.n = 0;
   return QMOE_OK;

@@ -1,0 +1,394 @@
+// Kernels of the attention + MoE block around the routed-MoE layer.
+//
+// "CKE Zip: From Splitting Tokens To Splitting Qwen3.5 Weights", "What PR #382
+// Now Splits": one Qwen3.5 block with full attention (16 query heads, 2 KV
+// heads) and the MoE layer, recombined as attention + residual, routing on the
+// whole state, MoE + residual. "Distributed CPU: Zip Fusion Beyond Tensor
+// Parallelism", "Two-Dimensional Attention at Long Context": attention over
+// context shards merged exactly from each shard's (max, normaliser, weighted
+// output) -- used here inside one GPU by the split-context decode kernel.
+#include "kernels.cuh"
+
+namespace qmoe {
+
+// ---------------------------------------------------------------------------
+// RMSNorm: y = x / sqrt(mean(x^2) + eps) * gamma, one CTA per row.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                                      float eps, float* __restrict__ y, int H) {
+  __shared__ float red[8];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const float* xr = x + (size_t)t * H;
+  float s = 0.f;
+  for (int i = tid; i < H; i += 256) s = fmaf(xr[i], xr[i], s);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if ((tid & 31) == 0) red[tid >> 5] = s;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / (float)H + eps);
+  for (int i = tid; i < H; i += 256) y[(size_t)t * H + i] = xr[i] * inv * gamma[i];
+}
+
+// Routing of a dense projection seen as one expert (index 0) holding all rows.
+__global__ void dense_route_kernel(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T; i += gridDim.x * blockDim.x) perm[i] = i;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    offsets[0] = 0;
+    offsets[1] = T;
+    offsets[2] = T;
+    active[0] = 0;
+    n_active[0] = 1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Rotate-half RoPE on q [T][nh][hd] (in place) and k [T][nkv][hd]; the rotated
+// keys and the values are written to the bf16 caches at positions pos0 + t.
+// Angles pos * theta^(-2i/hd) and their sines and cosines are taken in double
+// (positions reach thousands of radians).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rope_cache_kernel(float* __restrict__ q, const float* __restrict__ k,
+                                                         const float* __restrict__ v, __nv_bfloat16* __restrict__ kc,
+                                                         __nv_bfloat16* __restrict__ vc, int pos0, int nh, int nkv,
+                                                         int hd, double theta) {
+  extern __shared__ float cs[];  // [hd/2] cos, [hd/2] sin
+  const int t = blockIdx.x, tid = threadIdx.x, half = hd / 2;
+  const int pos = pos0 + t;
+  for (int i = tid; i < half; i += 256) {
+    const double inv = pow(theta, -2.0 * (double)i / (double)hd);
+    double sn, cn;
+    sincos((double)pos * inv, &sn, &cn);
+    cs[i] = (float)cn;
+    cs[half + i] = (float)sn;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < nh * half; idx += 256) {
+    const int h = idx / half, i = idx % half;
+    float* r = q + ((size_t)t * nh + h) * hd;
+    const float a = r[i], b = r[i + half], c = cs[i], s = cs[half + i];
+    r[i] = a * c - b * s;
+    r[i + half] = b * c + a * s;
+  }
+  for (int idx = tid; idx < nkv * half; idx += 256) {
+    const int h = idx / half, i = idx % half;
+    const float* r = k + ((size_t)t * nkv + h) * hd;
+    const float a = r[i], b = r[i + half], c = cs[i], s = cs[half + i];
+    __nv_bfloat16* dst = kc + ((size_t)pos * nkv + h) * hd;
+    dst[i] = __float2bfloat16_rn(a * c - b * s);
+    dst[i + half] = __float2bfloat16_rn(b * c + a * s);
+  }
+  for (int idx = tid; idx < nkv * hd; idx += 256) {
+    const int h = idx / hd, d = idx % hd;
+    vc[((size_t)pos * nkv + h) * hd + d] = __float2bfloat16_rn(v[((size_t)t * nkv + h) * hd + d]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-context attention for few query rows: CTA (row t, head h, chunk c)
+// scores the chunk's 256 cache positions (causal: <= pos0 + t), and writes the
+// chunk's (max m, normaliser l, weighted sum o[hd]) for the exact merge.
+// ---------------------------------------------------------------------------
+constexpr int ATT_CHUNK = 256;
+
+__global__ void __launch_bounds__(256) attn_chunk_kernel(const float* __restrict__ q,
+                                                         const __nv_bfloat16* __restrict__ kc,
+                                                         const __nv_bfloat16* __restrict__ vc,
+                                                         float* __restrict__ part, int pos0, int nh, int nkv,
+                                                         int hd, int nchunks) {
+  extern __shared__ float sm[];
+  float* qs = sm;          // [hd]
+  float* ps = sm + hd;     // [ATT_CHUNK]
+  __shared__ float red[8];
+  __shared__ float stat[2];
+  const int tid = threadIdx.x;
+  const int th = blockIdx.x, c = blockIdx.y;
+  const int t = th / nh, h = th % nh, g = h / (nh / nkv);
+  const int nvalid = pos0 + t + 1;
+  const int j0 = c * ATT_CHUNK;
+  float* out = part + ((size_t)th * nchunks + c) * (hd + 2);
+  if (j0 >= nvalid) {
+    for (int d = tid; d < hd + 2; d += 256) out[d] = (d == 0) ? -INFINITY : 0.f;
+    return;
+  }
+  const float scale = rsqrtf((float)hd);
+  for (int d = tid; d < hd; d += 256) qs[d] = q[((size_t)t * nh + h) * hd + d] * scale;
+  __syncthreads();
+  const int j = j0 + tid;
+  float s = -INFINITY;
+  if (tid < ATT_CHUNK && j < nvalid) {
+    const uint4* kr = reinterpret_cast<const uint4*>(kc + ((size_t)j * nkv + g) * hd);
+    float acc = 0.f;
+    for (int i = 0; i < hd / 8; ++i) {
+      const uint4 u = __ldg(kr + i);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float2 f = __bfloat1622float2(b2[m]);
+        acc = fmaf(qs[8 * i + 2 * m], f.x, acc);
+        acc = fmaf(qs[8 * i + 2 * m + 1], f.y, acc);
+      }
+    }
+    s = acc;
+  }
+  // chunk max
+  float mx = s;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  if (tid == 0) {
+    float m = red[0];
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+    stat[0] = m;
+  }
+  __syncthreads();
+  const float m = stat[0];
+  const float p = (s == -INFINITY) ? 0.f : __expf(s - m);
+  ps[tid] = p;
+  float l = p;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  __syncthreads();
+  if ((tid & 31) == 0) red[tid >> 5] = l;
+  __syncthreads();
+  if (tid == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    stat[1] = tot;
+  }
+  const int nk = min(ATT_CHUNK, nvalid - j0);
+  for (int d = tid; d < hd; d += 256) {
+    const __nv_bfloat16* vp = vc + ((size_t)j0 * nkv + g) * hd + d;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < nk; ++i) acc = fmaf(ps[i], __bfloat162float(vp[(size_t)i * nkv * hd]), acc);
+    out[2 + d] = acc;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    out[0] = m;
+    out[1] = stat[1];
+  }
+}
+
+// Exact merge of the chunks of one (row, head): rescale every chunk to the
+// common maximum, then o = sum(o_c e^(m_c - M)) / sum(l_c e^(m_c - M)).
+__global__ void attn_merge_kernel(const float* __restrict__ part, float* __restrict__ o, int nchunks, int hd) {
+  const int th = blockIdx.x;
+  const float* pc = part + (size_t)th * nchunks * (hd + 2);
+  float M = -INFINITY;
+  for (int c = 0; c < nchunks; ++c)
+    if (pc[(size_t)c * (hd + 2) + 1] > 0.f) M = fmaxf(M, pc[(size_t)c * (hd + 2)]);
+  for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+    float L = 0.f, acc = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+      const float* q = pc + (size_t)c * (hd + 2);
+      if (q[1] > 0.f) {
+        const float sc = __expf(q[0] - M);
+        L = fmaf(q[1], sc, L);
+        acc = fmaf(q[2 + d], sc, acc);
+      }
+    }
+    o[(size_t)th * hd + d] = acc / L;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Causal attention for many query rows: CTA (64-row q tile, head) walks 64-key
+// tiles with an online softmax. fp32 SIMT; K and V come from the bf16 caches.
+// ---------------------------------------------------------------------------
+constexpr int PF_BQ = 64, PF_BK = 64, PF_HD = 128;
+
+__global__ void __launch_bounds__(256) attn_prefill_kernel(const float* __restrict__ q,
+                                                           const __nv_bfloat16* __restrict__ kc,
+                                                           const __nv_bfloat16* __restrict__ vc,
+                                                           float* __restrict__ o, int T, int pos0, int nh, int nkv) {
+  extern __shared__ float sm[];
+  float* Qs = sm;                          // [64][128]
+  float* Ks = Qs + PF_BQ * PF_HD;          // [64][129]
+  float* Vs = Ks + PF_BK * (PF_HD + 1);    // [64][128]
+  float* Ps = Vs + PF_BK * PF_HD;          // [64][65]
+  float* mrow = Ps + PF_BQ * (PF_BK + 1);  // [64]
+  float* lrow = mrow + PF_BQ;              // [64]
+  float* arow = lrow + PF_BQ;              // [64]
+  const int tid = threadIdx.x;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // heavy (late) tiles first
+  const int h = blockIdx.y, g = h / (nh / nkv);
+  const int t0 = qt * PF_BQ;
+  const float scale = rsqrtf((float)PF_HD);
+  for (int i = tid; i < PF_BQ * PF_HD; i += 256) {
+    const int r = i / PF_HD, d = i % PF_HD;
+    const int t = t0 + r;
+    Qs[i] = t < T ? q[((size_t)t * nh + h) * PF_HD + d] * scale : 0.f;
+  }
+  if (tid < PF_BQ) {
+    mrow[tid] = -INFINITY;
+    lrow[tid] = 0.f;
+  }
+  const int ro = tid >> 2, co = (tid & 3) * 32;  // output row and 32 columns of this thread
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  const int last_row = min(T - 1, t0 + PF_BQ - 1);
+  const int kend = pos0 + last_row + 1;  // keys [0, kend)
+  const int tr = tid >> 4, tc = tid & 15;  // S block: rows tr*4.., keys tc*4..
+  for (int k0 = 0; k0 < kend; k0 += PF_BK) {
+    __syncthreads();
+    for (int i = tid; i < PF_BK * PF_HD / 8; i += 256) {
+      const int r = i / (PF_HD / 8), c8 = i % (PF_HD / 8);
+      const int j = k0 + r;
+      float kv[8], vv[8];
+      if (j < kend) {
+        const uint4 ku = __ldg(reinterpret_cast<const uint4*>(kc + ((size_t)j * nkv + g) * PF_HD) + c8);
+        const uint4 vu = __ldg(reinterpret_cast<const uint4*>(vc + ((size_t)j * nkv + g) * PF_HD) + c8);
+        const __nv_bfloat162* kb = reinterpret_cast<const __nv_bfloat162*>(&ku);
+        const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&vu);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float2 a = __bfloat1622float2(kb[m]), b = __bfloat1622float2(vb[m]);
+          kv[2 * m] = a.x;
+          kv[2 * m + 1] = a.y;
+          vv[2 * m] = b.x;
+          vv[2 * m + 1] = b.y;
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) kv[m] = vv[m] = 0.f;
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        Ks[r * (PF_HD + 1) + 8 * c8 + m] = kv[m];
+        Vs[r * PF_HD + 8 * c8 + m] = vv[m];
+      }
+    }
+    __syncthreads();
+    // S = Q K^T for a 4x4 block
+    float s[4][4] = {};
+    for (int d = 0; d < PF_HD; ++d) {
+      float qa[4], kb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qa[i] = Qs[(tr * 4 + i) * PF_HD + d];
+        kb[i] = Ks[(tc * 4 + i) * (PF_HD + 1) + d];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qa[i], kb[j], s[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = tr * 4 + i, key = k0 + tc * 4 + j;
+        const bool ok = (t0 + r < T) && (key <= pos0 + t0 + r) && (key < kend);
+        Ps[r * (PF_BK + 1) + tc * 4 + j] = ok ? s[i][j] : -INFINITY;
+      }
+    __syncthreads();
+    if (tid < PF_BQ) {
+      const int r = tid;
+      float mx = mrow[r];
+      for (int j = 0; j < PF_BK; ++j) mx = fmaxf(mx, Ps[r * (PF_BK + 1) + j]);
+      const float alpha = (mrow[r] == -INFINITY) ? 0.f : __expf(mrow[r] - mx);
+      float lsum = 0.f;
+      for (int j = 0; j < PF_BK; ++j) {
+        const float sv = Ps[r * (PF_BK + 1) + j];
+        const float p = (sv == -INFINITY) ? 0.f : __expf(sv - mx);
+        Ps[r * (PF_BK + 1) + j] = p;
+        lsum += p;
+      }
+      lrow[r] = lrow[r] * alpha + lsum;
+      mrow[r] = mx;
+      arow[r] = alpha;
+    }
+    __syncthreads();
+    const float al = arow[ro];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] *= al;
+    for (int j = 0; j < PF_BK; ++j) {
+      const float p = Ps[ro * (PF_BK + 1) + j];
+      const float4* v4 = reinterpret_cast<const float4*>(Vs + j * PF_HD + co);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 v = v4[i];
+        acc[4 * i] = fmaf(p, v.x, acc[4 * i]);
+        acc[4 * i + 1] = fmaf(p, v.y, acc[4 * i + 1]);
+        acc[4 * i + 2] = fmaf(p, v.z, acc[4 * i + 2]);
+        acc[4 * i + 3] = fmaf(p, v.w, acc[4 * i + 3]);
+      }
+    }
+  }
+  __syncthreads();
+  const int t = t0 + ro;
+  if (t < T) {
+    const float inv = 1.f / lrow[ro];
+    float* dst = o + ((size_t)t * nh + h) * PF_HD + co;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) dst[i] = acc[i] * inv;
+  }
+}
+
+__global__ void add_kernel(const float* __restrict__ a, const float* __restrict__ b, float* __restrict__ y, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    y[i] = a[i] + b[i];
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, float* y, int T, int H, cudaStream_t st) {
+  rmsnorm_kernel<<<T, 256, 0, st>>>(x, gamma, eps, y, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dense_route(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T,
+                               cudaStream_t st) {
+  int blocks = (T + 255) / 256;
+  if (blocks > 64) blocks = 64;
+  dense_route_kernel<<<blocks, 256, 0, st>>>(offsets, perm, active, n_active, T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_cache(float* q, const float* k, const float* v, __nv_bfloat16* kc, __nv_bfloat16* vc, int T,
+                              int pos0, int nh, int nkv, int hd, double theta, cudaStream_t st) {
+  rope_cache_kernel<<<T, 256, sizeof(float) * hd, st>>>(q, k, v, kc, vc, pos0, nh, nkv, hd, theta);
+  return cudaGetLastError();
+}
+
+int attn_nchunks(int T, int pos0) { return (pos0 + T + ATT_CHUNK - 1) / ATT_CHUNK; }
+
+cudaError_t launch_attention(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* part, float* o,
+                             int T, int pos0, int nh, int nkv, int hd, bool chunked, cudaStream_t st) {
+  if (chunked) {
+    const int nc = attn_nchunks(T, pos0);
+    attn_chunk_kernel<<<dim3(T * nh, nc), 256, sizeof(float) * (hd + ATT_CHUNK), st>>>(q, kc, vc, part, pos0, nh,
+                                                                                          nkv, hd, nc);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    attn_merge_kernel<<<T * nh, 128, 0, st>>>(part, o, nc, hd);
+    return cudaGetLastError();
+  }
+  if (hd != PF_HD) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(float) * (PF_BQ * PF_HD + PF_BK * (PF_HD + 1) + PF_BK * PF_HD + PF_BQ * (PF_BK + 1) +
+                                       3 * PF_BQ);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  attn_prefill_kernel<<<dim3((T + PF_BQ - 1) / PF_BQ, nh), 256, smem, st>>>(q, kc, vc, o, T, pos0, nh, nkv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaStream_t st) {
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  add_kernel<<<blocks, 256, 0, st>>>(a, b, y, n);
+  return cudaGetLastError();
+}
+
+}  // namespace qmoe

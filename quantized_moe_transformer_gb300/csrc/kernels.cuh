@@ -49,9 +49,11 @@ struct GroupedTcArgs {
   const int32_t* n_mtiles;
   int max_mtiles;
   const float* X;
+  const __nv_bfloat16* xb;
   const __nv_bfloat16* hin;
   __nv_bfloat16* hout;
   __nv_bfloat16* yout;
+  float* yout_f32;  // down pass: write fp32 instead of bf16 when not null
   int T, k, E, H, F;
   int* status;
 };
@@ -60,7 +62,38 @@ cudaError_t launch_build_mtiles(const int32_t* offsets, int E, int2* mtiles, int
                                 cudaStream_t st);
 cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st);
 cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st);
+cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, size_t n, cudaStream_t st);
 cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* w, const float* R, float* out,
                                 int T, int H, int k, int has_shared, cudaStream_t st);
+
+// block.cu: the attention + MoE block's other kernels.
+cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, float* y, int T, int H, cudaStream_t st);
+cudaError_t launch_dense_route(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T,
+                               cudaStream_t st);
+cudaError_t launch_rope_cache(float* q, const float* k, const float* v, __nv_bfloat16* kc, __nv_bfloat16* vc, int T,
+                              int pos0, int nh, int nkv, int hd, double theta, cudaStream_t st);
+int attn_nchunks(int T, int pos0);
+cudaError_t launch_attention(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* part, float* o,
+                             int T, int pos0, int nh, int nkv, int hd, bool chunked, cudaStream_t st);
+cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaStream_t st);
+
+// moe_decode.cu: three PDL-chained kernels for T <= 4.
+struct DecodeLaunch {
+  const float* X;
+  const float* R;
+  float* out;
+  const float* Wr;
+  const uint8_t *Wg, *Wu, *Wd, *Sg, *Su, *Sd;
+  int T, H, E, k, F, gate_qt, down_qt;
+  float* part;
+  float* hbuf;
+  float* ybuf;
+  int32_t* ids;
+  float* w;
+  int* status;
+};
+int decode_router_splits(int H, int E);
+bool decode_path_supported(int T, int H, int E, int k, int F, int gate_qt, int down_qt);
+cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st);
 
 }  // namespace qmoe

@@ -10,14 +10,18 @@
 // Splitting Qwen3.5 Weights": gate, up, SwiGLU and down per expert).
 //
 // One persistent CTA per SM walks work items (m-tile of 128 rows of one expert,
-// n-tile of 256 output columns). Warp roles (288 threads):
-//   warps 0-3  epilogue: TMEM -> registers (warp w reads lanes 32w..32w+31),
-//              fused SwiGLU (gate/up) or bf16 store (down);
-//   warps 4-7  producers: gather the 128 activation rows of the k-tile as
-//              bf16 and dequantise the 256 weight rows, both written in the
-//              128-byte-swizzled K-major layout the MMA descriptors describe;
-//   warp 8     allocates 512 TMEM columns (two 256-column accumulators) and
-//              issues the MMAs from one lane.
+// n-tile of 256 output columns). Warp roles (416 threads):
+//   warps 0-3   epilogue: TMEM -> registers (warp w reads lanes 32w..32w+31),
+//               fused SwiGLU (gate/up) or bf16 store (down);
+//   warps 4-11  producers: thread p owns weight row p of the n-tile; it keeps
+//               the packed super-block of its row in registers, prefetching
+//               the next super-block (or the next work item's first one)
+//               while it dequantises the current one to bf16; threads 0..127
+//               also gather activation row p of the k-tile (bf16) with
+//               cp.async. Both operands are written in the 128-byte-swizzled
+//               K-major layout the MMA descriptors describe;
+//   warp 12     allocates 512 TMEM columns (two 256-column accumulators) and
+//               issues the MMAs from one lane.
 // A 4-stage shared-memory ring (48 KB per stage) decouples producers and the
 // MMA issuer; the two accumulators let the epilogue of one tile overlap the
 // main loop of the next. Every wait is bounded: on time-out the CTA records
@@ -28,7 +32,9 @@
 namespace qmoe {
 
 constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
-constexpr int TC_THREADS = 288;
+constexpr int TC_THREADS = 416;
+constexpr int TC_MMA_WARP = 12;
+constexpr int TC_PRODUCERS = 256;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 32 KB
 constexpr int TC_SMEM = TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
@@ -43,56 +49,87 @@ struct TcArgs {
   const int2* mtiles;  // (expert, first row) per m-tile
   const int32_t* n_mtiles;
   const float* X;               // gate/up A source, [T][H] fp32
+  const __nv_bfloat16* xb;      // gate/up A source, [T][H] bf16 (converted X)
   const __nv_bfloat16* hin;     // down A source, [P+T][F] bf16
   __nv_bfloat16* hout;          // gate/up output, [P+T][F] bf16
   __nv_bfloat16* yout;          // down output, [P+T][H] bf16
+  float* yout_f32;              // down output in fp32 instead, when not null
   int T, k, E, H, F;
   int* status;
 };
 
 __device__ __forceinline__ int tc_pair_row(int p, int T, int k) { return p < T * k ? p / k : p - T * k; }
 
-// Dequantises 8 consecutive weights (word ``w`` of a sub-block's quants, high
-// bits ``hb8`` for Q5_K) as d*s*q - dmin*m and packs them as 4 bf16x2 words.
+// Packed super-block of one weight row held in registers (16-byte chunks).
 template <int QT>
-__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t hb8, float ds, float dm) {
-  float v[8];
+struct RawBlock {
+  static constexpr int N = (QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES) / 16;
+  uint4 c[N];
+};
+
+template <int QT>
+__device__ __forceinline__ void load_raw(RawBlock<QT>& r, const uint8_t* blk) {
+  const uint4* p = reinterpret_cast<const uint4*>(blk);
 #pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    uint32_t q = (w >> (4 * b)) & 15u;
-    if (QT == QMOE_Q5K) q |= ((hb8 >> b) & 1u) << 4;
-    v[b] = fmaf(ds, (float)q, -dm);
-  }
-  uint4 o;
-  o.x = tc::pack_bf16x2(v[0], v[1]);
-  o.y = tc::pack_bf16x2(v[2], v[3]);
-  o.z = tc::pack_bf16x2(v[4], v[5]);
-  o.w = tc::pack_bf16x2(v[6], v[7]);
-  return o;
+  for (int i = 0; i < RawBlock<QT>::N; ++i) r.c[i] = __ldg(p + i);
 }
 
-// Writes the 64 dequantised weights of k-tile ``kt`` of one packed row into
-// row ``r`` of a swizzled B stage.
-template <int QT>
-__device__ __forceinline__ void produce_b_row(const uint8_t* row, int kt, uint8_t* stage, int r) {
-  constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
-  const uint8_t* blk = row + (size_t)(kt >> 2) * BYTES;
-  const int j0 = (kt & 3) * 2;
-  const KHeader h = load_header(blk);
+// Dequantises sub-blocks j0, j0+1 (64 weights, w = d*s*q - dmin*m) of a
+// register-held super-block and stores them as 8 swizzled 16-byte bf16
+// chunks of row ``r`` of a B stage. Each quant byte becomes the float
+// 0.5 + q/256 through one byte permute; w = 256*ds*f - (128*ds + dm).
+template <int QT, int J0>
+__device__ __forceinline__ void dequant_store(const RawBlock<QT>& raw, uint8_t* stage, int r) {
+  KHeader h;
+  const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&raw.c[0].x));
+  h.d = dd.x;
+  h.dmin = dd.y;
+  h.f0 = raw.c[0].y;
+  h.f1 = raw.c[0].z;
+  h.f2 = raw.c[0].w;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    const int j = j0 + s;
+    constexpr int unused = 0;
+    (void)unused;
+    const int j = J0 + s;
     const float2 sc = sub_scale(h, j);
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(blk + quant_offset(QT, j)));
-    const uint32_t hb = QT == QMOE_Q5K ? __ldg(reinterpret_cast<const uint32_t*>(blk + 16 + 4 * j)) : 0u;
+    const float a = 256.f * sc.x, b = -(128.f * sc.x + sc.y);
+    const uint4 q = QT == QMOE_Q5K ? raw.c[3 + j] : raw.c[1 + j];
+    uint32_t hb = 0;
+    if (QT == QMOE_Q5K) {
+      const uint4 hq = raw.c[1 + (j >> 2)];
+      const uint32_t hw[4] = {hq.x, hq.y, hq.z, hq.w};
+      hb = hw[j & 3];
+    }
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint4 o = dequant8<QT>(w[c], hb >> (8 * c), sc.x, sc.y);
-      *reinterpret_cast<uint4*>(stage + tc::sw128_offset(r, 4 * s + c)) = o;
+    for (int n = 0; n < 4; ++n) {
+      uint32_t ev = w[n] & 0x0F0F0F0Fu;
+      uint32_t od = (w[n] >> 4) & 0x0F0F0F0Fu;
+      if (QT == QMOE_Q5K) {
+        ev |= spread4(hb >> (8 * n), 0);
+        od |= spread4(hb >> (8 * n), 1);
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t sel = 0x7044u | ((uint32_t)k << 8);
+        const float fe = fmaf(a, __uint_as_float(__byte_perm(ev, 0x3F000000u, sel)), b);
+        const float fo = fmaf(a, __uint_as_float(__byte_perm(od, 0x3F000000u, sel)), b);
+        o[k] = tc::pack_bf16x2(fe, fo);
+      }
+      *reinterpret_cast<uint4*>(stage + tc::sw128_offset(r, 4 * s + n)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t n = valid ? 16u : 0u;  // 0: fill the 16 bytes with zeros, read nothing
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 template <bool GATEUP, int QT>
 __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
@@ -116,7 +153,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < TC_STAGES; ++i) {
-      tc::mbar_init(&full[i], 128);
+      tc::mbar_init(&full[i], TC_PRODUCERS);
       tc::mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -127,7 +164,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 8) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == TC_MMA_WARP) tc::tmem_alloc(tmem_slot, 512);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -170,10 +207,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
       } else {
         const int pair = valid ? g.perm[pos] : 0;
         __nv_bfloat16* dst = g.yout + (size_t)pair * g.H + nt * TC_BN;
+        float* dst32 = g.yout_f32 ? g.yout_f32 + (size_t)pair * g.H + nt * TC_BN : nullptr;
 #pragma unroll 1
         for (int c = 0; c < TC_BN; c += 32) {
           uint32_t a[16], b[16];
           tc::tmem_ld16x2(tq + c, tq + c + 16, a, b);
+          if (g.yout_f32 != nullptr) {
+            if (valid) {
+              float4* d4 = reinterpret_cast<float4*>(dst32 + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
+                                    __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[4 + i] = make_float4(__uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]),
+                                        __uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]));
+            }
+            continue;
+          }
           uint32_t o[16];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -192,77 +244,75 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
       tc::tc_fence_before();
       tc::mbar_arrive(&acc_empty[acc]);
     }
-  } else if (warp < 8) {
+  } else if (warp < 4 + TC_PRODUCERS / 32) {
     // ------------------------------------------------------------ producers
-    const int p = threadIdx.x - 128;  // A row and B rows p, p + 128
+    constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
+    const int p = threadIdx.x - 128;  // weight row p of the n-tile; activation row p (< 128)
+    const int KB = KT / 4;            // super-blocks along K
+    const size_t rb = GATEUP ? (size_t)(g.H / QK) * BYTES : (size_t)(g.F / QK) * BYTES;
+    // packed row of work item wi for this thread
+    auto row_of = [&](int wi) -> const uint8_t* {
+      const int2 mt = g.mtiles[wi / NT];
+      const int nt = wi % NT, e = mt.x;
+      if (GATEUP) {
+        const bool up = p >= 128;
+        const uint8_t* base = e < g.E ? (up ? g.W2 : g.W) + (size_t)e * g.F * rb : (up ? g.S2 : g.S);
+        return base + (size_t)(nt * 128 + (p & 127)) * rb;
+      }
+      const uint8_t* base = e < g.E ? g.W + (size_t)e * g.H * rb : g.S;
+      return base + (size_t)(nt * TC_BN + p) * rb;
+    };
+    RawBlock<QT> cur, nxt;
+    int wi = blockIdx.x;
+    if (wi < total) load_raw<QT>(cur, row_of(wi));
     int stage = 0;
     uint32_t phase = 0;
-    for (int wi = blockIdx.x; wi < total; wi += gridDim.x) {
+    bool ok = true;
+    for (; wi < total && ok; wi += gridDim.x) {
       const int2 mt = g.mtiles[wi / NT];
-      const int nt = wi % NT;
       const int e = mt.x, m0 = mt.y;
       const int base = g.offsets[e];
       const int Me = g.offsets[e + 1] - base;
-      const bool valid = m0 + p < Me;
-      const int pos = base + m0 + p;
-      const float* xa = nullptr;
-      const __nv_bfloat16* ha = nullptr;
-      if (valid) {
-        if (GATEUP) xa = g.X + (size_t)tc_pair_row(g.perm[pos], g.T, g.k) * g.H;
-        else ha = g.hin + (size_t)pos * g.F;
-      }
-      const uint8_t *b0, *b1;
-      if (GATEUP) {
-        const size_t rb = (size_t)(g.H / QK) * (QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES);
-        const uint8_t* wg = e < g.E ? g.W + (size_t)e * g.F * rb : g.S;
-        const uint8_t* wu = e < g.E ? g.W2 + (size_t)e * g.F * rb : g.S2;
-        b0 = wg + (size_t)(nt * 128 + p) * rb;
-        b1 = wu + (size_t)(nt * 128 + p) * rb;
-      } else {
-        const size_t rb = (size_t)(g.F / QK) * (QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES);
-        const uint8_t* wd = e < g.E ? g.W + (size_t)e * g.H * rb : g.S;
-        b0 = wd + (size_t)(nt * TC_BN + p) * rb;
-        b1 = wd + (size_t)(nt * TC_BN + 128 + p) * rb;
-      }
-      bool ok = true;
-      for (int kt = 0; kt < KT; ++kt) {
-        if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint8_t* a_st = sA + stage * TC_A_BYTES;
-        uint8_t* b_st = sB + stage * TC_B_BYTES;
-        // A row p: 64 activations of k-tile kt as bf16
-        if (GATEUP) {
-          const float4* src = reinterpret_cast<const float4*>(xa + kt * TC_BK);
+      const int pa = p & 127;
+      const bool valid = (p < 128) && (m0 + pa < Me);
+      const int pos = base + m0 + pa;
+      const __nv_bfloat16* arow = GATEUP ? g.xb : g.hin;  // zero-fill reads nothing
+      if (valid)
+        arow = GATEUP ? g.xb + (size_t)tc_pair_row(g.perm[pos], g.T, g.k) * g.H : g.hin + (size_t)pos * g.F;
+      const uint8_t* brow = row_of(wi);
+      for (int sb = 0; sb < KB && ok; ++sb) {
+        // prefetch the next packed super-block of this row (or of the next item)
+        if (sb + 1 < KB) load_raw<QT>(nxt, brow + (size_t)(sb + 1) * BYTES);
+        else if (wi + (int)gridDim.x < total) load_raw<QT>(nxt, row_of(wi + gridDim.x));
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (valid) {
-              float4 u = __ldg(src + 2 * c), v = __ldg(src + 2 * c + 1);
-              o = make_uint4(tc::pack_bf16x2(u.x, u.y), tc::pack_bf16x2(u.z, u.w),
-                             tc::pack_bf16x2(v.x, v.y), tc::pack_bf16x2(v.z, v.w));
-            }
-            *reinterpret_cast<uint4*>(a_st + tc::sw128_offset(p, c)) = o;
+        for (int kk = 0; kk < 4; ++kk) {
+          const int kt = 4 * sb + kk;
+          if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
           }
-        } else {
-          const uint4* src = reinterpret_cast<const uint4*>(ha + kt * TC_BK);
+          uint8_t* a_st = sA + stage * TC_A_BYTES;
+          uint8_t* b_st = sB + stage * TC_B_BYTES;
+          if (p < 128) {
+            const __nv_bfloat16* src = arow + (valid ? kt * TC_BK : 0);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 o = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(a_st + tc::sw128_offset(p, c)) = o;
+            for (int c = 0; c < 8; ++c) cp_async16(a_st + tc::sw128_offset(p, c), src + (valid ? 8 * c : 0), valid);
+            cp_async_commit();
+          }
+          if (kk == 0) dequant_store<QT, 0>(cur, b_st, p);
+          else if (kk == 1) dequant_store<QT, 2>(cur, b_st, p);
+          else if (kk == 2) dequant_store<QT, 4>(cur, b_st, p);
+          else dequant_store<QT, 6>(cur, b_st, p);
+          if (p < 128) cp_async_wait_all();
+          tc::fence_proxy_async_smem();
+          tc::mbar_arrive(&full[stage]);
+          if (++stage == TC_STAGES) {
+            stage = 0;
+            phase ^= 1;
           }
         }
-        produce_b_row<QT>(b0, kt, b_st, p);
-        produce_b_row<QT>(b1, kt, b_st, p + 128);
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&full[stage]);
-        if (++stage == TC_STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
+        cur = nxt;
       }
-      if (!ok) break;
     }
   } else {
     // ------------------------------------------------------------ MMA issuer
@@ -315,7 +365,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 8) tc::tmem_dealloc(tmem, 512);
+  if (warp == TC_MMA_WARP) tc::tmem_dealloc(tmem, 512);
 }
 
 // Builds the m-tile list: for every expert with rows (the shared expert last),
@@ -395,6 +445,26 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
   }
 }
 
+// X [T][H] fp32 -> bf16 (round to nearest even), the A operand of gate/up.
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y,
+                                                      size_t n4) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(x)[i];
+    uint2 o;
+    o.x = tc::pack_bf16x2(v.x, v.y);
+    o.y = tc::pack_bf16x2(v.z, v.w);
+    reinterpret_cast<uint2*>(y)[i] = o;
+  }
+}
+
+cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, size_t n, cudaStream_t st) {
+  const size_t n4 = n / 4;
+  int blocks = (int)((n4 + 255) / 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  to_bf16_kernel<<<blocks, 256, 0, st>>>(x, y, n4);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 int tc_num_sms() {
   static int n = 0;
@@ -438,7 +508,7 @@ cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st) {
   TcArgs a{};
   a.W = p.W; a.W2 = p.W2; a.S = p.S; a.S2 = p.S2;
   a.offsets = p.offsets; a.perm = p.perm; a.mtiles = p.mtiles; a.n_mtiles = p.n_mtiles;
-  a.X = p.X; a.hout = p.hout;
+  a.X = p.X; a.xb = p.xb; a.hout = p.hout;
   a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
   const int items = p.max_mtiles * (p.F / 128);
   return p.qt == QMOE_Q5K ? tc_launch_t<true, QMOE_Q5K>(a, items, st) : tc_launch_t<true, QMOE_Q4K>(a, items, st);
@@ -448,7 +518,7 @@ cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
   TcArgs a{};
   a.W = p.W; a.S = p.S;
   a.offsets = p.offsets; a.perm = p.perm; a.mtiles = p.mtiles; a.n_mtiles = p.n_mtiles;
-  a.hin = p.hin; a.yout = p.yout;
+  a.hin = p.hin; a.yout = p.yout; a.yout_f32 = p.yout_f32;
   a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
   const int items = p.max_mtiles * (p.H / TC_BN);
   return p.qt == QMOE_Q5K ? tc_launch_t<false, QMOE_Q5K>(a, items, st) : tc_launch_t<false, QMOE_Q4K>(a, items, st);

@@ -135,8 +135,8 @@ __global__ void __launch_bounds__(256) gateup_gemv_kernel(GroupedArgs g, const u
       load_x32(x + c * SUBK, xv, xs);
 #pragma unroll
       for (int p = 0; p < PASSES; ++p) {
-        ag[p] += pg[p][j].sc.x * dot_sub<QT>(pg[p][j].q, pg[p][j].hb, xv) - pg[p][j].sc.y * xs;
-        au[p] += pu[p][j].sc.x * dot_sub<QT>(pu[p][j].q, pu[p][j].hb, xv) - pu[p][j].sc.y * xs;
+        ag[p] += sub_contrib(dot_sub_prmt<QT>(pg[p][j].q, pg[p][j].hb, xv), xs, pg[p][j].sc);
+        au[p] += sub_contrib(dot_sub_prmt<QT>(pu[p][j].q, pu[p][j].hb, xv), xs, pu[p][j].sc);
       }
     }
 #pragma unroll
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(256) down_gemv_kernel(GroupedArgs g, const flo
       load_x32(x + c * SUBK, xv, xs);
 #pragma unroll
       for (int p = 0; p < PASSES; ++p)
-        acc[p] += pd[p][j].sc.x * dot_sub<QT>(pd[p][j].q, pd[p][j].hb, xv) - pd[p][j].sc.y * xs;
+        acc[p] += sub_contrib(dot_sub_prmt<QT>(pd[p][j].q, pd[p][j].hb, xv), xs, pd[p][j].sc);
     }
 #pragma unroll
     for (int p = 0; p < PASSES; ++p) {

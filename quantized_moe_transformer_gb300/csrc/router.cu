@@ -83,10 +83,19 @@ __device__ __forceinline__ void warp_topk_row(const float* part, int nsplit, int
   float v[EPL];
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
-    int e = lane + 32 * j;
+    const int e = lane + 32 * j;
     float s = 0.f;
     if (e < E) {
-      for (int sp = 0; sp < nsplit; ++sp) s += part[((size_t)sp * T + t) * E + e];
+      // the split partials are loaded 16 at a time (independent loads in
+      // flight) and added in split order
+      for (int s0 = 0; s0 < nsplit; s0 += 16) {
+        float pv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          pv[q] = (s0 + q < nsplit) ? __ldcg(part + ((size_t)(s0 + q) * T + t) * E + e) : 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) s += pv[q];
+      }
     }
     v[j] = (e < E) ? s : -INFINITY;
   }

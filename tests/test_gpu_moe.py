@@ -85,7 +85,7 @@ def test_tiny_layer(oracle, seed, R_mode):
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_decode_layer(oracle, seed):
     run_and_check(oracle, seed, 1, R_mode="x")
-    assert qb.last_path() == "gemv"
+    assert qb.last_path() == "decode"
 
 
 @pytest.mark.parametrize("routing", ["uniform", "zipf"])
@@ -158,7 +158,12 @@ def test_stagewise_expert_outputs(oracle):
     T = 2
     X = inputs.hidden(11, T, 2048)
     ws = lay.workspace(T)
-    qb.moe_forward(lay, torch.from_numpy(X).cuda(), ws=ws)
+    qb.set_decode_max_rows(0)
+    try:
+        qb.moe_forward(lay, torch.from_numpy(X).cuda(), ws=ws)
+        assert qb.last_path() == "gemv"
+    finally:
+        qb.set_decode_max_rows(-1)
     torch.cuda.synchronize()
     L = lay.workspace_layout(T)
     rows = T * k + T
@@ -256,3 +261,61 @@ def test_tensor_core_path_bit_identical():
     b = qb.moe_forward(lay, X)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("routing", ["uniform", "zipf"])
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_decode_path_matches_gemv_path(oracle, T, routing):
+    """The PDL-chained decode path and the grouped GEMV path on the same rows;
+    both against the oracle; the decode path's routes and per-pair outputs."""
+    arr, lay, k = layer_pair(1, routing)
+    X = inputs.hidden(31 + T, T, 2048, routing)
+    R = inputs.residual(5, T, 2048)
+    Xd, Rd = torch.from_numpy(X).cuda(), torch.from_numpy(R).cuda()
+    ws = lay.workspace(T)
+    a = qb.moe_forward(lay, Xd, Rd, ws=ws)
+    assert qb.last_path() == "decode"
+    torch.cuda.synchronize()
+    L = lay.workspace_layout(T)
+    ids = ws[L.ids:L.ids + 4 * T * k].view(torch.int32).reshape(T, k).cpu().numpy()
+    w = ws[L.w:L.w + 4 * T * k].view(torch.float32).reshape(T, k).cpu().numpy()
+    rows = T * k + T
+    y = ws[L.y:L.y + 4 * rows * 2048].view(torch.float32).reshape(rows, 2048).cpu().numpy()
+    qb.set_decode_max_rows(0)
+    try:
+        b = qb.moe_forward(lay, Xd, Rd)
+        assert qb.last_path() == "gemv"
+    finally:
+        qb.set_decode_max_rows(-1)
+    torch.cuda.synchronize()
+    assert_close(a.cpu().numpy(), b.cpu().numpy(), TOL_GEMV)
+    ref, parts = oracle.moe_forward(X, arr, k, R, return_parts=True)
+    ok = check_routes(ids, parts["ids"], parts["gap"], parts["logits"])
+    assert_close(a.cpu().numpy(), ref, TOL_GEMV, rows=ok)
+    np.testing.assert_allclose(w[ok], parts["w"][ok], rtol=0, atol=2e-6)
+    for t in np.nonzero(ok)[0]:
+        for s2 in range(k):
+            assert_close(y[t * k + s2], parts["y"][t, s2], TOL_GEMV)
+        assert_close(y[T * k + t], parts["y_shared"][t], TOL_GEMV)
+
+
+def test_decode_path_bit_identical_and_chained():
+    """Run to run bit identity, and a chain of layers where each output is the
+    next input (the previous kernel's output read after the PDL wait)."""
+    arr, lay, k = layer_pair(2)
+    X = torch.from_numpy(inputs.hidden(8, 1, 2048)).cuda()
+    a = qb.moe_forward(lay, X, X)
+    b = qb.moe_forward(lay, X, X)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    h1 = qb.moe_forward(lay, X, X)
+    h2 = qb.moe_forward(lay, h1 / h1.abs().max(), h1 / h1.abs().max())
+    torch.cuda.synchronize()
+    qb.set_decode_max_rows(0)
+    try:
+        g1 = qb.moe_forward(lay, X, X)
+        g2 = qb.moe_forward(lay, g1 / g1.abs().max(), g1 / g1.abs().max())
+    finally:
+        qb.set_decode_max_rows(-1)
+    torch.cuda.synchronize()
+    assert_close(h2.cpu().numpy(), g2.cpu().numpy(), TOL_GEMV)

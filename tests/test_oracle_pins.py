@@ -360,3 +360,14 @@ def test_block_decode_step_matches_prefill_row(oracle):
     oracle.block_forward(X[:4], blk, 2, 0, kc2, vc2)
     last, _ = oracle.block_forward(X[4:], blk, 2, 4, kc2, vc2)
     assert np.allclose(last[0], full[4], rtol=1e-12, atol=1e-12 * np.abs(full).max())
+
+
+def test_block_rows_restriction(oracle):
+    """Evaluating only some query rows gives those rows of the full block."""
+    blk, X = _small_block(2, T=7, ctx=16)
+    kc = oracle.bf16_bits_to_f64(blk["k_cache"])
+    vc = oracle.bf16_bits_to_f64(blk["v_cache"])
+    full, _ = oracle.block_forward(X, blk, 2, 3, kc.copy(), vc.copy())
+    rows = np.array([0, 4, 6])
+    part, _ = oracle.block_forward_rows(X, blk, 2, 3, kc.copy(), vc.copy(), rows)
+    assert np.max(np.abs(part - full[rows])) <= 1e-12 * np.max(np.abs(full))
