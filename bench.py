@@ -63,6 +63,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     p.add_argument("--layers", type=int, default=16)
+    p.add_argument("--T", type=int, default=None, help="override the workload's row count")
+    p.add_argument("--routing", choices=["uniform", "zipf"], default=None)
     p.add_argument("--gemm-threshold", type=int, default=None,
                    help="rows above which the tensor-core path is taken (library default if unset)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -270,6 +272,10 @@ def ours_main(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     wl = WORKLOADS[args.workload]
     T, routing = wl["T"], wl["routing"]
+    if args.T is not None:
+        T = args.T
+    if args.routing is not None:
+        routing = args.routing
     NL = args.layers
     peaks = {}
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/qmoe.h"
+#include "qmoe.h"
 
 namespace qmoe {
 

@@ -31,13 +31,22 @@
 
 namespace qmoe {
 
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64;
 constexpr int TC_THREADS = 416;
 constexpr int TC_MMA_WARP = 12;
 constexpr int TC_PRODUCERS = 256;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 32 KB
-constexpr int TC_SMEM = TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
+// Per weight format: RS stages of packed super-blocks (256 rows each, filled by
+// bulk copies) and BS stages of bf16 operand tiles, within 227 KB.
+template <int QT>
+struct TcCfg {
+  static constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
+  static constexpr int RS = 2;
+  static constexpr int BS = QT == QMOE_Q5K ? 2 : 3;
+  static constexpr int RAW_STAGE = TC_PRODUCERS * BYTES;
+  static constexpr int SMEM = BS * (TC_A_BYTES + TC_B_BYTES) + RS * RAW_STAGE + 1024 /*align*/ + 256 /*barriers*/;
+};
 
 struct TcArgs {
   const uint8_t* W;   // gate (gate/up pass) or down weights of the routed experts
@@ -135,12 +144,16 @@ template <bool GATEUP, int QT>
 __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using Cfg = TcCfg<QT>;
+  constexpr int BS = Cfg::BS, RS = Cfg::RS;
   uint8_t* sA = smem;
-  uint8_t* sB = smem + TC_STAGES * TC_A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + TC_STAGES * TC_B_BYTES);
-  uint64_t* full = bars;                     // [STAGES]
-  uint64_t* empty = bars + TC_STAGES;        // [STAGES]
-  uint64_t* acc_full = bars + 2 * TC_STAGES; // [2]
+  uint8_t* sB = smem + BS * TC_A_BYTES;
+  uint8_t* sRaw = sB + BS * TC_B_BYTES;              // [RS][256 rows][BYTES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + RS * Cfg::RAW_STAGE);
+  uint64_t* full = bars;                     // [BS]
+  uint64_t* empty = bars + BS;               // [BS]
+  uint64_t* raw_full = bars + 2 * BS;        // [RS]
+  uint64_t* acc_full = raw_full + RS;        // [2]
   uint64_t* acc_empty = acc_full + 2;        // [2]
   uint64_t* drain = acc_empty + 2;           // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -152,10 +165,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
   const int total = g.n_mtiles[0] * NT;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < TC_STAGES; ++i) {
+    for (int i = 0; i < BS; ++i) {
       tc::mbar_init(&full[i], TC_PRODUCERS);
       tc::mbar_init(&empty[i], 1);
     }
+    for (int i = 0; i < RS; ++i) tc::mbar_init(&raw_full[i], TC_PRODUCERS);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
       tc::mbar_init(&acc_empty[i], 128);
@@ -246,11 +260,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
     }
   } else if (warp < 4 + TC_PRODUCERS / 32) {
     // ------------------------------------------------------------ producers
-    constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
-    const int p = threadIdx.x - 128;  // weight row p of the n-tile; activation row p (< 128)
-    const int KB = KT / 4;            // super-blocks along K
+    // Thread p owns weight row p of the n-tile (and, p < 128, activation row
+    // p). Packed super-blocks of its row arrive by bulk copy into a ring of RS
+    // stages, RS super-blocks ahead of use; the activation row of the next
+    // k-tile is gathered with cp.async while the current k-tile is
+    // dequantised; each k-tile's operand stage is released with one arrive.
+    constexpr int BYTES = Cfg::BYTES;
+    const int p = threadIdx.x - 128;
+    const int KB = KT / 4;  // super-blocks along K
     const size_t rb = GATEUP ? (size_t)(g.H / QK) * BYTES : (size_t)(g.F / QK) * BYTES;
-    // packed row of work item wi for this thread
+    const int n_mine = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    auto item = [&](int j) { return (int)blockIdx.x + j * (int)gridDim.x; };
     auto row_of = [&](int wi) -> const uint8_t* {
       const int2 mt = g.mtiles[wi / NT];
       const int nt = wi % NT, e = mt.x;
@@ -262,58 +282,78 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
       const uint8_t* base = e < g.E ? g.W + (size_t)e * g.H * rb : g.S;
       return base + (size_t)(nt * TC_BN + p) * rb;
     };
-    RawBlock<QT> cur, nxt;
-    int wi = blockIdx.x;
-    if (wi < total) load_raw<QT>(cur, row_of(wi));
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (; wi < total && ok; wi += gridDim.x) {
+    // activation row p of item j, or nullptr (rows past the expert's count read zeros)
+    auto arow_of = [&](int wi) -> const __nv_bfloat16* {
       const int2 mt = g.mtiles[wi / NT];
       const int e = mt.x, m0 = mt.y;
       const int base = g.offsets[e];
-      const int Me = g.offsets[e + 1] - base;
-      const int pa = p & 127;
-      const bool valid = (p < 128) && (m0 + pa < Me);
-      const int pos = base + m0 + pa;
-      const __nv_bfloat16* arow = GATEUP ? g.xb : g.hin;  // zero-fill reads nothing
-      if (valid)
-        arow = GATEUP ? g.xb + (size_t)tc_pair_row(g.perm[pos], g.T, g.k) * g.H : g.hin + (size_t)pos * g.F;
-      const uint8_t* brow = row_of(wi);
-      for (int sb = 0; sb < KB && ok; ++sb) {
-        // prefetch the next packed super-block of this row (or of the next item)
-        if (sb + 1 < KB) load_raw<QT>(nxt, brow + (size_t)(sb + 1) * BYTES);
-        else if (wi + (int)gridDim.x < total) load_raw<QT>(nxt, row_of(wi + gridDim.x));
+      if (m0 + p >= g.offsets[e + 1] - base) return nullptr;
+      const int pos = base + m0 + p;
+      return GATEUP ? g.xb + (size_t)tc_pair_row(g.perm[pos], g.T, g.k) * g.H : g.hin + (size_t)pos * g.F;
+    };
+    auto issue_raw = [&](int u) {
+      const int j = u / KB;
+      if (j >= n_mine) return;
+      uint64_t* bar = &raw_full[u % RS];
+      tc::mbar_expect_tx(bar, BYTES);
+      tc::bulk_g2s(sRaw + (size_t)(u % RS) * Cfg::RAW_STAGE + (size_t)p * BYTES,
+                   row_of(item(j)) + (size_t)(u % KB) * BYTES, BYTES, bar);
+    };
+    const int n_kt = n_mine * KT;
+    const __nv_bfloat16* a_cur = nullptr;  // activation row of the k-tile being gathered
+    auto issue_a = [&](int kg) {
+      const int kt = kg % KT;
+      if (kt == 0) a_cur = p < 128 ? arow_of(item(kg / KT)) : nullptr;
+      if (p < 128) {
+        uint8_t* a_st = sA + (kg % BS) * TC_A_BYTES;
+        const bool valid = a_cur != nullptr;
+        const __nv_bfloat16* src = valid ? a_cur + kt * TC_BK : g.hin ? g.hin : g.xb;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int kt = 4 * sb + kk;
-          if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+        for (int c = 0; c < 8; ++c) cp_async16(a_st + tc::sw128_offset(p, c), src + (valid ? 8 * c : 0), valid);
+      }
+      cp_async_commit();
+    };
+    for (int u = 0; u < RS; ++u) issue_raw(u);
+    bool ok = true;
+    if (n_kt > 0) {
+      if (!tc::mbar_wait(&empty[0], 1, abort_flag)) ok = false;
+      else issue_a(0);
+    }
+    int kg = 0;
+    for (int u = 0; u < n_mine * KB && ok; ++u) {
+      if (!tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      RawBlock<QT> cur;
+      const uint4* rp = reinterpret_cast<const uint4*>(sRaw + (size_t)(u % RS) * Cfg::RAW_STAGE + (size_t)p * BYTES);
+#pragma unroll
+      for (int i = 0; i < RawBlock<QT>::N; ++i) cur.c[i] = rp[i];
+      tc::fence_proxy_async_smem();  // these reads come before the copy that refills the slot
+      issue_raw(u + RS);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint8_t* b_st = sB + (kg % BS) * TC_B_BYTES;
+        if (kk == 0) dequant_store<QT, 0>(cur, b_st, p);
+        else if (kk == 1) dequant_store<QT, 2>(cur, b_st, p);
+        else if (kk == 2) dequant_store<QT, 4>(cur, b_st, p);
+        else dequant_store<QT, 6>(cur, b_st, p);
+        if (kg + 1 < n_kt) {
+          if (!tc::mbar_wait(&empty[(kg + 1) % BS], (((kg + 1) / BS) & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-          uint8_t* a_st = sA + stage * TC_A_BYTES;
-          uint8_t* b_st = sB + stage * TC_B_BYTES;
-          if (p < 128) {
-            const __nv_bfloat16* src = arow + (valid ? kt * TC_BK : 0);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) cp_async16(a_st + tc::sw128_offset(p, c), src + (valid ? 8 * c : 0), valid);
-            cp_async_commit();
-          }
-          if (kk == 0) dequant_store<QT, 0>(cur, b_st, p);
-          else if (kk == 1) dequant_store<QT, 2>(cur, b_st, p);
-          else if (kk == 2) dequant_store<QT, 4>(cur, b_st, p);
-          else dequant_store<QT, 6>(cur, b_st, p);
-          if (p < 128) cp_async_wait_all();
-          tc::fence_proxy_async_smem();
-          tc::mbar_arrive(&full[stage]);
-          if (++stage == TC_STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          issue_a(kg + 1);
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+          cp_async_wait_all();
         }
-        cur = nxt;
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&full[kg % BS]);
+        ++kg;
       }
     }
+    cp_async_wait_all();
   } else {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = tc::idesc_bf16_f32(TC_BM, TC_BN);
@@ -344,7 +384,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
           tc::mma_commit(&empty[stage]);
         }
         __syncwarp();
-        if (++stage == TC_STAGES) {
+        if (++stage == BS) {
           stage = 0;
           phase ^= 1;
         }
@@ -493,14 +533,14 @@ static cudaError_t tc_launch_t(const TcArgs& a, int max_items, cudaStream_t st) 
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(moe_tc_kernel<GATEUP, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TC_SMEM);
+                                         TcCfg<QT>::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   int grid = tc_num_sms();
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
-  moe_tc_kernel<GATEUP, QT><<<grid, TC_THREADS, TC_SMEM, st>>>(a);
+  moe_tc_kernel<GATEUP, QT><<<grid, TC_THREADS, TcCfg<QT>::SMEM, st>>>(a);
   return cudaGetLastError();
 }
 
