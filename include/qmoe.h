@@ -271,6 +271,10 @@ int qmoe_block_forward(const qmoe_block_desc *b, const float *X, float *out, int
                        uint16_t *k_cache, uint16_t *v_cache, int pos0, int ctx_cap, void *ws,
                        size_t ws_bytes, qmoe_stream_t stream);
 
+/* The CUDA runtime error code (cudaError_t) behind the last QMOE_ERR_LAUNCH
+ * returned on this thread, 0 if none. */
+int qmoe_last_cuda_error(void);
+
 /* Human-readable text of a status code (static storage). */
 const char *qmoe_status_str(int status);
 

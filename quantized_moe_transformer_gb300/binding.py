@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         L.qmoe_profile_start.argtypes = [_c_int]
         L.qmoe_profile_stop.argtypes = [P(ctypes.c_double), P(_c_int)]
         L.qmoe_moe_forward_noalloc.argtypes = [P(MoeDesc), _vp, _vp, _vp, _c_int, _vp]
+        L.qmoe_last_cuda_error.argtypes = []
         L.qmoe_get_decode_max_rows.argtypes = []
         L.qmoe_set_decode_max_rows.argtypes = [_c_int]
         L.qmoe_set_decode_max_rows.restype = None
@@ -89,13 +90,16 @@ def exported_symbols() -> list[str]:
             "qmoe_moe_forward", "qmoe_moe_forward_host_workspace_bytes", "qmoe_moe_forward_host",
             "qmoe_launch_count", "qmoe_profile_start", "qmoe_profile_stop",
             "qmoe_moe_forward_noalloc", "qmoe_get_decode_max_rows", "qmoe_set_decode_max_rows",
-            "qmoe_rmsnorm", "qmoe_attn_workspace_bytes", "qmoe_attn_forward", "qmoe_block_workspace_bytes",
+            "qmoe_last_cuda_error", "qmoe_rmsnorm", "qmoe_attn_workspace_bytes", "qmoe_attn_forward", "qmoe_block_workspace_bytes",
             "qmoe_block_forward"]
 
 
 def _check(status: int):
     if status != 0:
-        raise QmoeError(f"qmoe status {status}: {lib().qmoe_status_str(status).decode()}")
+        msg = f"qmoe status {status}: {lib().qmoe_status_str(status).decode()}"
+        if status == -6:
+            msg += f" (cudaError {int(lib().qmoe_last_cuda_error())})"
+        raise QmoeError(msg)
 
 
 def _ptr(t: torch.Tensor | None):

@@ -20,6 +20,7 @@ std::atomic<int> g_gemm_threshold{kDefaultGemmThreshold};
 constexpr int kDefaultDecodeRows = 4;
 std::atomic<int> g_decode_max_rows{kDefaultDecodeRows};
 thread_local int g_last_path = QMOE_PATH_NONE;
+thread_local int g_last_cuda_error = 0;
 std::atomic<long long> g_launches{0};
 
 // Opt-in per-stage timing: events recorded around every launch of one stage.
@@ -49,6 +50,7 @@ cudaError_t staged(int stage, int n_kernels, cudaStream_t st, F&& launch) {
   }
   cudaError_t e = launch();
   g_launches.fetch_add(n_kernels);
+  if (e != cudaSuccess) g_last_cuda_error = (int)e;
   if (prof) {
     cudaEventRecord(g_prof.stop[g_prof.n], st);
     ++g_prof.n;
@@ -94,9 +96,7 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   const size_t P = (size_t)T * k, rows = P + T;
   L.nsplit = router_splits(T, H, E);
   size_t o = 0;
-  const int ns_alloc = T <= kDefaultDecodeRows && decode_router_splits(H, E) > L.nsplit
-                           ? decode_router_splits(H, E) : L.nsplit;
-  L.part = o;     o += up256(sizeof(float) * (size_t)ns_alloc * T * E);
+  L.part = o;     o += up256(sizeof(float) * (size_t)L.nsplit * T * E);
   L.ids = o;      o += up256(sizeof(int32_t) * P);
   L.w = o;        o += up256(sizeof(float) * P);
   L.offsets = o;  o += up256(sizeof(int32_t) * (E + 2));
@@ -132,7 +132,11 @@ int check_desc(const qmoe_moe_desc* d) {
   return QMOE_OK;
 }
 
-int launch_status(cudaError_t e) { return e == cudaSuccess ? QMOE_OK : QMOE_ERR_LAUNCH; }
+int launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return QMOE_OK;
+  g_last_cuda_error = (int)e;
+  return QMOE_ERR_LAUNCH;
+}
 
 // ---------------------------------------------------------------- block
 struct AttnWs {
@@ -276,7 +280,7 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
     e = launch_add(R, proj_out, out, (size_t)T * H, st);
     g_launches.fetch_add(1);
   }
-  return e == cudaSuccess ? QMOE_OK : QMOE_ERR_LAUNCH;
+  return launch_status(e);
 }
 
 }  // namespace
@@ -375,6 +379,7 @@ int qmoe_query_status(qmoe_stream_t stream) {
 int qmoe_get_gemm_threshold(void) { return g_gemm_threshold.load(); }
 void qmoe_set_gemm_threshold(int rows) { g_gemm_threshold.store(rows < 0 ? kDefaultGemmThreshold : rows); }
 int qmoe_last_path(void) { return g_last_path; }
+int qmoe_last_cuda_error(void) { return g_last_cuda_error; }
 int qmoe_get_decode_max_rows(void) { return g_decode_max_rows.load(); }
 void qmoe_set_decode_max_rows(int rows) {
   g_decode_max_rows.store(rows < 0 ? kDefaultDecodeRows : (rows > kDefaultDecodeRows ? kDefaultDecodeRows : rows));

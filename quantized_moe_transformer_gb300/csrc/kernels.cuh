@@ -92,7 +92,6 @@ struct DecodeLaunch {
   float* w;
   int* status;
 };
-int decode_router_splits(int H, int E);
 bool decode_path_supported(int T, int H, int E, int k, int F, int gate_qt, int down_qt);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st);
 

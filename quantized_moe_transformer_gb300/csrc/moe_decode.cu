@@ -8,20 +8,23 @@
 // Decode Result Shows Why Axis Choice Matters": with one row the independent
 // work is the eight selected routes, merged in selected-slot order.
 //
-//   K1 router     NS CTAs, each streams a contiguous slab of Wr rows into shared
-//                 memory (bulk async copy issued before waiting on the previous
-//                 grid) and writes partial logits part[c][t][e].
+//   K1 router     one CTA per 8 experts: its threads load their Wr rows' 32
+//                 bytes for those experts before waiting on the previous grid,
+//                 then reduce x . Wr over all of H in a fixed order and write
+//                 the final logits l[t][e] (no partials left to combine).
 //   K2 gate/up    one CTA per (expert slot, 32 intermediate rows). The shared
 //                 expert's CTAs start their weight copies before the router has
-//                 finished; every CTA then reduces the router partials in a fixed
-//                 order, takes the top-k itself (no separate routing kernel) and
-//                 streams its expert's rows. Output h per (row, slot) pair.
-//   K3 down       one CTA per 8 output rows. It routes again from the partials,
+//                 finished; every CTA then takes the top-k of the logits itself
+//                 (no separate routing kernel) and streams its expert's rows.
+//                 Output h per (row, slot) pair.
+//   K3 down       one CTA per 8 output rows. It routes again from the logits,
 //                 streams its 8 rows of every selected expert's down matrix
 //                 while K2 is still running, then waits for h, and forms
 //                 out = R + y_shared + sum_s w_s y_s in slot order.
 // Every CTA reaches the same routing decision from the same partials; every
 // wait on a copy is bounded and records QMOE_ERR_TIMEOUT on expiry.
+#include <mutex>
+
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -37,8 +40,8 @@ struct DecodeArgs {
   float* out;
   const float* Wr;
   const uint8_t *Wg, *Wu, *Wd, *Sg, *Su, *Sd;
-  int T, H, E, k, F, has_shared, NS;
-  float* part;     // [NS][T][E]
+  int T, H, E, k, F, has_shared;
+  float* logits;   // [T][E]
   float* hbuf;     // [T*k + T][F], indexed by pair (t*k + s; shared T*k + t)
   float* ybuf;     // [T*k + T][H]
   int32_t* ids;    // [T][k]
@@ -59,37 +62,24 @@ struct RouteSmem {
 
 __device__ void decode_route(const DecodeArgs& a, float* logits /*[T][E]*/, int32_t* mark /*[E]*/,
                              RouteSmem& rs) {
+  __shared__ float cand_v[8][16];
+  __shared__ int32_t cand_e[8][16];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, E = a.E, k = a.k;
-  // the NS partials of a logit are loaded 32 at a time (independent loads in
-  // flight) and summed in a fixed order
-  for (int i = tid; i < T * E; i += DEC_THREADS) {
-    float s = 0.f;
-    for (int c0 = 0; c0 < a.NS; c0 += 32) {
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        v[j] = (c0 + j < a.NS) ? __ldcg(a.part + (size_t)(c0 + j) * T * E + i) : 0.f;
-#pragma unroll
-      for (int w2 = 16; w2 > 0; w2 >>= 1)
-#pragma unroll
-        for (int j = 0; j < w2; ++j) v[j] += v[j + w2];
-      s += v[0];
-    }
-    logits[i] = s;
-  }
+  for (int i = tid; i < T * E; i += DEC_THREADS) logits[i] = __ldcg(a.logits + i);
   for (int e = tid; e < E; e += DEC_THREADS) mark[e] = 0;
   __syncthreads();
-  if (warp < T) {
-    // lane l holds experts l + 32j (j < 32: E <= 1024); taken is a bit mask
-    // over j, so each round is one pass over the lane's entries
-    const float* L = logits + warp * E;
+  // two-level top-k per row: each warp takes the top k of its eighth of the
+  // experts (lane l holds experts w*32 + l + 256j), then warp 0 merges the 8k
+  // candidates. Order: larger logit first, lower index on ties.
+  for (int t = 0; t < T; ++t) {
+    const float* L = logits + t * E;
     uint32_t taken = 0;
     for (int r = 0; r < k; ++r) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
-      for (int j = 0; j * 32 < E; ++j) {
-        const int e = lane + 32 * j;
+      for (int j = 0; warp * 32 + 256 * j < E; ++j) {
+        const int e = warp * 32 + lane + 256 * j;
         if (e < E && !((taken >> j) & 1u)) {
           const float v = L[e];
           if (v > bv || (v == bv && e < be)) {
@@ -100,31 +90,73 @@ __device__ void decode_route(const DecodeArgs& a, float* logits /*[T][E]*/, int3
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
         if (ov > bv || (ov == bv && oe < be)) {
           bv = ov;
           be = oe;
         }
       }
-      if (be >= E) be = 0;  // every remaining logit NaN: keep the id in range
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (be < E && (be & 31) == lane) taken |= 1u << ((be - warp * 32) >> 8);
       if (lane == 0) {
-        rs.ids[warp * k + r] = be;
-        rs.w[warp * k + r] = bv;  // the logit, turned into a weight below
+        cand_v[warp][r] = bv;
+        cand_e[warp][r] = be;
       }
     }
-    __syncwarp();
-    if (lane < k) {
-      const float l0 = rs.w[warp * k];
-      float den = 0.f;
-      for (int r = 0; r < k; ++r) den += expf(rs.w[warp * k + r] - l0);
-      const float wl = expf(rs.w[warp * k + lane] - l0) / den;
-      __syncwarp(0xffffffffu >> (32 - k));
-      rs.w[warp * k + lane] = wl;
+    __syncthreads();
+    if (warp == 0) {
+      // 8k candidates: lane l holds candidates l and l + 32 (warp-major order)
+      float v0 = -INFINITY, v1 = -INFINITY;
+      int e0 = 0x7fffffff, e1 = 0x7fffffff;
+      if (lane < 8 * k) {
+        v0 = cand_v[lane / k][lane % k];
+        e0 = cand_e[lane / k][lane % k];
+      }
+      if (lane + 32 < 8 * k) {
+        v1 = cand_v[(lane + 32) / k][(lane + 32) % k];
+        e1 = cand_e[(lane + 32) / k][(lane + 32) % k];
+      }
+      for (int r = 0; r < k; ++r) {
+        float bv = v0;
+        int be = e0;
+        if (v1 > bv || (v1 == bv && e1 < be)) {
+          bv = v1;
+          be = e1;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if (e0 == be) {
+          v0 = -INFINITY;
+          e0 = 0x7fffffff;
+        } else if (e1 == be) {
+          v1 = -INFINITY;
+          e1 = 0x7fffffff;
+        }
+        if (be >= E) be = 0;  // every remaining logit NaN: keep the id in range
+        if (lane == 0) {
+          rs.ids[t * k + r] = be;
+          rs.w[t * k + r] = bv;  // the logit, turned into a weight below
+        }
+      }
+      __syncwarp();
+      if (lane < k) {
+        const float l0 = rs.w[t * k];
+        float den = 0.f;
+        for (int r = 0; r < k; ++r) den += expf(rs.w[t * k + r] - l0);
+        const float wl = expf(rs.w[t * k + lane] - l0) / den;
+        __syncwarp(0xffffffffu >> (32 - k));
+        rs.w[t * k + lane] = wl;
+      }
     }
+    __syncthreads();
   }
-  __syncthreads();
   for (int p = tid; p < T * k; p += DEC_THREADS) mark[rs.ids[p]] = 1;
   __syncthreads();
   if (warp == 0) {
@@ -149,42 +181,62 @@ __device__ __forceinline__ bool wait_copies(uint64_t* bar, int* status) {
 }
 
 // ---------------------------------------------------------------------------
-// K1: router partial logits
+// K1: router logits. CTA c owns experts 8c..8c+7; thread i loads rows
+// i + 256j of Wr (32 bytes each) before the dependency wait, multiplies them
+// with x after it, and the CTA reduces over its 8 warps in a fixed order.
 // ---------------------------------------------------------------------------
+constexpr int RT_EPC = 8;  // experts per CTA
+
+template <int RPT>  // Wr rows per thread = H / 256
 __global__ void __launch_bounds__(DEC_THREADS) decode_router_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
-  const int c = blockIdx.x, tid = threadIdx.x;
-  const int HS = a.H / a.NS, E = a.E, T = a.T;
-  float* ws = reinterpret_cast<float*>(smem);  // [HS][E]
-  float* xs = ws + (size_t)HS * E;             // [T][HS]
-  const uint32_t bytes = (uint32_t)(HS * E * sizeof(float));
-  if (tid == 0) {
-    tc::mbar_init(&bar, 1);
-    tc::fence_barrier_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    tc::mbar_expect_tx(&bar, bytes);
-    tc::bulk_g2s(ws, a.Wr + (size_t)c * HS * E, bytes, &bar);
+  float* xs = reinterpret_cast<float*>(smem);  // [T][H]
+  __shared__ float red[8][4][RT_EPC];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = a.H, E = a.E, T = a.T;
+  const int e0 = blockIdx.x * RT_EPC;
+  float4 w[RPT][2];
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) {
+    const float4* src = reinterpret_cast<const float4*>(a.Wr + (size_t)(tid + 256 * j) * E + e0);
+    w[j][0] = __ldg(src);
+    w[j][1] = __ldg(src + 1);
   }
   tc::grid_dep_wait();    // X may come from the previous grid
   tc::grid_dep_launch();
-  for (int i = tid; i < T * HS; i += DEC_THREADS) {
-    const int t = i / HS, h = i % HS;
-    xs[i] = a.X[(size_t)t * a.H + c * HS + h];
+  for (int i = tid; i < T * H / 4; i += DEC_THREADS)
+    reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(a.X) + i);
+  __syncthreads();
+  for (int t = 0; t < T; ++t) {
+    float acc[RT_EPC] = {};
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const float x = xs[t * H + tid + 256 * j];
+      acc[0] = fmaf(x, w[j][0].x, acc[0]);
+      acc[1] = fmaf(x, w[j][0].y, acc[1]);
+      acc[2] = fmaf(x, w[j][0].z, acc[2]);
+      acc[3] = fmaf(x, w[j][0].w, acc[3]);
+      acc[4] = fmaf(x, w[j][1].x, acc[4]);
+      acc[5] = fmaf(x, w[j][1].y, acc[5]);
+      acc[6] = fmaf(x, w[j][1].z, acc[6]);
+      acc[7] = fmaf(x, w[j][1].w, acc[7]);
+    }
+#pragma unroll
+    for (int q = 0; q < RT_EPC; ++q) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], off);
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int q = 0; q < RT_EPC; ++q) red[warp][t][q] = acc[q];
   }
   __syncthreads();
-  if (!wait_copies(&bar, a.status)) return;
-  for (int e = tid; e < E; e += DEC_THREADS) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int h = 0; h < HS; ++h) {
-      const float wv = ws[h * E + e];
+  if (tid < T * RT_EPC) {
+    const int t = tid / RT_EPC, q = tid % RT_EPC;
+    float s2 = 0.f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
-        if (t < T) acc[t] = fmaf(xs[t * HS + h], wv, acc[t]);
-    }
-    for (int t = 0; t < T; ++t) a.part[((size_t)c * T + t) * E + e] = acc[t];
+    for (int w8 = 0; w8 < 8; ++w8) s2 += red[w8][t][q];
+    if (e0 + q < E) a.logits[(size_t)t * E + e0 + q] = s2;
   }
 }
 
@@ -345,9 +397,13 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_down_kernel(DecodeArgs a) 
   const int r0 = blockIdx.x * DEC_HROWS;
   const int maxx = T * k + 1;  // experts incl. shared
   const int P = T * k + (a.has_shared ? T : 0);
+  // h rows are staged with each 32-float sub-block padded to 36 floats, so
+  // that the 8 lanes of a quarter-warp reading 8 different sub-blocks of a row
+  // hit 8 different bank groups
+  constexpr int HSTRIDE = NSUBD * 36;
   uint8_t* wsm = smem;                                                       // [maxx][8 rows]
-  float* hs = reinterpret_cast<float*>(smem + (size_t)maxx * blk_bytes);    // [P][F]
-  float* logits = hs + (size_t)(T * k + T) * F;                              // [T][E]
+  float* hs = reinterpret_cast<float*>(smem + (size_t)maxx * blk_bytes);    // [P][NSUBD][36]
+  float* logits = hs + (size_t)(T * k + T) * HSTRIDE;                        // [T][E]
   int32_t* mark = reinterpret_cast<int32_t*>(logits + (size_t)T * E);
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
@@ -381,8 +437,11 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_down_kernel(DecodeArgs a) 
   }
   tc::grid_dep_wait();     // h from the gate/up grid is complete
   tc::grid_dep_launch();
-  for (int i = tid; i < P * F / 4; i += DEC_THREADS)
-    reinterpret_cast<float4*>(hs)[i] = __ldcg(reinterpret_cast<const float4*>(a.hbuf) + i);
+  for (int i = tid; i < P * F / 4; i += DEC_THREADS) {
+    const int p = i / (F / 4), rem = i % (F / 4);
+    reinterpret_cast<float4*>(hs + (size_t)p * HSTRIDE + (rem >> 3) * 36)[rem & 7] =
+        __ldcg(reinterpret_cast<const float4*>(a.hbuf) + i);
+  }
   __syncthreads();
   if (!wait_copies(&bar, a.status)) return;
 
@@ -408,7 +467,7 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_down_kernel(DecodeArgs a) 
         hd.f2 = hv.w;
         const uint4 qv = *reinterpret_cast<const uint4*>(blk + quant_offset(QT, sj));
         const uint32_t hb = QT == QMOE_Q5K ? *reinterpret_cast<const uint32_t*>(blk + 16 + 4 * sj) : 0u;
-        const float4* x4 = reinterpret_cast<const float4*>(hs + (size_t)p * F + c * SUBK);
+        const float4* x4 = reinterpret_cast<const float4*>(hs + (size_t)p * HSTRIDE + c * 36);
         float xv[32], xsum = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -442,16 +501,7 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_down_kernel(DecodeArgs a) 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-int decode_router_splits(int H, int E) {
-  int ns = 16;
-  while ((size_t)(H / ns) * E * sizeof(float) > 64 * 1024 && H / (ns * 2) >= 4) ns *= 2;
-  return ns;
-}
-
-static size_t router_smem(int T, int H, int E) {
-  const int ns = decode_router_splits(H, E);
-  return sizeof(float) * ((size_t)(H / ns) * E + (size_t)T * (H / ns));
-}
+static size_t router_smem(int T, int H) { return sizeof(float) * (size_t)T * H; }
 
 static size_t gateup_smem(int T, int H, int E, int qt) {
   const size_t row_bytes = (size_t)(H / QK) * qtype_bytes(qt);
@@ -461,26 +511,56 @@ static size_t gateup_smem(int T, int H, int E, int qt) {
 static size_t down_smem(int T, int E, int F, int k, int qt) {
   const size_t row_bytes = (size_t)(F / QK) * qtype_bytes(qt);
   const int P = T * k + T;
-  return (size_t)(T * k + 1) * DEC_HROWS * row_bytes + sizeof(float) * ((size_t)P * F + (size_t)T * E) +
+  return (size_t)(T * k + 1) * DEC_HROWS * row_bytes + sizeof(float) * ((size_t)P * (F / SUBK) * 36 + (size_t)T * E) +
          sizeof(int32_t) * E;
 }
 
 bool decode_path_supported(int T, int H, int E, int k, int F, int gate_qt, int down_qt) {
-  if (T < 1 || T > 4 || k > 16) return false;
+  if (T < 1 || T > 4 || k > 8) return false;
   if (H != 1024 && H != 2048 && H != 4096) return false;
   if (F != 256 && F != 512 && F != 1024 && F != 2048) return false;
-  if (router_smem(T, H, E) > 200 * 1024) return false;
+  if (E % RT_EPC != 0) return false;
+  if (router_smem(T, H) > 200 * 1024) return false;
   if (gateup_smem(T, H, E, gate_qt) > 200 * 1024) return false;
   if (down_smem(T, E, F, k, down_qt) > 200 * 1024) return false;
   return true;
 }
 
+// Per-kernel launch attributes, set once per kernel (and again whenever a
+// launch needs more dynamic shared memory than before). All decode kernels
+// share one signature, so the bookkeeping is keyed by the kernel's address.
+static cudaError_t prepare_kernel(const void* fn, size_t smem) {
+  static std::mutex mu;
+  static const void* fns[32];
+  static size_t smem_set[32];
+  static int n = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int i = 0;
+  while (i < n && fns[i] != fn) ++i;
+  if (i == n) {
+    if (n == 32) return cudaErrorInvalidValue;
+    // the three kernels run concurrently: ask for the largest shared-memory
+    // carveout so that CTAs of different kernels can share an SM
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    fns[n] = fn;
+    smem_set[n] = 0;
+    ++n;
+  }
+  // static shared memory counts against the same limit, so the dynamic
+  // maximum is raised for every launch size not seen before
+  if (smem > smem_set[i]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set[i] = smem;
+  }
+  return cudaSuccess;
+}
+
 template <typename K>
 static cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t st, const DecodeArgs& a) {
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t pe = prepare_kernel(reinterpret_cast<const void*>(kernel), smem);
+  if (pe != cudaSuccess) return pe;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(DEC_THREADS);
@@ -511,9 +591,16 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.X = L.X; a.R = L.R; a.out = L.out; a.Wr = L.Wr;
   a.Wg = L.Wg; a.Wu = L.Wu; a.Wd = L.Wd; a.Sg = L.Sg; a.Su = L.Su; a.Sd = L.Sd;
   a.T = L.T; a.H = L.H; a.E = L.E; a.k = L.k; a.F = L.F; a.has_shared = L.Sg != nullptr;
-  a.NS = decode_router_splits(L.H, L.E);
-  a.part = L.part; a.hbuf = L.hbuf; a.ybuf = L.ybuf; a.ids = L.ids; a.w = L.w; a.status = L.status;
-  cudaError_t e = launch_pdl(decode_router_kernel, a.NS, router_smem(L.T, L.H, L.E), st, a);
+  a.logits = L.part; a.hbuf = L.hbuf; a.ybuf = L.ybuf; a.ids = L.ids; a.w = L.w; a.status = L.status;
+  const int g1 = L.E / RT_EPC;
+  const size_t s1 = router_smem(L.T, L.H);
+  cudaError_t e;
+  switch (L.H) {
+    case 1024: e = launch_pdl(decode_router_kernel<4>, g1, s1, st, a); break;
+    case 2048: e = launch_pdl(decode_router_kernel<8>, g1, s1, st, a); break;
+    case 4096: e = launch_pdl(decode_router_kernel<16>, g1, s1, st, a); break;
+    default: return cudaErrorInvalidValue;
+  }
   if (e != cudaSuccess) return e;
   const int slots = a.has_shared + (L.T * L.k < L.E ? L.T * L.k : L.E);
   const int g2 = slots * (L.F / DEC_FROWS);
