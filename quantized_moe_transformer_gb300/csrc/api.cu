@@ -87,7 +87,7 @@ inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace carve-up (every piece 256-byte aligned).
 struct MoeWs {
-  size_t part, ids, w, offsets, perm, active, n_active, chunk, mtiles, n_mtiles, xb, h, y, total;
+  size_t part, ids, w, route, offsets, perm, active, n_active, chunk, mtiles, n_mtiles, xb, h, y, total;
   int nsplit;
 };
 
@@ -96,9 +96,11 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   const size_t P = (size_t)T * k, rows = P + T;
   L.nsplit = router_splits(T, H, E);
   size_t o = 0;
-  L.part = o;     o += up256(sizeof(float) * (size_t)L.nsplit * T * E);
+  const int parts = L.nsplit > 4 ? L.nsplit : 4;  // the decode router writes 4 partials
+  L.part = o;     o += up256(sizeof(float) * (size_t)parts * T * E);
   L.ids = o;      o += up256(sizeof(int32_t) * P);
   L.w = o;        o += up256(sizeof(float) * P);
+  L.route = o;    o += up256(sizeof(int32_t) * (P + 1));
   L.offsets = o;  o += up256(sizeof(int32_t) * (E + 2));
   L.perm = o;     o += up256(sizeof(int32_t) * rows);
   L.active = o;   o += up256(sizeof(int32_t) * (E + 1));
@@ -209,6 +211,7 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
     p.n_mtiles = n_mtiles;
     p.max_mtiles = tc_max_mtiles(T, 1, 1, 0);
     p.hin = xb;
+    p.a_rows = T;
     p.yout_f32 = y;
     p.T = T;
     p.k = 1;
@@ -496,6 +499,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     D.ybuf = y;
     D.ids = ws_ids;
     D.w = ws_w;
+    D.route = reinterpret_cast<int32_t*>(base + L.route);
     D.status = status;
     e = staged(QMOE_STAGE_DECODE, 3, st, [&] { return launch_decode(D, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
@@ -568,6 +572,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     p.qt = d->gate_type;
     p.X = X;
     p.xb = xb;
+    p.a_rows = T;
     p.hout = h16;
     e = staged(QMOE_STAGE_GATEUP, 1, st, [&] { return launch_gateup_tc(p, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
@@ -577,6 +582,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     p.S2 = nullptr;
     p.qt = d->down_type;
     p.hin = h16;
+    p.a_rows = P + T;
     p.yout = y16;
     e = staged(QMOE_STAGE_DOWN, 1, st, [&] { return launch_down_tc(p, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;

@@ -76,9 +76,11 @@ __device__ __forceinline__ float dot_sub(const uint4 qv, uint32_t hb, const floa
 }
 
 // Spreads four bits of ``h`` (bits b, b+2, b+4, b+6) to bit 4 of bytes 0..3.
+// One multiply places bit 2i at 6i + 2i + 4 = 8i + 4; the other partial
+// products land on positions the mask clears, and none of them carry into a
+// kept position.
 __device__ __forceinline__ uint32_t spread4(uint32_t h, int b) {
-  return (((h >> b) & 1u) << 4) | (((h >> (b + 2)) & 1u) << 12) | (((h >> (b + 4)) & 1u) << 20) |
-         (((h >> (b + 6)) & 1u) << 28);
+  return (((h >> b) & 0x55u) * 0x410410u) & 0x10101010u;
 }
 
 // S = sum over the 32 weights of one sub-block of (0.5 + q_i/256) * x_i.

@@ -54,6 +54,7 @@ struct GroupedTcArgs {
   __nv_bfloat16* hout;
   __nv_bfloat16* yout;
   float* yout_f32;  // down pass: write fp32 instead of bf16 when not null
+  int a_rows;       // rows of the bf16 activation matrix (xb: T; hin: its row count)
   int T, k, E, H, F;
   int* status;
 };
@@ -90,6 +91,7 @@ struct DecodeLaunch {
   float* ybuf;
   int32_t* ids;
   float* w;
+  int32_t* route;  // 1 + T*k int32
   int* status;
 };
 bool decode_path_supported(int T, int H, int E, int k, int F, int gate_qt, int down_qt);

@@ -8,16 +8,19 @@
 // Decode Result Shows Why Axis Choice Matters": with one row the independent
 // work is the eight selected routes, merged in selected-slot order.
 //
-//   K1 router     one CTA per 8 experts: its threads load their Wr rows' 32
-//                 bytes for those experts before waiting on the previous grid,
-//                 then reduce x . Wr over all of H in a fixed order and write
-//                 the final logits l[t][e] (no partials left to combine).
+//   K1 router     one CTA per (8 experts, quarter of H): its threads load
+//                 their Wr rows' 32 bytes for those experts before waiting on
+//                 the previous grid, then reduce x . Wr over the quarter in a
+//                 fixed order and write 4 partial logits per (row, expert);
+//                 128 CTAs share the 2 MB read.
+//   K1b route     one CTA: sums the partials in a fixed order, takes the top-k
+//                 by rank, the weights and the ascending list of distinct
+//                 selected experts, once for all later CTAs.
 //   K2 gate/up    one CTA per (expert slot, 32 intermediate rows). The shared
-//                 expert's CTAs start their weight copies before the router has
-//                 finished; every CTA then takes the top-k of the logits itself
-//                 (no separate routing kernel) and streams its expert's rows.
-//                 Output h per (row, slot) pair.
-//   K3 down       one CTA per 8 output rows. It routes again from the logits,
+//                 expert's CTAs start their weight copies before the routing
+//                 is known; the others read the routing record and stream
+//                 their expert's rows. Output h per (row, slot) pair.
+//   K3 down       one CTA per 8 output rows. It reads the routing record,
 //                 streams its 8 rows of every selected expert's down matrix
 //                 while K2 is still running, then waits for h, and forms
 //                 out = R + y_shared + sum_s w_s y_s in slot order.
@@ -31,6 +34,8 @@
 namespace qmoe {
 
 constexpr int DEC_THREADS = 256;
+constexpr int RT_EPC = 8;  // router: experts per CTA
+constexpr int RT_HQ = 4;   // router: parts of H (CTAs per expert group)
 constexpr int DEC_FROWS = 32;   // intermediate rows per gate/up CTA
 constexpr int DEC_HROWS = 8;    // output rows per down CTA
 
@@ -41,11 +46,12 @@ struct DecodeArgs {
   const float* Wr;
   const uint8_t *Wg, *Wu, *Wd, *Sg, *Su, *Sd;
   int T, H, E, k, F, has_shared;
-  float* logits;   // [T][E]
+  float* logits;   // [RT_HQ][T][E] partial logits
   float* hbuf;     // [T*k + T][F], indexed by pair (t*k + s; shared T*k + t)
   float* ybuf;     // [T*k + T][H]
   int32_t* ids;    // [T][k]
   float* w;        // [T][k]
+  int32_t* route;  // record: [0] n_distinct, [1..] distinct experts (T*k entries)
   int* status;
 };
 
@@ -60,104 +66,62 @@ struct RouteSmem {
   int32_t n_distinct;
 };
 
-__device__ void decode_route(const DecodeArgs& a, float* logits /*[T][E]*/, int32_t* mark /*[E]*/,
-                             RouteSmem& rs) {
-  __shared__ float cand_v[8][16];
-  __shared__ int32_t cand_e[8][16];
+// ---------------------------------------------------------------------------
+// K1b: routing, once, in one CTA: logits from the 4 partials (fixed order),
+// top-k by rank, weights, the ascending list of distinct selected experts.
+// The record (ids and w to the workspace, distinct list to ``route``) is read
+// by every CTA of the next two kernels.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(DEC_THREADS) decode_route_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  float* logits = reinterpret_cast<float*>(smem);                       // [T][E]
+  int32_t* mark = reinterpret_cast<int32_t*>(logits + (size_t)a.T * a.E);  // [E]
+  __shared__ float sel_l[4 * 16];
+  __shared__ int32_t sel_e[4 * 16];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, E = a.E, k = a.k;
-  for (int i = tid; i < T * E; i += DEC_THREADS) logits[i] = __ldcg(a.logits + i);
+  tc::grid_dep_wait();  // the router's partials are complete
+  tc::grid_dep_launch();
+  for (int i = tid; i < T * E; i += DEC_THREADS) {
+    float v[RT_HQ];
+#pragma unroll
+    for (int q = 0; q < RT_HQ; ++q) v[q] = __ldcg(a.logits + (size_t)q * T * E + i);
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < RT_HQ; ++q) sum += v[q];
+    logits[i] = (sum == sum) ? sum : -INFINITY;  // NaN sorts last
+  }
   for (int e = tid; e < E; e += DEC_THREADS) mark[e] = 0;
   __syncthreads();
-  // two-level top-k per row: each warp takes the top k of its eighth of the
-  // experts (lane l holds experts w*32 + l + 256j), then warp 0 merges the 8k
-  // candidates. Order: larger logit first, lower index on ties.
+  // top-k by rank: the thread of expert e counts the experts that come before
+  // it (larger logit first, lower index on ties), stopping once the count
+  // reaches k; a count below k is e's slot
   for (int t = 0; t < T; ++t) {
     const float* L = logits + t * E;
-    uint32_t taken = 0;
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-      for (int j = 0; warp * 32 + 256 * j < E; ++j) {
-        const int e = warp * 32 + lane + 256 * j;
-        if (e < E && !((taken >> j) & 1u)) {
-          const float v = L[e];
-          if (v > bv || (v == bv && e < be)) {
-            bv = v;
-            be = e;
-          }
-        }
+    for (int e = tid; e < E; e += DEC_THREADS) {
+      const float v = L[e];
+      int cnt = 0;
+      for (int j0 = 0; j0 < E && cnt < k; j0 += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(L + j0);
+        cnt += (q.x > v || (q.x == v && j0 < e)) + (q.y > v || (q.y == v && j0 + 1 < e)) +
+               (q.z > v || (q.z == v && j0 + 2 < e)) + (q.w > v || (q.w == v && j0 + 3 < e));
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (be < E && (be & 31) == lane) taken |= 1u << ((be - warp * 32) >> 8);
-      if (lane == 0) {
-        cand_v[warp][r] = bv;
-        cand_e[warp][r] = be;
+      if (cnt < k) {
+        sel_e[t * k + cnt] = e;
+        sel_l[t * k + cnt] = v;
       }
     }
-    __syncthreads();
-    if (warp == 0) {
-      // 8k candidates: lane l holds candidates l and l + 32 (warp-major order)
-      float v0 = -INFINITY, v1 = -INFINITY;
-      int e0 = 0x7fffffff, e1 = 0x7fffffff;
-      if (lane < 8 * k) {
-        v0 = cand_v[lane / k][lane % k];
-        e0 = cand_e[lane / k][lane % k];
-      }
-      if (lane + 32 < 8 * k) {
-        v1 = cand_v[(lane + 32) / k][(lane + 32) % k];
-        e1 = cand_e[(lane + 32) / k][(lane + 32) % k];
-      }
-      for (int r = 0; r < k; ++r) {
-        float bv = v0;
-        int be = e0;
-        if (v1 > bv || (v1 == bv && e1 < be)) {
-          bv = v1;
-          be = e1;
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-          }
-        }
-        if (e0 == be) {
-          v0 = -INFINITY;
-          e0 = 0x7fffffff;
-        } else if (e1 == be) {
-          v1 = -INFINITY;
-          e1 = 0x7fffffff;
-        }
-        if (be >= E) be = 0;  // every remaining logit NaN: keep the id in range
-        if (lane == 0) {
-          rs.ids[t * k + r] = be;
-          rs.w[t * k + r] = bv;  // the logit, turned into a weight below
-        }
-      }
-      __syncwarp();
-      if (lane < k) {
-        const float l0 = rs.w[t * k];
-        float den = 0.f;
-        for (int r = 0; r < k; ++r) den += expf(rs.w[t * k + r] - l0);
-        const float wl = expf(rs.w[t * k + lane] - l0) / den;
-        __syncwarp(0xffffffffu >> (32 - k));
-        rs.w[t * k + lane] = wl;
-      }
-    }
-    __syncthreads();
   }
-  for (int p = tid; p < T * k; p += DEC_THREADS) mark[rs.ids[p]] = 1;
+  __syncthreads();
+  if (tid < T * k) {
+    const int t = tid / k;
+    const float l0 = sel_l[t * k];
+    float den = 0.f;
+    for (int r = 0; r < k; ++r) den += expf(sel_l[t * k + r] - l0);
+    a.ids[tid] = sel_e[tid];
+    a.w[tid] = expf(sel_l[tid] - l0) / den;
+    mark[sel_e[tid]] = 1;
+  }
   __syncthreads();
   if (warp == 0) {
     int run = 0;
@@ -165,11 +129,25 @@ __device__ void decode_route(const DecodeArgs& a, float* logits /*[T][E]*/, int3
       const int e = b + lane;
       const int m = (e < E) ? mark[e] : 0;
       const unsigned bal = __ballot_sync(0xffffffffu, m);
-      if (m) rs.distinct[run + __popc(bal & ((1u << lane) - 1u))] = e;
+      if (m) a.route[1 + run + __popc(bal & ((1u << lane) - 1u))] = e;
       run += __popc(bal);
     }
-    if (lane == 0) rs.n_distinct = run;
+    if (lane == 0) a.route[0] = run;
   }
+}
+
+// Reads the routing record into shared memory (called after the PDL wait that
+// makes the routing grid's writes visible).
+__device__ void load_route(const DecodeArgs& a, RouteSmem& rs) {
+  const int tid = threadIdx.x;
+  const int P = a.T * a.k;
+  for (int p = tid; p < P; p += DEC_THREADS) {
+    rs.ids[p] = __ldcg(a.ids + p);
+    rs.w[p] = __ldcg(a.w + p);
+  }
+  if (tid == 0) rs.n_distinct = __ldcg(a.route);
+  __syncthreads();
+  for (int i = tid; i < rs.n_distinct; i += DEC_THREADS) rs.distinct[i] = __ldcg(a.route + 1 + i);
   __syncthreads();
 }
 
@@ -181,24 +159,24 @@ __device__ __forceinline__ bool wait_copies(uint64_t* bar, int* status) {
 }
 
 // ---------------------------------------------------------------------------
-// K1: router logits. CTA c owns experts 8c..8c+7; thread i loads rows
-// i + 256j of Wr (32 bytes each) before the dependency wait, multiplies them
-// with x after it, and the CTA reduces over its 8 warps in a fixed order.
+// K1: router partial logits. CTA (g, q) owns experts 8g..8g+7 and rows
+// [q H/4, (q+1) H/4); thread i loads rows i + 256j of that quarter (32 bytes
+// each) before the dependency wait, multiplies them with x after it, and the
+// CTA reduces over its 8 warps in a fixed order.
 // ---------------------------------------------------------------------------
-constexpr int RT_EPC = 8;  // experts per CTA
-
-template <int RPT>  // Wr rows per thread = H / 256
+template <int RPT>  // Wr rows per thread = H / (256 * RT_HQ)
 __global__ void __launch_bounds__(DEC_THREADS) decode_router_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   float* xs = reinterpret_cast<float*>(smem);  // [T][H]
   __shared__ float red[8][4][RT_EPC];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H, E = a.E, T = a.T;
-  const int e0 = blockIdx.x * RT_EPC;
+  const int e0 = (blockIdx.x / RT_HQ) * RT_EPC, hq = blockIdx.x % RT_HQ;
+  const int h0 = hq * (H / RT_HQ);
   float4 w[RPT][2];
 #pragma unroll
   for (int j = 0; j < RPT; ++j) {
-    const float4* src = reinterpret_cast<const float4*>(a.Wr + (size_t)(tid + 256 * j) * E + e0);
+    const float4* src = reinterpret_cast<const float4*>(a.Wr + (size_t)(h0 + tid + 256 * j) * E + e0);
     w[j][0] = __ldg(src);
     w[j][1] = __ldg(src + 1);
   }
@@ -211,7 +189,7 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_router_kernel(DecodeArgs a
     float acc[RT_EPC] = {};
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
-      const float x = xs[t * H + tid + 256 * j];
+      const float x = xs[t * H + h0 + tid + 256 * j];
       acc[0] = fmaf(x, w[j][0].x, acc[0]);
       acc[1] = fmaf(x, w[j][0].y, acc[1]);
       acc[2] = fmaf(x, w[j][0].z, acc[2]);
@@ -236,7 +214,7 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_router_kernel(DecodeArgs a
     float s2 = 0.f;
 #pragma unroll
     for (int w8 = 0; w8 < 8; ++w8) s2 += red[w8][t][q];
-    if (e0 + q < E) a.logits[(size_t)t * E + e0 + q] = s2;
+    if (e0 + q < E) a.logits[((size_t)hq * T + t) * E + e0 + q] = s2;
   }
 }
 
@@ -296,32 +274,35 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_gateup_kernel(DecodeArgs a
   constexpr uint32_t stage_rows_bytes = (uint32_t)(RPS * row_bytes);
   uint8_t* wgs = smem;                                   // 32 gate rows
   uint8_t* wus = smem + DEC_FROWS * row_bytes;           // 32 up rows
-  float* logits = reinterpret_cast<float*>(smem + 2 * DEC_FROWS * row_bytes);  // [T][E]
-  int32_t* mark = reinterpret_cast<int32_t*>(logits + (size_t)T * E);            // [E]
   const bool is_shared = a.has_shared && slot == 0;
   if (tid == 0) {
     for (int i = 0; i < DEC_STAGES; ++i) tc::mbar_init(&bar[i], 1);
     tc::fence_barrier_init();
   }
   __syncthreads();
+  // warp 0 issues the 8 copies (4 stages x gate/up) from 8 lanes, after lanes
+  // 0..3 have set each stage's expected byte count
   auto issue = [&](const uint8_t* gsrc, const uint8_t* usrc) {
-    for (int st = 0; st < DEC_STAGES; ++st) {
-      tc::mbar_expect_tx(&bar[st], 2 * stage_rows_bytes);
-      tc::bulk_g2s(wgs + st * stage_rows_bytes, gsrc + st * stage_rows_bytes, stage_rows_bytes, &bar[st]);
-      tc::bulk_g2s(wus + st * stage_rows_bytes, usrc + st * stage_rows_bytes, stage_rows_bytes, &bar[st]);
+    if (lane < DEC_STAGES) tc::mbar_expect_tx(&bar[lane], 2 * stage_rows_bytes);
+    __syncwarp();
+    if (lane < 2 * DEC_STAGES) {
+      const int st = lane >> 1;
+      const uint8_t* src = (lane & 1) ? usrc : gsrc;
+      uint8_t* dst = (lane & 1) ? wus : wgs;
+      tc::bulk_g2s(dst + st * stage_rows_bytes, src + st * stage_rows_bytes, stage_rows_bytes, &bar[st]);
     }
   };
   const size_t chunk_off = (size_t)fc * DEC_FROWS * row_bytes;
-  if (is_shared && tid == 0) issue(a.Sg + chunk_off, a.Su + chunk_off);
-  tc::grid_dep_wait();     // router partials (and X) are complete
+  if (is_shared && warp == 0) issue(a.Sg + chunk_off, a.Su + chunk_off);
+  tc::grid_dep_wait();     // the routing record (and X) are complete
   tc::grid_dep_launch();
-  decode_route(a, logits, mark, rs);
+  load_route(a, rs);
   int e = a.E;  // shared
   if (!is_shared) {
     const int ri = slot - a.has_shared;
     if (ri >= rs.n_distinct) return;  // this CTA issued no copies
     e = rs.distinct[ri];
-    if (tid == 0) {
+    if (warp == 0) {
       const size_t eoff = (size_t)e * F * row_bytes + chunk_off;
       issue(a.Wg + eoff, a.Wu + eoff);
     }
@@ -403,28 +384,24 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_down_kernel(DecodeArgs a) 
   constexpr int HSTRIDE = NSUBD * 36;
   uint8_t* wsm = smem;                                                       // [maxx][8 rows]
   float* hs = reinterpret_cast<float*>(smem + (size_t)maxx * blk_bytes);    // [P][NSUBD][36]
-  float* logits = hs + (size_t)(T * k + T) * HSTRIDE;                        // [T][E]
-  int32_t* mark = reinterpret_cast<int32_t*>(logits + (size_t)T * E);
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
     tc::fence_barrier_init();
   }
   __syncthreads();
-  // the router grid completed before the gate/up grid let this one launch
-  decode_route(a, logits, mark, rs);
+  // the routing grid completed before the gate/up grid let this one launch
+  load_route(a, rs);
   const int nd = rs.n_distinct;
-  if (tid == 0) {
+  if (warp == 0) {
+    // one copy per lane: 8 rows of every selected expert's down matrix, and
+    // of the shared expert's
     const int nx = nd + (a.has_shared ? 1 : 0);
-    tc::mbar_expect_tx(&bar, nx * blk_bytes);
-    for (int i = 0; i < nd; ++i)
-      tc::bulk_g2s(wsm + (size_t)i * blk_bytes, a.Wd + ((size_t)rs.distinct[i] * H + r0) * row_bytes, blk_bytes,
-                   &bar);
-    if (a.has_shared) tc::bulk_g2s(wsm + (size_t)nd * blk_bytes, a.Sd + (size_t)r0 * row_bytes, blk_bytes, &bar);
-    if (blockIdx.x == 0)
-      for (int p = 0; p < T * k; ++p) {
-        a.ids[p] = rs.ids[p];
-        a.w[p] = rs.w[p];
-      }
+    if (lane == 0) tc::mbar_expect_tx(&bar, nx * blk_bytes);
+    __syncwarp();
+    for (int i = lane; i < nx; i += 32) {
+      const uint8_t* src = i < nd ? a.Wd + ((size_t)rs.distinct[i] * H + r0) * row_bytes : a.Sd + (size_t)r0 * row_bytes;
+      tc::bulk_g2s(wsm + (size_t)i * blk_bytes, src, blk_bytes, &bar);
+    }
   }
   for (int p = tid; p < P; p += DEC_THREADS) {
     int sl = nd;  // shared
@@ -505,14 +482,15 @@ static size_t router_smem(int T, int H) { return sizeof(float) * (size_t)T * H; 
 
 static size_t gateup_smem(int T, int H, int E, int qt) {
   const size_t row_bytes = (size_t)(H / QK) * qtype_bytes(qt);
-  return 2 * DEC_FROWS * row_bytes + sizeof(float) * (size_t)T * E + sizeof(int32_t) * E;
+  return 2 * DEC_FROWS * row_bytes;
 }
+
+static size_t route_smem(int T, int E) { return sizeof(float) * (size_t)T * E + sizeof(int32_t) * E; }
 
 static size_t down_smem(int T, int E, int F, int k, int qt) {
   const size_t row_bytes = (size_t)(F / QK) * qtype_bytes(qt);
   const int P = T * k + T;
-  return (size_t)(T * k + 1) * DEC_HROWS * row_bytes + sizeof(float) * ((size_t)P * (F / SUBK) * 36 + (size_t)T * E) +
-         sizeof(int32_t) * E;
+  return (size_t)(T * k + 1) * DEC_HROWS * row_bytes + sizeof(float) * (size_t)P * (F / SUBK) * 36;
 }
 
 bool decode_path_supported(int T, int H, int E, int k, int F, int gate_qt, int down_qt) {
@@ -591,17 +569,19 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.X = L.X; a.R = L.R; a.out = L.out; a.Wr = L.Wr;
   a.Wg = L.Wg; a.Wu = L.Wu; a.Wd = L.Wd; a.Sg = L.Sg; a.Su = L.Su; a.Sd = L.Sd;
   a.T = L.T; a.H = L.H; a.E = L.E; a.k = L.k; a.F = L.F; a.has_shared = L.Sg != nullptr;
-  a.logits = L.part; a.hbuf = L.hbuf; a.ybuf = L.ybuf; a.ids = L.ids; a.w = L.w; a.status = L.status;
-  const int g1 = L.E / RT_EPC;
+  a.logits = L.part; a.hbuf = L.hbuf; a.ybuf = L.ybuf; a.ids = L.ids; a.w = L.w; a.route = L.route;
+  a.status = L.status;
+  const int g1 = (L.E / RT_EPC) * RT_HQ;
   const size_t s1 = router_smem(L.T, L.H);
   cudaError_t e;
   switch (L.H) {
-    case 1024: e = launch_pdl(decode_router_kernel<4>, g1, s1, st, a); break;
-    case 2048: e = launch_pdl(decode_router_kernel<8>, g1, s1, st, a); break;
-    case 4096: e = launch_pdl(decode_router_kernel<16>, g1, s1, st, a); break;
+    case 1024: e = launch_pdl(decode_router_kernel<1>, g1, s1, st, a); break;
+    case 2048: e = launch_pdl(decode_router_kernel<2>, g1, s1, st, a); break;
+    case 4096: e = launch_pdl(decode_router_kernel<4>, g1, s1, st, a); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
+  if ((e = launch_pdl(decode_route_kernel, 1, route_smem(L.T, L.E), st, a)) != cudaSuccess) return e;
   const int slots = a.has_shared + (L.T * L.k < L.E ? L.T * L.k : L.E);
   const int g2 = slots * (L.F / DEC_FROWS);
   const size_t s2 = gateup_smem(L.T, L.H, L.E, L.gate_qt);

@@ -15,13 +15,14 @@
 //               fused SwiGLU (gate/up) or bf16 store (down);
 //   warps 4-11  producers: thread p owns weight row p of the n-tile; it keeps
 //               the packed super-block of its row in registers, prefetching
-//               the next super-block (or the next work item's first one)
-//               while it dequantises the current one to bf16; threads 0..127
-//               also gather activation row p of the k-tile (bf16) with
-//               cp.async. Both operands are written in the 128-byte-swizzled
-//               K-major layout the MMA descriptors describe;
+//               the next super-blocks in a bulk-copy ring while it
+//               dequantises the current one to bf16, written in the
+//               128-byte-swizzled K-major layout the MMA descriptors describe;
 //   warp 12     allocates 512 TMEM columns (two 256-column accumulators) and
-//               issues the MMAs from one lane.
+//               issues the MMAs from one lane;
+//   warp 13     gathers the activation tile of each k-tile (the rows of an
+//               m-tile, through the permutation) with cp.async, up to BS
+//               k-tiles ahead of the MMAs.
 // A 4-stage shared-memory ring (48 KB per stage) decouples producers and the
 // MMA issuer; the two accumulators let the epilogue of one tile overlap the
 // main loop of the next. Every wait is bounded: on time-out the CTA records
@@ -32,8 +33,9 @@
 namespace qmoe {
 
 constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64;
-constexpr int TC_THREADS = 416;
+constexpr int TC_THREADS = 448;
 constexpr int TC_MMA_WARP = 12;
+constexpr int TC_LOAD_WARP = 13;
 constexpr int TC_PRODUCERS = 256;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 32 KB
@@ -63,6 +65,7 @@ struct TcArgs {
   __nv_bfloat16* hout;          // gate/up output, [P+T][F] bf16
   __nv_bfloat16* yout;          // down output, [P+T][H] bf16
   float* yout_f32;              // down output in fp32 instead, when not null
+  int a_rows;                   // rows of the activation tensor the TMA map covers
   int T, k, E, H, F;
   int* status;
 };
@@ -83,10 +86,19 @@ __device__ __forceinline__ void load_raw(RawBlock<QT>& r, const uint8_t* blk) {
   for (int i = 0; i < RawBlock<QT>::N; ++i) r.c[i] = __ldg(p + i);
 }
 
-// Dequantises sub-blocks j0, j0+1 (64 weights, w = d*s*q - dmin*m) of a
-// register-held super-block and stores them as 8 swizzled 16-byte bf16
-// chunks of row ``r`` of a B stage. Each quant byte becomes the float
-// 0.5 + q/256 through one byte permute; w = 256*ds*f - (128*ds + dm).
+// K order inside every group of 8 consecutive K values of the tensor-core
+// operands: element e of a 16-byte chunk holds K offset kPerm8[e]. The weight
+// dequantisation below produces this order directly (a bf16x2 word takes the
+// quants of weights i and i+4 from one 32-bit quant word), and the activation
+// producers (the bf16 conversion of X and the gate/up epilogue writing h)
+// store their rows in the same order, so the dot products are unchanged.
+__device__ constexpr int kPerm8[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+
+// Dequantises sub-blocks j0, j0+1 (64 weights) of a register-held super-block
+// into 8 swizzled 16-byte bf16 chunks of row ``r`` of a B stage, in bf16x2
+// arithmetic: q is exact (the quant bits under the exponent of 128.0, minus
+// 128), then w = q * (d*s_j) - dmin*m_j in one bf16x2 FMA with the two scales
+// rounded to bf16.
 template <int QT, int J0>
 __device__ __forceinline__ void dequant_store(const RawBlock<QT>& raw, uint8_t* stage, int r) {
   KHeader h;
@@ -96,13 +108,13 @@ __device__ __forceinline__ void dequant_store(const RawBlock<QT>& raw, uint8_t* 
   h.f0 = raw.c[0].y;
   h.f1 = raw.c[0].z;
   h.f2 = raw.c[0].w;
+  const __nv_bfloat162 m128 = __float2bfloat162_rn(-128.f);
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    constexpr int unused = 0;
-    (void)unused;
     const int j = J0 + s;
     const float2 sc = sub_scale(h, j);
-    const float a = 256.f * sc.x, b = -(128.f * sc.x + sc.y);
+    const __nv_bfloat162 ds2 = __float2bfloat162_rn(sc.x);
+    const __nv_bfloat162 ndm2 = __float2bfloat162_rn(-sc.y);
     const uint4 q = QT == QMOE_Q5K ? raw.c[3 + j] : raw.c[1 + j];
     uint32_t hb = 0;
     if (QT == QMOE_Q5K) {
@@ -113,32 +125,21 @@ __device__ __forceinline__ void dequant_store(const RawBlock<QT>& raw, uint8_t* 
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int n = 0; n < 4; ++n) {
-      uint32_t ev = w[n] & 0x0F0F0F0Fu;
-      uint32_t od = (w[n] >> 4) & 0x0F0F0F0Fu;
-      if (QT == QMOE_Q5K) {
-        ev |= spread4(hb >> (8 * n), 0);
-        od |= spread4(hb >> (8 * n), 1);
-      }
       uint32_t o[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t sel = 0x7044u | ((uint32_t)k << 8);
-        const float fe = fmaf(a, __uint_as_float(__byte_perm(ev, 0x3F000000u, sel)), b);
-        const float fo = fmaf(a, __uint_as_float(__byte_perm(od, 0x3F000000u, sel)), b);
-        o[k] = tc::pack_bf16x2(fe, fo);
+      for (int i = 0; i < 4; ++i) {
+        // quants of weights 8n+i and 8n+i+4 as bf16 128+q in the two halves
+        uint32_t x = ((w[n] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+        if (QT == QMOE_Q5K) x |= (((hb >> (8 * n + i)) & 0x11u) * 0x10010u) & 0x00100010u;
+        __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
+        v = __hadd2(v, m128);             // q, exact
+        v = __hfma2(v, ds2, ndm2);        // q*d*s - dmin*m, one rounding
+        o[i] = *reinterpret_cast<uint32_t*>(&v);
       }
       *reinterpret_cast<uint4*>(stage + tc::sw128_offset(r, 4 * s + n)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  const uint32_t n = valid ? 16u : 0u;  // 0: fill the 16 bytes with zeros, read nothing
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 template <bool GATEUP, int QT>
 __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < BS; ++i) {
-      tc::mbar_init(&full[i], TC_PRODUCERS);
+      tc::mbar_init(&full[i], TC_PRODUCERS + 32);  // + one cp.async completion per loader lane
       tc::mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < RS; ++i) tc::mbar_init(&raw_full[i], TC_PRODUCERS);
@@ -207,11 +208,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
         for (int c = 0; c < 128; c += 16) {
           uint32_t gr[16], ur[16];
           tc::tmem_ld16x2(tq + c, tq + 128 + c, gr, ur);
+          float hv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hv[i] = silu_mul(__uint_as_float(gr[i]), __uint_as_float(ur[i]));
+          // stored in the operand K order (kPerm8 inside each group of 8)
           uint32_t o[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            o[i] = tc::pack_bf16x2(silu_mul(__uint_as_float(gr[2 * i]), __uint_as_float(ur[2 * i])),
-                                   silu_mul(__uint_as_float(gr[2 * i + 1]), __uint_as_float(ur[2 * i + 1])));
+          for (int i = 0; i < 8; ++i) {
+            const int g8 = (i >> 2) * 8, e = 2 * (i & 3);
+            o[i] = tc::pack_bf16x2(hv[g8 + kPerm8[e]], hv[g8 + kPerm8[e + 1]]);
+          }
           if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c);
             d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -282,15 +288,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
       const uint8_t* base = e < g.E ? g.W + (size_t)e * g.H * rb : g.S;
       return base + (size_t)(nt * TC_BN + p) * rb;
     };
-    // activation row p of item j, or nullptr (rows past the expert's count read zeros)
-    auto arow_of = [&](int wi) -> const __nv_bfloat16* {
-      const int2 mt = g.mtiles[wi / NT];
-      const int e = mt.x, m0 = mt.y;
-      const int base = g.offsets[e];
-      if (m0 + p >= g.offsets[e + 1] - base) return nullptr;
-      const int pos = base + m0 + p;
-      return GATEUP ? g.xb + (size_t)tc_pair_row(g.perm[pos], g.T, g.k) * g.H : g.hin + (size_t)pos * g.F;
-    };
     auto issue_raw = [&](int u) {
       const int j = u / KB;
       if (j >= n_mine) return;
@@ -299,26 +296,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
       tc::bulk_g2s(sRaw + (size_t)(u % RS) * Cfg::RAW_STAGE + (size_t)p * BYTES,
                    row_of(item(j)) + (size_t)(u % KB) * BYTES, BYTES, bar);
     };
-    const int n_kt = n_mine * KT;
-    const __nv_bfloat16* a_cur = nullptr;  // activation row of the k-tile being gathered
-    auto issue_a = [&](int kg) {
-      const int kt = kg % KT;
-      if (kt == 0) a_cur = p < 128 ? arow_of(item(kg / KT)) : nullptr;
-      if (p < 128) {
-        uint8_t* a_st = sA + (kg % BS) * TC_A_BYTES;
-        const bool valid = a_cur != nullptr;
-        const __nv_bfloat16* src = valid ? a_cur + kt * TC_BK : g.hin ? g.hin : g.xb;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) cp_async16(a_st + tc::sw128_offset(p, c), src + (valid ? 8 * c : 0), valid);
-      }
-      cp_async_commit();
-    };
     for (int u = 0; u < RS; ++u) issue_raw(u);
     bool ok = true;
-    if (n_kt > 0) {
-      if (!tc::mbar_wait(&empty[0], 1, abort_flag)) ok = false;
-      else issue_a(0);
-    }
     int kg = 0;
     for (int u = 0; u < n_mine * KB && ok; ++u) {
       if (!tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag)) {
@@ -333,27 +312,64 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
       issue_raw(u + RS);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
+        if (!tc::mbar_wait(&empty[kg % BS], ((kg / BS) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         uint8_t* b_st = sB + (kg % BS) * TC_B_BYTES;
         if (kk == 0) dequant_store<QT, 0>(cur, b_st, p);
         else if (kk == 1) dequant_store<QT, 2>(cur, b_st, p);
         else if (kk == 2) dequant_store<QT, 4>(cur, b_st, p);
         else dequant_store<QT, 6>(cur, b_st, p);
-        if (kg + 1 < n_kt) {
-          if (!tc::mbar_wait(&empty[(kg + 1) % BS], (((kg + 1) / BS) & 1) ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          issue_a(kg + 1);
-          asm volatile("cp.async.wait_group 1;" ::: "memory");
-        } else {
-          cp_async_wait_all();
-        }
         tc::fence_proxy_async_smem();
         tc::mbar_arrive(&full[kg % BS]);
         ++kg;
       }
     }
-    cp_async_wait_all();
+  } else if (warp == TC_LOAD_WARP) {
+    // ------------------------------------------------------------ activation loader
+    // Lane l gathers rows l, l+32, l+64, l+96 of the m-tile (16-byte cp.async
+    // into the swizzled positions; rows past the expert's count are zero
+    // filled) up to BS k-tiles ahead; each lane's completion arrives on the
+    // stage's barrier (cp.async.mbarrier.arrive.noinc).
+    int kg = 0;
+    bool ok = true;
+    for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x) {
+      const int2 mt = g.mtiles[wi / NT];
+      const int e = mt.x, m0 = mt.y;
+      const int base = g.offsets[e];
+      const int Me = g.offsets[e + 1] - base;
+      const __nv_bfloat16* src[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = lane + 32 * q;
+        src[q] = nullptr;
+        if (m0 + r < Me) {
+          const int pos = base + m0 + r;
+          src[q] = GATEUP ? g.xb + (size_t)tc_pair_row(g.perm[pos], g.T, g.k) * g.H : g.hin + (size_t)pos * g.F;
+        }
+      }
+      const __nv_bfloat16* zsrc = GATEUP ? g.xb : g.hin;  // any valid address: nothing is read
+      for (int kt = 0; kt < KT; ++kt, ++kg) {
+        const int stage = kg % BS;
+        if (!tc::mbar_wait(&empty[stage], ((kg / BS) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_st = sA + stage * TC_A_BYTES;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = lane + 32 * q;
+          const bool valid = src[q] != nullptr;
+          const __nv_bfloat16* s0 = valid ? src[q] + kt * TC_BK : zsrc;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            tc::cp_async16(a_st + tc::sw128_offset(r, c), s0 + (valid ? 8 * c : 0), valid);
+        }
+        tc::cp_async_arrive_noinc(&full[stage]);
+      }
+    }
+    tc::cp_async_wait_all();
   } else {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = tc::idesc_bf16_f32(TC_BM, TC_BN);
@@ -372,6 +388,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
           ok = false;
           break;
         }
+        // the activation tile was written by cp.async (generic proxy): order it
+        // before the tensor core's reads
+        tc::fence_proxy_async_smem();
         tc::tc_fence_after();
         if (lane == 0) {
           const uint32_t a_addr = tc::smem_u32(sA + stage * TC_A_BYTES);
@@ -485,23 +504,28 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
   }
 }
 
-// X [T][H] fp32 -> bf16 (round to nearest even), the A operand of gate/up.
+// X [T][H] fp32 -> bf16 (round to nearest even) in the operand K order
+// (kPerm8 inside each group of 8), the A operand of the tensor-core path.
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y,
-                                                      size_t n4) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4*>(x)[i];
-    uint2 o;
-    o.x = tc::pack_bf16x2(v.x, v.y);
-    o.y = tc::pack_bf16x2(v.z, v.w);
-    reinterpret_cast<uint2*>(y)[i] = o;
+                                                      size_t n8) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(x)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(x)[2 * i + 1];
+    // group (0..7) = a.x a.y a.z a.w b.x b.y b.z b.w -> order 0,4,1,5,2,6,3,7
+    uint4 o;
+    o.x = tc::pack_bf16x2(a.x, b.x);
+    o.y = tc::pack_bf16x2(a.y, b.y);
+    o.z = tc::pack_bf16x2(a.z, b.z);
+    o.w = tc::pack_bf16x2(a.w, b.w);
+    reinterpret_cast<uint4*>(y)[i] = o;
   }
 }
 
 cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, size_t n, cudaStream_t st) {
-  const size_t n4 = n / 4;
-  int blocks = (int)((n4 + 255) / 256);
+  const size_t n8 = n / 8;
+  int blocks = (int)((n8 + 255) / 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
-  to_bf16_kernel<<<blocks, 256, 0, st>>>(x, y, n4);
+  to_bf16_kernel<<<blocks, 256, 0, st>>>(x, y, n8);
   return cudaGetLastError();
 }
 
@@ -548,7 +572,7 @@ cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st) {
   TcArgs a{};
   a.W = p.W; a.W2 = p.W2; a.S = p.S; a.S2 = p.S2;
   a.offsets = p.offsets; a.perm = p.perm; a.mtiles = p.mtiles; a.n_mtiles = p.n_mtiles;
-  a.X = p.X; a.xb = p.xb; a.hout = p.hout;
+  a.X = p.X; a.xb = p.xb; a.hout = p.hout; a.a_rows = p.a_rows;
   a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
   const int items = p.max_mtiles * (p.F / 128);
   return p.qt == QMOE_Q5K ? tc_launch_t<true, QMOE_Q5K>(a, items, st) : tc_launch_t<true, QMOE_Q4K>(a, items, st);
@@ -558,7 +582,7 @@ cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
   TcArgs a{};
   a.W = p.W; a.S = p.S;
   a.offsets = p.offsets; a.perm = p.perm; a.mtiles = p.mtiles; a.n_mtiles = p.n_mtiles;
-  a.hin = p.hin; a.yout = p.yout; a.yout_f32 = p.yout_f32;
+  a.hin = p.hin; a.yout = p.yout; a.yout_f32 = p.yout_f32; a.a_rows = p.a_rows;
   a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
   const int items = p.max_mtiles * (p.H / TC_BN);
   return p.qt == QMOE_Q5K ? tc_launch_t<false, QMOE_Q5K>(a, items, st) : tc_launch_t<false, QMOE_Q4K>(a, items, st);
