@@ -131,6 +131,7 @@ int qmoe_moe_route(const float *X, const float *Wr, int T, int H, int E, int k,
  * memory); qmoe_last_path() tells which ran.
  * A rank partial of the intermediate split is computed by passing that
  * rank's slices of the packed tensors with F halved.
+ * T * (k + 1) must stay below 2^24 (QMOE_ERR_ARG otherwise).
  */
 size_t qmoe_moe_workspace_bytes(const qmoe_moe_desc *d, int T);
 int qmoe_moe_forward(const qmoe_moe_desc *d, const float *X, const float *R,

@@ -87,7 +87,7 @@ inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace carve-up (every piece 256-byte aligned).
 struct MoeWs {
-  size_t part, ids, w, route, offsets, perm, active, n_active, chunk, mtiles, n_mtiles, xb, h, y, total;
+  size_t part, ids, w, route, offsets, perm, active, n_active, chunk, chunks, n_chunks, xb, h, y, total;
   int nsplit;
 };
 
@@ -106,11 +106,13 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   L.active = o;   o += up256(sizeof(int32_t) * (E + 1));
   L.n_active = o; o += 256;
   L.chunk = o;    o += up256(sizeof(int32_t) * (size_t)perm_chunks((int)P) * E);
-  L.mtiles = o;   o += up256(sizeof(int2) * (size_t)tc_max_mtiles(T, k, E, 1));
-  L.n_mtiles = o; o += 256;
-  L.xb = o;       o += up256(sizeof(uint16_t) * (size_t)T * H);
+  L.chunks = o;   o += up256(sizeof(int2) * (size_t)tc_max_chunks(T, k, E, 1));
+  L.n_chunks = o; o += 256;
   L.h = o;        o += up256(sizeof(float) * rows * F);
   L.y = o;        o += up256(sizeof(float) * rows * H);
+  // the tensor-core path's bf16 tokens [rows][H] live in y's space: they are
+  // dead once the gate/up kernel has run, before the down kernel writes y
+  L.xb = L.y;
   L.total = o;
   return L;
 }
@@ -142,7 +144,7 @@ int launch_status(cudaError_t e) {
 
 // ---------------------------------------------------------------- block
 struct AttnWs {
-  size_t r, q, k, v, o, part, offsets, perm, active, n_active, mtiles, n_mtiles, xb, total;
+  size_t r, q, k, v, o, part, offsets, perm, active, n_active, chunks, n_chunks, xb, total;
   bool chunked;
 };
 
@@ -164,8 +166,8 @@ AttnWs attn_ws_layout(const qmoe_block_desc* b, int T, int pos0) {
   L.perm = o;     o += up256(sizeof(int32_t) * T);
   L.active = o;   o += 256;
   L.n_active = o; o += 256;
-  L.mtiles = o;   o += up256(sizeof(int2) * (size_t)tc_max_mtiles(T, 1, 1, 0));
-  L.n_mtiles = o; o += 256;
+  L.chunks = o;   o += up256(sizeof(int2) * (size_t)tc_max_chunks(T, 1, 1, 0));
+  L.n_chunks = o; o += 256;
   L.xb = o;       o += up256(sizeof(uint16_t) * T * (Q > (size_t)H ? Q : (size_t)H));
   L.total = o;
   return L;
@@ -197,21 +199,21 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
   g_launches.fetch_add(1);
   if (e != cudaSuccess) return e;
   if (T > g_gemm_threshold.load() && N % 256 == 0) {
-    int2* mtiles = reinterpret_cast<int2*>(base + L.mtiles);
-    int32_t* n_mtiles = reinterpret_cast<int32_t*>(base + L.n_mtiles);
+    int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
+    int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
     __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
-    if ((e = launch_build_mtiles(offsets, 1, mtiles, n_mtiles, st)) != cudaSuccess) return e;
-    if ((e = launch_to_bf16(x, xb, (size_t)T * K, st)) != cudaSuccess) return e;
+    if ((e = launch_build_chunks(offsets, 1, chunks, n_chunks, st)) != cudaSuccess) return e;
+    if ((e = launch_to_bf16(x, xb, T, K, nullptr, T, 1, st)) != cudaSuccess) return e;
     GroupedTcArgs p{};
     p.W = static_cast<const uint8_t*>(W);
     p.qt = qt;
     p.offsets = offsets;
     p.perm = perm;
-    p.mtiles = mtiles;
-    p.n_mtiles = n_mtiles;
-    p.max_mtiles = tc_max_mtiles(T, 1, 1, 0);
+    p.chunks = chunks;
+    p.n_chunks = n_chunks;
+    p.max_chunks = tc_max_chunks(T, 1, 1, 0);
     p.hin = xb;
-    p.a_rows = T;
+    p.tok_rows = T;
     p.yout_f32 = y;
     p.T = T;
     p.k = 1;
@@ -440,7 +442,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
                      qmoe_stream_t stream) {
   int r = check_desc(d);
   if (r != QMOE_OK) return r;
-  if (T < 0) return QMOE_ERR_ARG;
+  if (T < 0 || (long long)T * (d->k + 1) >= (1LL << 24)) return QMOE_ERR_ARG;
   if ((ids == nullptr) != (w == nullptr)) return QMOE_ERR_NULL;
   if (T == 0) {
     g_last_path = QMOE_PATH_NONE;
@@ -542,23 +544,23 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
 
   if (T > g_gemm_threshold.load()) {
     // grouped dequant + bf16 tcgen05 GEMM path: h and y are bf16
-    int2* mtiles = reinterpret_cast<int2*>(base + L.mtiles);
-    int32_t* n_mtiles = reinterpret_cast<int32_t*>(base + L.n_mtiles);
+    int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
+    int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
     __nv_bfloat16* h16 = reinterpret_cast<__nv_bfloat16*>(hbuf);
     __nv_bfloat16* y16 = reinterpret_cast<__nv_bfloat16*>(y);
     __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
     e = staged(QMOE_STAGE_ROUTE, 2, st, [&] {
-      cudaError_t e2 = launch_build_mtiles(offsets, E, mtiles, n_mtiles, st);
+      cudaError_t e2 = launch_build_chunks(offsets, E, chunks, n_chunks, st);
       if (e2 != cudaSuccess) return e2;
-      return launch_to_bf16(X, xb, (size_t)T * H, st);
+      return launch_to_bf16(X, xb, (int)(P + (has_shared ? T : 0)), H, perm, T, k, st);
     });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
     GroupedTcArgs p{};
     p.offsets = offsets;
     p.perm = perm;
-    p.mtiles = mtiles;
-    p.n_mtiles = n_mtiles;
-    p.max_mtiles = tc_max_mtiles(T, k, E, has_shared);
+    p.chunks = chunks;
+    p.n_chunks = n_chunks;
+    p.max_chunks = tc_max_chunks(T, k, E, has_shared);
     p.T = T;
     p.k = k;
     p.E = E;
@@ -570,9 +572,8 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     p.S = static_cast<const uint8_t*>(d->Sg);
     p.S2 = static_cast<const uint8_t*>(d->Su);
     p.qt = d->gate_type;
-    p.X = X;
     p.xb = xb;
-    p.a_rows = T;
+    p.tok_rows = (int)(P + (has_shared ? T : 0));
     p.hout = h16;
     e = staged(QMOE_STAGE_GATEUP, 1, st, [&] { return launch_gateup_tc(p, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
@@ -582,7 +583,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     p.S2 = nullptr;
     p.qt = d->down_type;
     p.hin = h16;
-    p.a_rows = P + T;
+    p.tok_rows = (int)(P + (has_shared ? T : 0));
     p.yout = y16;
     e = staged(QMOE_STAGE_DOWN, 1, st, [&] { return launch_down_tc(p, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;

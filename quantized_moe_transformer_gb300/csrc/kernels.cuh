@@ -45,25 +45,25 @@ struct GroupedTcArgs {
   int qt;
   const int32_t* offsets;
   const int32_t* perm;
-  const int2* mtiles;
-  const int32_t* n_mtiles;
-  int max_mtiles;
-  const float* X;
+  const int2* chunks;       // token chunks of at most 128 rows, built on the device
+  const int32_t* n_chunks;
+  int max_chunks;           // grid bound on the chunk count
   const __nv_bfloat16* xb;
   const __nv_bfloat16* hin;
   __nv_bfloat16* hout;
   __nv_bfloat16* yout;
   float* yout_f32;  // down pass: write fp32 instead of bf16 when not null
-  int a_rows;       // rows of the bf16 activation matrix (xb: T; hin: its row count)
+  int tok_rows;     // rows of the token matrix (xb for gate/up, hin for down)
   int T, k, E, H, F;
   int* status;
 };
-int tc_max_mtiles(int T, int k, int E, int has_shared);
-cudaError_t launch_build_mtiles(const int32_t* offsets, int E, int2* mtiles, int32_t* n_mtiles,
+int tc_max_chunks(int T, int k, int E, int has_shared);
+cudaError_t launch_build_chunks(const int32_t* offsets, int E, int2* chunks, int32_t* n_chunks,
                                 cudaStream_t st);
 cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st);
 cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st);
-cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, size_t n, cudaStream_t st);
+cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, int rows, int K, const int32_t* perm, int T, int k,
+                           cudaStream_t st);
 cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* w, const float* R, float* out,
                                 int T, int H, int k, int has_shared, cudaStream_t st);
 

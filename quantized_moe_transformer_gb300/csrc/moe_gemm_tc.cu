@@ -3,51 +3,78 @@
 // "Distributed CPU: Zip Fusion Beyond Tensor Parallelism", "Prefill First, Then
 // One Matrix-Work Scheduler": with many rows per weight region each packed
 // weight is reused across the rows and the region becomes GEMM-bound. Here the
-// rows routed to one expert (contiguous in permutation order) form the M side
-// of a tile; the expert's packed Q4_K/Q5_K rows are dequantised to bf16 in
-// shared memory and fed to tcgen05.mma with the fp32 accumulator in tensor
-// memory ("What PR #382 Now Splits" in "CKE Zip: From Splitting Tokens To
-// Splitting Qwen3.5 Weights": gate, up, SwiGLU and down per expert).
+// rows routed to one expert (contiguous in permutation order) are cut into
+// chunks of at most 128 tokens; per work item one expert's packed Q4_K/Q5_K
+// rows are dequantised to bf16 and multiplied with the chunk's activations on
+// the tensor cores, fp32 accumulation in tensor memory ("What PR #382 Now
+// Splits" in "CKE Zip: From Splitting Tokens To Splitting Qwen3.5 Weights":
+// gate, up, SwiGLU and down per expert).
 //
-// One persistent CTA per SM walks work items (m-tile of 128 rows of one expert,
-// n-tile of 256 output columns). Warp roles (416 threads):
+// The weights are the MMA's M side and the tokens its N side: the
+// dequantised weights go from registers straight into tensor memory
+// (tcgen05.st) and are read there as the A operand, so they never pass through
+// shared memory; only the token tile is staged in shared memory (128-byte
+// swizzled, K-major). N is the chunk's token count rounded up to 16, so a
+// chunk of 20 tokens costs the tensor core 32 columns, not 128 rows.
+//
+// A work item is (token chunk, weight block). A weight block is two 128-row
+// matrices A0, A1 with accumulators D0, D1 (TMEM columns 0-127, 128-255):
+// gate rows and the matching up rows (gate/up pass: SwiGLU pairs lane f of D0
+// with lane f of D1 in one thread), or two consecutive 128-row blocks of the
+// down matrix. One persistent CTA per SM walks the items; warp roles (768
+// threads):
 //   warps 0-3   epilogue: TMEM -> registers (warp w reads lanes 32w..32w+31),
-//               fused SwiGLU (gate/up) or bf16 store (down);
-//   warps 4-11  producers: thread p owns weight row p of the n-tile; it keeps
-//               the packed super-block of its row in registers, prefetching
-//               the next super-blocks in a bulk-copy ring while it
-//               dequantises the current one to bf16, written in the
-//               128-byte-swizzled K-major layout the MMA descriptors describe;
-//   warp 12     allocates 512 TMEM columns (two 256-column accumulators) and
-//               issues the MMAs from one lane;
-//   warp 13     gathers the activation tile of each k-tile (the rows of an
-//               m-tile, through the permutation) with cp.async, up to BS
-//               k-tiles ahead of the MMAs.
-// A 4-stage shared-memory ring (48 KB per stage) decouples producers and the
-// MMA issuer; the two accumulators let the epilogue of one tile overlap the
-// main loop of the next. Every wait is bounded: on time-out the CTA records
-// QMOE_ERR_TIMEOUT, drains its MMAs, frees its TMEM and returns.
+//               SwiGLU to bf16 h (gate/up) or the y store (down), leaving
+//               through a small shared-memory transpose in 16-byte stores;
+//   warps 4-19  producers: warp 4 + pw covers lane quarter pw % 4 of A0
+//               (pw / 4 even) or A1, and sub-block pw / 8 of each k-tile; a
+//               thread dequantises 32 weights of its row per k-tile in bf16x2
+//               arithmetic from the packed super-block ring and stores them
+//               into the k-tile's A stage in TMEM (columns 256 + 64 s ..);
+//   warps 20,23 issue the MMAs of D0 and D1 (one lane each); warp 20 also
+//               allocates the 512 TMEM columns;
+//   warp 21     copies each k-tile's token rows into the stage's
+//               shared-memory tile (one lane, 2-D tensor copies);
+//   warp 22     copies the packed weight rows into the super-block ring (one
+//               lane, 2-D tensor copies).
+// Four stages (A in TMEM, token tile in shared memory) decouple the roles.
+// Every wait is bounded: on time-out the CTA records QMOE_ERR_TIMEOUT, drains
+// its MMAs, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
 #include "kernels.cuh"
 #include "tc.cuh"
 
 namespace qmoe {
 
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64;
-constexpr int TC_THREADS = 448;
-constexpr int TC_MMA_WARP = 12;
-constexpr int TC_LOAD_WARP = 13;
-constexpr int TC_PRODUCERS = 256;
-constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
-constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 32 KB
-// Per weight format: RS stages of packed super-blocks (256 rows each, filled by
-// bulk copies) and BS stages of bf16 operand tiles, within 227 KB.
+constexpr int TC_N = 128;       // tokens per chunk (largest MMA N used)
+constexpr int TC_BK = 64;       // K per stage
+constexpr int TC_STAGES = 4;
+constexpr int TC_PRODUCER_WARPS = 16;
+constexpr int TC_MMA_WARP = 4 + TC_PRODUCER_WARPS;  // 20
+constexpr int TC_LOAD_WARP = TC_MMA_WARP + 1;       // 21: token tiles
+constexpr int TC_RAW_WARP = TC_MMA_WARP + 2;        // 22: packed weights
+constexpr int TC_MMA_WARP2 = TC_MMA_WARP + 3;       // 23: MMAs of the second accumulator
+constexpr int TC_THREADS = 32 * (TC_MMA_WARP2 + 1); // 768
+constexpr int TC_B_BYTES = TC_N * TC_BK * 2;  // 16 KB token tile per stage
+constexpr int TC_EPI_BYTES = 2048;            // per epilogue warp: 16 tokens x 32 values x 4 B
+constexpr uint32_t TC_D1_COL = 128;      // D0 at column 0, D1 at 128
+constexpr uint32_t TC_A_COL = 256;       // A stage s: A0 at 256 + 64 s, A1 at + 32
+constexpr uint32_t TC_A_STAGE_COLS = 64;
+
+// Packed weights are staged per super-block: RS ring stages of 256 rows (A0
+// rows, then A1 rows), each filled by one or two 2-D tensor copies.
 template <int QT>
 struct TcCfg {
   static constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
-  static constexpr int RS = 2;
-  static constexpr int BS = QT == QMOE_Q5K ? 2 : 3;
-  static constexpr int RAW_STAGE = TC_PRODUCERS * BYTES;
-  static constexpr int SMEM = BS * (TC_A_BYTES + TC_B_BYTES) + RS * RAW_STAGE + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int RS = QT == QMOE_Q5K ? 3 : 4;
+  static constexpr int RAW_STAGE = 256 * BYTES;
+  static constexpr int SMEM = TC_STAGES * TC_B_BYTES + RS * RAW_STAGE + 4 * TC_EPI_BYTES + 1024 /*align*/ +
+                              256 /*barriers*/;
 };
 
 struct TcArgs {
@@ -57,125 +84,142 @@ struct TcArgs {
   const uint8_t* S2;  // shared expert counterpart of W2
   const int32_t* offsets;
   const int32_t* perm;
-  const int2* mtiles;  // (expert, first row) per m-tile
-  const int32_t* n_mtiles;
-  const float* X;               // gate/up A source, [T][H] fp32
-  const __nv_bfloat16* xb;      // gate/up A source, [T][H] bf16 (converted X)
-  const __nv_bfloat16* hin;     // down A source, [P+T][F] bf16
+  const int2* chunks;  // (expert, first row | (rows - 1) << 24) per token chunk
+  const int32_t* n_chunks;
+  const __nv_bfloat16* xb;      // gate/up token source, [P+T][H] bf16: X rows in permutation order
+  const __nv_bfloat16* hin;     // down token source, [P+T][F] bf16
   __nv_bfloat16* hout;          // gate/up output, [P+T][F] bf16
   __nv_bfloat16* yout;          // down output, [P+T][H] bf16
   float* yout_f32;              // down output in fp32 instead, when not null
-  int a_rows;                   // rows of the activation tensor the TMA map covers
   int T, k, E, H, F;
   int* status;
 };
 
-__device__ __forceinline__ int tc_pair_row(int p, int T, int k) { return p < T * k ? p / k : p - T * k; }
-
-// Packed super-block of one weight row held in registers (16-byte chunks).
-template <int QT>
-struct RawBlock {
-  static constexpr int N = (QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES) / 16;
-  uint4 c[N];
+// Tensor maps of the packed weights as 2-D byte arrays [rows][row bytes]:
+// w/w2 the routed experts' gate/up (or down in w), s/s2 the shared expert's.
+struct TcMaps {
+  CUtensorMap w, w2, s, s2;
+  CUtensorMap tok;  // token rows [rows][K] bf16, 128-byte swizzled boxes of 16 rows x 64
 };
 
-template <int QT>
-__device__ __forceinline__ void load_raw(RawBlock<QT>& r, const uint8_t* blk) {
-  const uint4* p = reinterpret_cast<const uint4*>(blk);
-#pragma unroll
-  for (int i = 0; i < RawBlock<QT>::N; ++i) r.c[i] = __ldg(p + i);
+__device__ __forceinline__ int tc_pair_row(int p, int T, int k) { return p < T * k ? p / k : p - T * k; }
+
+struct Chunk {
+  int e, c0, n;
+};
+__device__ __forceinline__ Chunk chunk_at(const int2* chunks, int i) {
+  const int2 c = chunks[i];
+  return {c.x, c.y & 0xFFFFFF, (c.y >> 24) + 1};
+}
+
+// 2-D tensor copy of the box at (x, y) into shared memory, completing its
+// bytes on ``bar``.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
+      : "memory");
 }
 
 // K order inside every group of 8 consecutive K values of the tensor-core
-// operands: element e of a 16-byte chunk holds K offset kPerm8[e]. The weight
-// dequantisation below produces this order directly (a bf16x2 word takes the
-// quants of weights i and i+4 from one 32-bit quant word), and the activation
-// producers (the bf16 conversion of X and the gate/up epilogue writing h)
-// store their rows in the same order, so the dot products are unchanged.
-__device__ constexpr int kPerm8[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+// operands: element e of a group holds K offset kPerm8[e],
+//   kPerm8 = {0, 4, 1, 5, 2, 6, 3, 7}.
+// The weight dequantisation below produces this order directly (a bf16x2
+// word takes the quants of weights i and i+4 from one 32-bit quant word), and
+// the activation producers (the bf16 conversion of X and the gate/up epilogue
+// writing h) store their rows in the same order, so the dot products are
+// unchanged.
+// Position within its group of 8 at which K offset f % 8 is stored (the
+// inverse of kPerm8), as an index into the row.
+__device__ __forceinline__ int kperm_slot(int f) { return (f & ~7) | ((f & 3) << 1) | ((f >> 2) & 1); }
 
-// Dequantises sub-blocks j0, j0+1 (64 weights) of a register-held super-block
-// into 8 swizzled 16-byte bf16 chunks of row ``r`` of a B stage, in bf16x2
-// arithmetic: q is exact (the quant bits under the exponent of 128.0, minus
-// 128), then w = q * (d*s_j) - dmin*m_j in one bf16x2 FMA with the two scales
-// rounded to bf16.
-template <int QT, int J0>
-__device__ __forceinline__ void dequant_store(const RawBlock<QT>& raw, uint8_t* stage, int r) {
+// Dequantises sub-block j (32 weights) into 16 bf16x2 words in kPerm8 order,
+// in bf16x2 arithmetic: q is exact (the quant bits under the exponent of
+// 128.0, minus 128), then w = q * (d*s_j) - dmin*m_j in one bf16x2 FMA with the
+// two scales rounded to bf16. ``hdr`` is the super-block's first 16 bytes,
+// ``qv`` the sub-block's 16 quant bytes, ``hb`` (Q5_K) its 32 high bits.
+template <int QT>
+__device__ __forceinline__ void dequant_sub(const uint4 hdr, const uint4 qv, uint32_t hb, int j, uint32_t* o) {
   KHeader h;
-  const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&raw.c[0].x));
+  const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
   h.d = dd.x;
   h.dmin = dd.y;
-  h.f0 = raw.c[0].y;
-  h.f1 = raw.c[0].z;
-  h.f2 = raw.c[0].w;
+  h.f0 = hdr.y;
+  h.f1 = hdr.z;
+  h.f2 = hdr.w;
   const __nv_bfloat162 m128 = __float2bfloat162_rn(-128.f);
+  const float2 sc = sub_scale(h, j);
+  const __nv_bfloat162 ds2 = __float2bfloat162_rn(sc.x);
+  const __nv_bfloat162 ndm2 = __float2bfloat162_rn(-sc.y);
+  const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const int j = J0 + s;
-    const float2 sc = sub_scale(h, j);
-    const __nv_bfloat162 ds2 = __float2bfloat162_rn(sc.x);
-    const __nv_bfloat162 ndm2 = __float2bfloat162_rn(-sc.y);
-    const uint4 q = QT == QMOE_Q5K ? raw.c[3 + j] : raw.c[1 + j];
-    uint32_t hb = 0;
-    if (QT == QMOE_Q5K) {
-      const uint4 hq = raw.c[1 + (j >> 2)];
-      const uint32_t hw[4] = {hq.x, hq.y, hq.z, hq.w};
-      hb = hw[j & 3];
-    }
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  for (int n = 0; n < 4; ++n) {
 #pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        // quants of weights 8n+i and 8n+i+4 as bf16 128+q in the two halves
-        uint32_t x = ((w[n] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-        if (QT == QMOE_Q5K) x |= (((hb >> (8 * n + i)) & 0x11u) * 0x10010u) & 0x00100010u;
-        __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
-        v = __hadd2(v, m128);             // q, exact
-        v = __hfma2(v, ds2, ndm2);        // q*d*s - dmin*m, one rounding
-        o[i] = *reinterpret_cast<uint32_t*>(&v);
-      }
-      *reinterpret_cast<uint4*>(stage + tc::sw128_offset(r, 4 * s + n)) = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int i = 0; i < 4; ++i) {
+      // quants of weights 8n+i and 8n+i+4 as bf16 128+q in the two halves
+      uint32_t x = ((w[n] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+      if (QT == QMOE_Q5K) x |= (((hb >> (8 * n + i)) & 0x11u) * 0x10010u) & 0x00100010u;
+      __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
+      v = __hadd2(v, m128);             // q, exact
+      v = __hfma2(v, ds2, ndm2);        // q*d*s - dmin*m, one rounding
+      o[4 * n + i] = *reinterpret_cast<uint32_t*>(&v);
     }
   }
 }
 
+__device__ __forceinline__ int pick_row(const int (&p)[4], int i) {
+  return i == 0 ? p[0] : (i == 1 ? p[1] : (i == 2 ? p[2] : p[3]));
+}
+
+__device__ __forceinline__ uint32_t pick_word(const uint4 v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
 template <bool GATEUP, int QT>
-__global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
+__global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, const __grid_constant__ TcMaps maps) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned start, reached by pointer arithmetic on the shared
+  // array so that accesses stay shared-memory instructions
+  const uint32_t s0 = tc::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((s0 + 1023u) & ~1023u) - s0);
+  constexpr int S = TC_STAGES;
   using Cfg = TcCfg<QT>;
-  constexpr int BS = Cfg::BS, RS = Cfg::RS;
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + BS * TC_A_BYTES;
-  uint8_t* sRaw = sB + BS * TC_B_BYTES;              // [RS][256 rows][BYTES]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + RS * Cfg::RAW_STAGE);
-  uint64_t* full = bars;                     // [BS]
-  uint64_t* empty = bars + BS;               // [BS]
-  uint64_t* raw_full = bars + 2 * BS;        // [RS]
-  uint64_t* acc_full = raw_full + RS;        // [2]
-  uint64_t* acc_empty = acc_full + 2;        // [2]
-  uint64_t* drain = acc_empty + 2;           // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  constexpr int RS = Cfg::RS, BYTES = Cfg::BYTES;
+  uint8_t* sB = smem;                                         // [S][TC_N][128 B] token tiles
+  uint8_t* sRaw = smem + S * TC_B_BYTES;                      // [RS][256][BYTES] packed rows
+  uint8_t* sEpi = sRaw + RS * Cfg::RAW_STAGE;                 // [4][TC_EPI_BYTES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + 4 * TC_EPI_BYTES);
+  uint64_t* full = bars;                // [S]  A stage stored + token tile landed
+  uint64_t* empty = bars + S;           // [S]  MMAs of the stage done
+  uint64_t* raw_full = bars + 2 * S;    // [RS] packed rows landed
+  uint64_t* raw_empty = raw_full + RS;  // [RS] packed rows consumed
+  uint64_t* acc_full = raw_empty + RS;  // [1]
+  uint64_t* acc_empty = acc_full + 1;   // [1]
+  uint64_t* drain = acc_empty + 1;      // [2] one per MMA warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NT = GATEUP ? g.F / 128 : g.H / TC_BN;      // n-tiles per m-tile
-  const int KT = GATEUP ? g.H / TC_BK : g.F / TC_BK;    // k-tiles
-  const int total = g.n_mtiles[0] * NT;
+  const int NB = GATEUP ? g.F / 128 : g.H / 256;      // weight blocks per chunk
+  const int KT = GATEUP ? g.H / TC_BK : g.F / TC_BK;  // k-tiles
+  const int KB = KT / 4;                              // super-blocks along K
+  const int total = g.n_chunks[0] * NB;
+  const int n_mine = (int)blockIdx.x < total ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < BS; ++i) {
-      tc::mbar_init(&full[i], TC_PRODUCERS + 32);  // + one cp.async completion per loader lane
-      tc::mbar_init(&empty[i], 1);
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], TC_PRODUCER_WARPS + 1);  // + the token loader's arrive (with its bytes)
+      tc::mbar_init(&empty[i], 2);  // one commit per MMA warp
     }
-    for (int i = 0; i < RS; ++i) tc::mbar_init(&raw_full[i], TC_PRODUCERS);
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&acc_full[i], 1);
-      tc::mbar_init(&acc_empty[i], 128);
+    for (int i = 0; i < RS; ++i) {
+      tc::mbar_init(&raw_full[i], 1);
+      tc::mbar_init(&raw_empty[i], TC_PRODUCER_WARPS);
     }
-    tc::mbar_init(drain, 1);
+    tc::mbar_init(acc_full, 2);
+    tc::mbar_init(acc_empty, 4);
+    tc::mbar_init(&drain[0], 1);
+    tc::mbar_init(&drain[1], 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -187,235 +231,272 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
 
   if (warp < 4) {
     // ------------------------------------------------------------ epilogue
+    // Per 16 tokens: TMEM -> registers, the values of the warp's 32 rows are
+    // transposed through shared memory so that each token's 32 outputs leave
+    // in 16-byte stores.
+    const int r = 32 * warp + lane;  // row of A0/A1 = TMEM lane
+    const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+    uint8_t* stg = sEpi + warp * TC_EPI_BYTES;
     int it = 0;
     for (int wi = blockIdx.x; wi < total; wi += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!tc::mbar_wait(&acc_full[acc], ph, abort_flag)) break;
+      // warp-uniform outcome: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(acc_full, it & 1, abort_flag))) break;
       tc::tc_fence_after();
-      const int2 mt = g.mtiles[wi / NT];
-      const int nt = wi % NT;
-      const int e = mt.x, m0 = mt.y;
-      const int row = 32 * warp + lane;
-      const int base = g.offsets[e];
-      const int Me = g.offsets[e + 1] - base;
-      const bool valid = m0 + row < Me;
-      const int pos = base + m0 + row;
-      const uint32_t tq = tmem + (uint32_t)(acc * 256) + ((uint32_t)(32 * warp) << 16);
-      if (GATEUP) {
-        __nv_bfloat16* dst = g.hout + (size_t)pos * g.F + nt * 128;
+      const Chunk ch = chunk_at(g.chunks, wi / NB);
+      const int blk = wi % NB;
+      const int pos0 = g.offsets[ch.e] + ch.c0;
+      // down: destination rows of the chunk's tokens, lane l holding tokens l + 32q
+      int prow[4] = {0, 0, 0, 0};
+      if (!GATEUP) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (lane + 32 * q < ch.n) prow[q] = g.perm[pos0 + lane + 32 * q];
+      }
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 16) {
-          uint32_t gr[16], ur[16];
-          tc::tmem_ld16x2(tq + c, tq + 128 + c, gr, ur);
-          float hv[16];
+      for (int c = 0; c < ch.n; c += 16) {
+        uint32_t a[16], b[16];
+        tc::tmem_ld16x2(tq + c, tq + TC_D1_COL + c, a, b);
+        if (GATEUP) {
+          // h[pos][f] = silu(gate) * up, in the operand K order
+          __nv_bfloat16* st16 = reinterpret_cast<__nv_bfloat16*>(stg);
+          const int col = kperm_slot(lane);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) hv[i] = silu_mul(__uint_as_float(gr[i]), __uint_as_float(ur[i]));
-          // stored in the operand K order (kPerm8 inside each group of 8)
-          uint32_t o[8];
+          for (int i = 0; i < 16; ++i)
+            st16[i * 32 + col] = __float2bfloat16_rn(silu_mul(__uint_as_float(a[i]), __uint_as_float(b[i])));
+          __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int g8 = (i >> 2) * 8, e = 2 * (i & 3);
-            o[i] = tc::pack_bf16x2(hv[g8 + kPerm8[e]], hv[g8 + kPerm8[e + 1]]);
+          for (int q = 0; q < 2; ++q) {
+            const int id = lane + 32 * q, i = id >> 2, part = id & 3;
+            if (c + i < ch.n)
+              *reinterpret_cast<uint4*>(g.hout + (size_t)(pos0 + c + i) * g.F + blk * 128 + 32 * warp + 8 * part) =
+                  reinterpret_cast<const uint4*>(stg)[id];
           }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-            d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-        }
-      } else {
-        const int pair = valid ? g.perm[pos] : 0;
-        __nv_bfloat16* dst = g.yout + (size_t)pair * g.H + nt * TC_BN;
-        float* dst32 = g.yout_f32 ? g.yout_f32 + (size_t)pair * g.H + nt * TC_BN : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < TC_BN; c += 32) {
-          uint32_t a[16], b[16];
-          tc::tmem_ld16x2(tq + c, tq + c + 16, a, b);
-          if (g.yout_f32 != nullptr) {
-            if (valid) {
-              float4* d4 = reinterpret_cast<float4*>(dst32 + c);
+          __syncwarp();
+        } else {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                d4[i] = make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]),
-                                    __uint_as_float(a[4 * i + 2]), __uint_as_float(a[4 * i + 3]));
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t* v = half ? b : a;
+            const int col0 = blk * 256 + half * 128 + 32 * warp;
+            if (g.yout_f32 != nullptr) {
+              float* s32 = reinterpret_cast<float*>(stg);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                d4[4 + i] = make_float4(__uint_as_float(b[4 * i]), __uint_as_float(b[4 * i + 1]),
-                                        __uint_as_float(b[4 * i + 2]), __uint_as_float(b[4 * i + 3]));
+              for (int i = 0; i < 16; ++i) s32[i * 32 + lane] = __uint_as_float(v[i]);
+              __syncwarp();
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int id = lane + 32 * q, i = id >> 3, part = id & 7;
+                const int t = c + i;
+                const int row = __shfl_sync(0xffffffffu, pick_row(prow, c >> 5), t & 31);
+                if (t < ch.n)
+                  *reinterpret_cast<uint4*>(g.yout_f32 + (size_t)row * g.H + col0 + 4 * part) =
+                      reinterpret_cast<const uint4*>(stg)[id];
+              }
+            } else {
+              __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) s16[i * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[i]));
+              __syncwarp();
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const int id = lane + 32 * q, i = id >> 2, part = id & 3;
+                const int t = c + i;
+                const int row = __shfl_sync(0xffffffffu, pick_row(prow, c >> 5), t & 31);
+                if (t < ch.n)
+                  *reinterpret_cast<uint4*>(g.yout + (size_t)row * g.H + col0 + 8 * part) =
+                      reinterpret_cast<const uint4*>(stg)[id];
+              }
             }
-            continue;
-          }
-          uint32_t o[16];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            o[i] = tc::pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-            o[8 + i] = tc::pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
-          }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-            d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            d4[2] = make_uint4(o[8], o[9], o[10], o[11]);
-            d4[3] = make_uint4(o[12], o[13], o[14], o[15]);
+            __syncwarp();
           }
         }
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(&acc_empty[acc]);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(acc_empty);
     }
-  } else if (warp < 4 + TC_PRODUCERS / 32) {
+  } else if (warp < 4 + TC_PRODUCER_WARPS) {
     // ------------------------------------------------------------ producers
-    // Thread p owns weight row p of the n-tile (and, p < 128, activation row
-    // p). Packed super-blocks of its row arrive by bulk copy into a ring of RS
-    // stages, RS super-blocks ahead of use; the activation row of the next
-    // k-tile is gathered with cp.async while the current k-tile is
-    // dequantised; each k-tile's operand stage is released with one arrive.
-    constexpr int BYTES = Cfg::BYTES;
-    const int p = threadIdx.x - 128;
-    const int KB = KT / 4;  // super-blocks along K
-    const size_t rb = GATEUP ? (size_t)(g.H / QK) * BYTES : (size_t)(g.F / QK) * BYTES;
-    const int n_mine = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    auto item = [&](int j) { return (int)blockIdx.x + j * (int)gridDim.x; };
-    auto row_of = [&](int wi) -> const uint8_t* {
-      const int2 mt = g.mtiles[wi / NT];
-      const int nt = wi % NT, e = mt.x;
-      if (GATEUP) {
-        const bool up = p >= 128;
-        const uint8_t* base = e < g.E ? (up ? g.W2 : g.W) + (size_t)e * g.F * rb : (up ? g.S2 : g.S);
-        return base + (size_t)(nt * 128 + (p & 127)) * rb;
+    // Warp 4 + pw covers TMEM lane quarter pw % 4 of matrix (pw / 4) % 2, and
+    // sub-block s = pw / 8 of each k-tile's two: thread = one weight row, 32
+    // weights per k-tile. The dequantisation of the next k-tile overlaps the
+    // TMEM stores of the current one.
+    const int pw = warp - 4;
+    const int mat = (pw >> 2) & 1, s = pw >> 3;
+    const int r = 32 * (pw & 3) + lane;
+    const uint32_t ta0 = tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * 32 + s * 16);
+    const uint8_t* my_row = sRaw + (size_t)(mat * 128 + r) * BYTES;
+    const int NU = n_mine * KB;
+    uint32_t wa[16], wb[16];
+    uint4 hdr = make_uint4(0, 0, 0, 0), hq0 = hdr, hq1 = hdr;
+    // loads the super-block header (and Q5_K high bits) of ring slot u % RS
+    auto open_sb = [&](int u) -> bool {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag))) return false;
+      const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
+      hdr = rp[0];
+      if (QT == QMOE_Q5K) {
+        hq0 = rp[1];
+        hq1 = rp[2];
       }
-      const uint8_t* base = e < g.E ? g.W + (size_t)e * g.H * rb : g.S;
-      return base + (size_t)(nt * TC_BN + p) * rb;
+      return true;
     };
-    auto issue_raw = [&](int u) {
-      const int j = u / KB;
-      if (j >= n_mine) return;
-      uint64_t* bar = &raw_full[u % RS];
-      tc::mbar_expect_tx(bar, BYTES);
-      tc::bulk_g2s(sRaw + (size_t)(u % RS) * Cfg::RAW_STAGE + (size_t)p * BYTES,
-                   row_of(item(j)) + (size_t)(u % KB) * BYTES, BYTES, bar);
+    auto deq = [&](int u, int kk, uint32_t* o) {
+      const int j = 2 * kk + s;
+      const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
+      const uint4 qv = rp[(QT == QMOE_Q5K ? 3 : 1) + j];
+      const uint32_t hb = QT == QMOE_Q5K ? pick_word((j >> 2) ? hq1 : hq0, j & 3) : 0u;
+      dequant_sub<QT>(hdr, qv, hb, j, o);
     };
-    for (int u = 0; u < RS; ++u) issue_raw(u);
-    bool ok = true;
+    bool ok = NU > 0 && open_sb(0);
+    if (ok) deq(0, 0, wa);
     int kg = 0;
-    for (int u = 0; u < n_mine * KB && ok; ++u) {
-      if (!tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      RawBlock<QT> cur;
-      const uint4* rp = reinterpret_cast<const uint4*>(sRaw + (size_t)(u % RS) * Cfg::RAW_STAGE + (size_t)p * BYTES);
-#pragma unroll
-      for (int i = 0; i < RawBlock<QT>::N; ++i) cur.c[i] = rp[i];
-      tc::fence_proxy_async_smem();  // these reads come before the copy that refills the slot
-      issue_raw(u + RS);
+    for (int u = 0; u < NU && ok; ++u) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        if (!tc::mbar_wait(&empty[kg % BS], ((kg / BS) & 1) ^ 1, abort_flag)) {
+        uint32_t* cur = (kk & 1) ? wb : wa;
+        uint32_t* nxt = (kk & 1) ? wa : wb;
+        const int stage = kg % S;
+        // warp-uniform outcome: the TMEM stores below are warp-collective
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], ((kg / S) & 1) ^ 1, abort_flag))) {
           ok = false;
           break;
         }
-        uint8_t* b_st = sB + (kg % BS) * TC_B_BYTES;
-        if (kk == 0) dequant_store<QT, 0>(cur, b_st, p);
-        else if (kk == 1) dequant_store<QT, 2>(cur, b_st, p);
-        else if (kk == 2) dequant_store<QT, 4>(cur, b_st, p);
-        else dequant_store<QT, 6>(cur, b_st, p);
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&full[kg % BS]);
+        tc::tc_fence_after();
+        tc::tmem_st16(ta0 + (uint32_t)stage * TC_A_STAGE_COLS, cur);
+        if (kk < 3) {
+          deq(u, kk + 1, nxt);
+        } else {
+          // every read of slot u is done: release it to the weight loader
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&raw_empty[u % RS]);
+          if (u + 1 < NU) {
+            if (!open_sb(u + 1)) ok = false;
+            else deq(u + 1, 0, nxt);
+          }
+        }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&full[stage]);
         ++kg;
+        if (!ok) break;
       }
     }
+  } else if (warp == TC_RAW_WARP) {
+    // ------------------------------------------------------------ weight loader
+    // One lane: super-block u of the CTA's item sequence goes to ring slot
+    // u % RS as 2-D tensor copies of 128 (gate/up: A0 from the gate matrix, A1
+    // from the up matrix) or 256 (down) rows x one super-block column; the
+    // next item's rows are prefetched into L2 when an item starts.
+    if (lane == 0) {
+      const int NU = n_mine * KB;
+      const size_t rb = (size_t)KB * BYTES;
+      auto block_of = [&](int j, int& e, int& y0) {
+        const int wi = (int)blockIdx.x + j * (int)gridDim.x;
+        const Chunk ch = chunk_at(g.chunks, wi / NB);
+        const int blk = wi % NB;
+        e = ch.e;
+        y0 = GATEUP ? (e < g.E ? e * g.F : 0) + blk * 128 : (e < g.E ? e * g.H : 0) + blk * 256;
+      };
+      // the item that starts about RS super-blocks after item j does
+      const int lead = (RS + KB - 1) / KB;
+      auto prefetch_item = [&](int j) {
+        if (j >= n_mine) return;
+        int e, y0;
+        block_of(j, e, y0);
+        const uint32_t rows = GATEUP ? 128u : 256u;
+        tc::prefetch_l2((e < g.E ? g.W : g.S) + (size_t)y0 * rb, rows * (uint32_t)rb);
+        if (GATEUP) tc::prefetch_l2((e < g.E ? g.W2 : g.S2) + (size_t)y0 * rb, rows * (uint32_t)rb);
+      };
+      for (int j = 0; j < lead; ++j) prefetch_item(j);
+      for (int u = 0; u < NU; ++u) {
+        const int slot = u % RS;
+        if (!tc::mbar_wait(&raw_empty[slot], ((u / RS) & 1) ^ 1, abort_flag)) break;
+        const int j = u / KB, sb = u % KB;
+        int e, y0;
+        block_of(j, e, y0);
+        if (sb == 0) prefetch_item(j + lead);
+        uint8_t* dst = sRaw + (size_t)slot * Cfg::RAW_STAGE;
+        tc::mbar_expect_tx(&raw_full[slot], 256 * BYTES);
+        const int x = sb * BYTES;
+        if (GATEUP) {
+          tma_load_2d(dst, e < g.E ? &maps.w : &maps.s, x, y0, &raw_full[slot]);
+          tma_load_2d(dst + 128 * BYTES, e < g.E ? &maps.w2 : &maps.s2, x, y0, &raw_full[slot]);
+        } else {
+          tma_load_2d(dst, e < g.E ? &maps.w : &maps.s, x, y0, &raw_full[slot]);
+        }
+      }
+    }
+    __syncwarp();
   } else if (warp == TC_LOAD_WARP) {
-    // ------------------------------------------------------------ activation loader
-    // Lane l gathers rows l, l+32, l+64, l+96 of the m-tile (16-byte cp.async
-    // into the swizzled positions; rows past the expert's count are zero
-    // filled) up to BS k-tiles ahead; each lane's completion arrives on the
-    // stage's barrier (cp.async.mbarrier.arrive.noinc).
-    int kg = 0;
-    bool ok = true;
-    for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x) {
-      const int2 mt = g.mtiles[wi / NT];
-      const int e = mt.x, m0 = mt.y;
-      const int base = g.offsets[e];
-      const int Me = g.offsets[e + 1] - base;
-      const __nv_bfloat16* src[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = lane + 32 * q;
-        src[q] = nullptr;
-        if (m0 + r < Me) {
-          const int pos = base + m0 + r;
-          src[q] = GATEUP ? g.xb + (size_t)tc_pair_row(g.perm[pos], g.T, g.k) * g.H : g.hin + (size_t)pos * g.F;
+    // ------------------------------------------------------------ token loader
+    // The chunk's rows are consecutive rows of the token matrix (X in
+    // permutation order, or h): per k-tile one lane copies them as boxes of
+    // 16 rows x 64 values with 128-byte swizzle, which is the layout the MMA's
+    // operand descriptor describes. Rows past the chunk (up to the MMA N) are
+    // the next rows of the matrix or zero fill past its end; their outputs
+    // are never stored.
+    if (lane == 0) {
+      int kg = 0;
+      bool ok = true;
+      for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x) {
+        const Chunk ch = chunk_at(g.chunks, wi / NB);
+        const int n16 = (ch.n + 15) >> 4;
+        const int pos0 = g.offsets[ch.e] + ch.c0;
+        for (int kt = 0; kt < KT; ++kt, ++kg) {
+          const int stage = kg % S;
+          if (!tc::mbar_wait(&empty[stage], ((kg / S) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* b_st = sB + stage * TC_B_BYTES;
+          tc::mbar_expect_tx(&full[stage], (uint32_t)n16 * 16 * 128);
+          for (int i = 0; i < n16; ++i)
+            tma_load_2d(b_st + i * 2048, &maps.tok, kt * TC_BK, pos0 + 16 * i, &full[stage]);
         }
-      }
-      const __nv_bfloat16* zsrc = GATEUP ? g.xb : g.hin;  // any valid address: nothing is read
-      for (int kt = 0; kt < KT; ++kt, ++kg) {
-        const int stage = kg % BS;
-        if (!tc::mbar_wait(&empty[stage], ((kg / BS) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint8_t* a_st = sA + stage * TC_A_BYTES;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = lane + 32 * q;
-          const bool valid = src[q] != nullptr;
-          const __nv_bfloat16* s0 = valid ? src[q] + kt * TC_BK : zsrc;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            tc::cp_async16(a_st + tc::sw128_offset(r, c), s0 + (valid ? 8 * c : 0), valid);
-        }
-        tc::cp_async_arrive_noinc(&full[stage]);
       }
     }
-    tc::cp_async_wait_all();
-  } else {
-    // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = tc::idesc_bf16_f32(TC_BM, TC_BN);
-    int stage = 0;
-    uint32_t phase = 0;
+    __syncwarp();
+  } else if (warp == TC_MMA_WARP || warp == TC_MMA_WARP2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two warps, one per accumulator (D0 from A0, D1 from A1), each issuing
+    // from one lane and committing its own MMAs: a commit holds up the
+    // issuing thread for a while, and the other warp's MMAs fill that gap.
+    const int which = warp == TC_MMA_WARP ? 0 : 1;
+    const uint32_t d_tmem = tmem + (uint32_t)which * TC_D1_COL;
+    int kg = 0;
     int it = 0;
     bool ok = true;
     for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!tc::mbar_wait(&acc_empty[acc], ph ^ 1, abort_flag)) break;
+      const Chunk ch = chunk_at(g.chunks, wi / NB);
+      const uint32_t idesc = tc::idesc_bf16_f32(128, (ch.n + 15) & ~15);
+      if (!tc::mbar_wait(acc_empty, (it & 1) ^ 1, abort_flag)) break;
       tc::tc_fence_after();
-      const uint32_t d_tmem = tmem + (uint32_t)(acc * 256);
-      for (int kt = 0; kt < KT; ++kt) {
-        if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
+      for (int kt = 0; kt < KT; ++kt, ++kg) {
+        const int stage = kg % S;
+        if (!tc::mbar_wait(&full[stage], (kg / S) & 1, abort_flag)) {
           ok = false;
           break;
         }
-        // the activation tile was written by cp.async (generic proxy): order it
-        // before the tensor core's reads
-        tc::fence_proxy_async_smem();
         tc::tc_fence_after();
         if (lane == 0) {
-          const uint32_t a_addr = tc::smem_u32(sA + stage * TC_A_BYTES);
           const uint32_t b_addr = tc::smem_u32(sB + stage * TC_B_BYTES);
+          const uint32_t a = tmem + TC_A_COL + (uint32_t)stage * TC_A_STAGE_COLS + (uint32_t)which * 32;
 #pragma unroll
-          for (int kk = 0; kk < TC_BK / 16; ++kk) {
-            tc::mma_bf16(d_tmem, tc::sw128_desc(a_addr + 32 * kk), tc::sw128_desc(b_addr + 32 * kk), idesc,
-                         (kt | kk) != 0);
-          }
+          for (int kk = 0; kk < TC_BK / 16; ++kk)
+            tc::mma_bf16_ts(d_tmem, a + 8 * kk, tc::sw128_desc(b_addr + 32 * kk), idesc, (kt | kk) != 0);
           tc::mma_commit(&empty[stage]);
         }
         __syncwarp();
-        if (++stage == BS) {
-          stage = 0;
-          phase ^= 1;
-        }
       }
-      if (ok && lane == 0) tc::mma_commit(&acc_full[acc]);
+      if (ok && lane == 0) tc::mma_commit(acc_full);
       __syncwarp();
     }
     // drain: every MMA this thread issued has completed before TMEM is freed
     if (lane == 0) {
-      tc::mma_commit(drain);
+      tc::mma_commit(&drain[which]);
       volatile int never = 0;
-      tc::mbar_wait(drain, 0, &never);
+      tc::mbar_wait(&drain[which], 0, &never);
     }
     __syncwarp();
   }
@@ -427,18 +508,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(TcArgs g) {
   if (warp == TC_MMA_WARP) tc::tmem_dealloc(tmem, 512);
 }
 
-// Builds the m-tile list: for every expert with rows (the shared expert last),
-// one entry per 128 rows. One CTA; the scan runs in warp 0.
-__global__ void __launch_bounds__(1024) build_mtiles_kernel(const int32_t* __restrict__ offsets, int E,
-                                                            int2* __restrict__ mtiles,
-                                                            int32_t* __restrict__ n_mtiles) {
-  extern __shared__ int32_t start[];  // [E+1] exclusive scan of tile counts
+// Builds the token-chunk list: every expert with rows (the shared expert
+// last) is cut into ceil(rows / 128) chunks of near-equal size (first row
+// below 2^24, packed with the row count). One CTA; the scan of chunk counts
+// runs in warp 0.
+__global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __restrict__ offsets, int E,
+                                                            int2* __restrict__ chunks,
+                                                            int32_t* __restrict__ n_chunks) {
+  extern __shared__ int32_t start[];  // [E+1] exclusive scan of chunk counts
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
     int run = 0;
     for (int b = 0; b <= E; b += 32) {
       const int e = b + lane;
-      const int c = e <= E ? (offsets[e + 1] - offsets[e] + TC_BM - 1) / TC_BM : 0;
+      const int c = e <= E ? (offsets[e + 1] - offsets[e] + TC_N - 1) / TC_N : 0;
       int incl = c;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -448,13 +531,19 @@ __global__ void __launch_bounds__(1024) build_mtiles_kernel(const int32_t* __res
       if (e <= E) start[e] = run + incl - c;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) n_mtiles[0] = run;
+    if (lane == 0) n_chunks[0] = run;
   }
   __syncthreads();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     const int Me = offsets[e + 1] - offsets[e];
-    int s = start[e];
-    for (int m0 = 0; m0 < Me; m0 += TC_BM) mtiles[s++] = make_int2(e, m0);
+    if (Me <= 0) continue;
+    const int nc = (Me + TC_N - 1) / TC_N;
+    for (int i = 0; i < nc; ++i) {
+      // rows [i*Me/nc, (i+1)*Me/nc): between 1 and 128 of them
+      const int c0 = (int)((long long)i * Me / nc);
+      const int c1 = (int)((long long)(i + 1) * Me / nc);
+      chunks[start[e] + i] = make_int2(e, c0 | ((c1 - c0 - 1) << 24));
+    }
   }
 }
 
@@ -504,13 +593,21 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
   }
 }
 
-// X [T][H] fp32 -> bf16 (round to nearest even) in the operand K order
-// (kPerm8 inside each group of 8), the A operand of the tensor-core path.
+// y[i] = bf16(x[row(i)]) (round to nearest even) for the rows i of y, in the
+// operand K order (kPerm8 inside each group of 8): the token operand of the
+// tensor-core path. row(i) = i, or with ``perm`` the token of permutation
+// position i (pairs t*k + s, then the shared expert's rows t).
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y,
-                                                      size_t n8) {
+                                                      int rows, int K, const int32_t* __restrict__ perm, int T,
+                                                      int k) {
+  const int K8 = K / 8;
+  const size_t n8 = (size_t)rows * K8;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(x)[2 * i];
-    const float4 b = reinterpret_cast<const float4*>(x)[2 * i + 1];
+    const int r = (int)(i / K8), c = (int)(i % K8);
+    const int src = perm ? tc_pair_row(perm[r], T, k) : r;
+    const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)src * K) + 2 * c;
+    const float4 a = x4[0];
+    const float4 b = x4[1];
     // group (0..7) = a.x a.y a.z a.w b.x b.y b.z b.w -> order 0,4,1,5,2,6,3,7
     uint4 o;
     o.x = tc::pack_bf16x2(a.x, b.x);
@@ -521,11 +618,13 @@ __global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ 
   }
 }
 
-cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, size_t n, cudaStream_t st) {
-  const size_t n8 = n / 8;
+cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, int rows, int K, const int32_t* perm, int T, int k,
+                           cudaStream_t st) {
+  const size_t n8 = (size_t)rows * (K / 8);
   int blocks = (int)((n8 + 255) / 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
-  to_bf16_kernel<<<blocks, 256, 0, st>>>(x, y, n8);
+  if (blocks < 1) blocks = 1;
+  to_bf16_kernel<<<blocks, 256, 0, st>>>(x, y, rows, K, perm, T, k);
   return cudaGetLastError();
 }
 
@@ -541,19 +640,76 @@ int tc_num_sms() {
   return n;
 }
 
-int tc_max_mtiles(int T, int k, int E, int has_shared) {
+int tc_max_chunks(int T, int k, int E, int has_shared) {
   const int P = T * k;
-  return (P + (has_shared ? T : 0)) / TC_BM + E + 1;
+  return (P + (has_shared ? T : 0)) / TC_N + E + 1;
 }
 
-cudaError_t launch_build_mtiles(const int32_t* offsets, int E, int2* mtiles, int32_t* n_mtiles,
-                                cudaStream_t st) {
-  build_mtiles_kernel<<<1, 1024, sizeof(int32_t) * (E + 1), st>>>(offsets, E, mtiles, n_mtiles);
+cudaError_t launch_build_chunks(const int32_t* offsets, int E, int2* chunks, int32_t* n_chunks, cudaStream_t st) {
+  build_chunks_kernel<<<1, 1024, sizeof(int32_t) * (E + 1), st>>>(offsets, E, chunks, n_chunks);
   return cudaGetLastError();
 }
 
+// cuTensorMapEncodeTiled, taken from the driver through the runtime once.
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a packed matrix seen as bytes [rows][row_bytes], box = one
+// super-block column (``bytes``) x ``box_rows`` rows, no swizzle. Encoded maps
+// are kept in a small cache keyed by their arguments (a map is 128 bytes and
+// holds no device state).
+static bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t bytes,
+                        uint32_t box_rows) {
+  if (base == nullptr) {
+    memset(m, 0, sizeof(*m));
+    return true;
+  }
+  struct Entry {
+    const void* base;
+    uint64_t rows, row_bytes;
+    uint32_t bytes, box_rows;
+    CUtensorMap map;
+  };
+  static Entry cache[32];
+  static int n = 0, next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i) {
+    const Entry& c = cache[i];
+    if (c.base == base && c.rows == rows && c.row_bytes == row_bytes && c.bytes == bytes && c.box_rows == box_rows) {
+      *m = c.map;
+      return true;
+    }
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {bytes, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& c = cache[next];
+  c = Entry{base, rows, row_bytes, bytes, box_rows, *m};
+  next = (next + 1) % 32;
+  if (n < 32) ++n;
+  return true;
+}
+
 template <bool GATEUP, int QT>
-static cudaError_t tc_launch_t(const TcArgs& a, int max_items, cudaStream_t st) {
+static cudaError_t tc_launch_t(const TcArgs& a, const TcMaps& maps, int max_items, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(moe_tc_kernel<GATEUP, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -564,28 +720,78 @@ static cudaError_t tc_launch_t(const TcArgs& a, int max_items, cudaStream_t st) 
   int grid = tc_num_sms();
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
-  moe_tc_kernel<GATEUP, QT><<<grid, TC_THREADS, TcCfg<QT>::SMEM, st>>>(a);
+  moe_tc_kernel<GATEUP, QT><<<grid, TC_THREADS, TcCfg<QT>::SMEM, st>>>(a, maps);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st) {
+static TcArgs tc_args(const GroupedTcArgs& p) {
   TcArgs a{};
   a.W = p.W; a.W2 = p.W2; a.S = p.S; a.S2 = p.S2;
-  a.offsets = p.offsets; a.perm = p.perm; a.mtiles = p.mtiles; a.n_mtiles = p.n_mtiles;
-  a.X = p.X; a.xb = p.xb; a.hout = p.hout; a.a_rows = p.a_rows;
+  a.offsets = p.offsets; a.perm = p.perm; a.chunks = p.chunks; a.n_chunks = p.n_chunks;
+  a.xb = p.xb; a.hin = p.hin; a.hout = p.hout; a.yout = p.yout; a.yout_f32 = p.yout_f32;
   a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
-  const int items = p.max_mtiles * (p.F / 128);
-  return p.qt == QMOE_Q5K ? tc_launch_t<true, QMOE_Q5K>(a, items, st) : tc_launch_t<true, QMOE_Q4K>(a, items, st);
+  return a;
+}
+
+// Token matrix [rows][K] bf16 as boxes of 16 rows x 64 values, 128-byte swizzle.
+static bool encode_tokens(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+  struct Entry {
+    const void* base;
+    uint64_t rows, K;
+    CUtensorMap map;
+  };
+  static Entry cache[16];
+  static int n = 0, next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (cache[i].base == base && cache[i].rows == rows && cache[i].K == K) {
+      *m = cache[i].map;
+      return true;
+    }
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache[next] = Entry{base, rows, K, *m};
+  next = (next + 1) % 16;
+  if (n < 16) ++n;
+  return true;
+}
+
+cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st) {
+  const TcArgs a = tc_args(p);
+  const uint32_t bytes = (uint32_t)qtype_bytes(p.qt);
+  const uint64_t rb = (uint64_t)(p.H / QK) * bytes;
+  TcMaps m;
+  if (!encode_rows(&m.w, p.W, (uint64_t)p.E * p.F, rb, bytes, 128) ||
+      !encode_rows(&m.w2, p.W2, (uint64_t)p.E * p.F, rb, bytes, 128) ||
+      !encode_rows(&m.s, p.S, (uint64_t)p.F, rb, bytes, 128) || !encode_rows(&m.s2, p.S2, (uint64_t)p.F, rb, bytes, 128) ||
+      !encode_tokens(&m.tok, p.xb, (uint64_t)p.tok_rows, (uint64_t)p.H))
+    return cudaErrorInvalidValue;
+  const int items = p.max_chunks * (p.F / 128);
+  return p.qt == QMOE_Q5K ? tc_launch_t<true, QMOE_Q5K>(a, m, items, st) : tc_launch_t<true, QMOE_Q4K>(a, m, items, st);
 }
 
 cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
-  TcArgs a{};
-  a.W = p.W; a.S = p.S;
-  a.offsets = p.offsets; a.perm = p.perm; a.mtiles = p.mtiles; a.n_mtiles = p.n_mtiles;
-  a.hin = p.hin; a.yout = p.yout; a.yout_f32 = p.yout_f32; a.a_rows = p.a_rows;
-  a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
-  const int items = p.max_mtiles * (p.H / TC_BN);
-  return p.qt == QMOE_Q5K ? tc_launch_t<false, QMOE_Q5K>(a, items, st) : tc_launch_t<false, QMOE_Q4K>(a, items, st);
+  const TcArgs a = tc_args(p);
+  const uint32_t bytes = (uint32_t)qtype_bytes(p.qt);
+  const uint64_t rb = (uint64_t)(p.F / QK) * bytes;
+  TcMaps m;
+  if (!encode_rows(&m.w, p.W, (uint64_t)p.E * p.H, rb, bytes, 256) ||
+      !encode_rows(&m.s, p.S, (uint64_t)p.H, rb, bytes, 256) ||
+      !encode_tokens(&m.tok, p.hin, (uint64_t)p.tok_rows, (uint64_t)p.F))
+    return cudaErrorInvalidValue;
+  memset(&m.w2, 0, sizeof(m.w2));
+  memset(&m.s2, 0, sizeof(m.s2));
+  const int items = p.max_chunks * (p.H / 256);
+  return p.qt == QMOE_Q5K ? tc_launch_t<false, QMOE_Q5K>(a, m, items, st) : tc_launch_t<false, QMOE_Q4K>(a, m, items, st);
 }
 
 cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* w, const float* R, float* out, int T, int H,
