@@ -139,7 +139,9 @@ int qmoe_moe_forward(const qmoe_moe_desc *d, const float *X, const float *R,
                      void *ws, size_t ws_bytes, qmoe_stream_t stream);
 
 /* Path selection threshold: T above it takes the tensor-core path (built-in
- * value 64 rows). qmoe_set_gemm_threshold(-1) restores the built-in value. */
+ * value 4 rows: from 5 rows on, one pass over each expert's weights on the
+ * tensor cores beats the grouped GEMV). qmoe_set_gemm_threshold(-1) restores
+ * the built-in value. */
 int qmoe_get_gemm_threshold(void);
 void qmoe_set_gemm_threshold(int rows);
 int qmoe_last_path(void);

@@ -15,7 +15,7 @@ __device__ int g_status_word;
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_arch_ok[kMaxDevices];     // 0 unknown, 1 sm_103, -1 other
 std::atomic<int*> g_status_ptr[kMaxDevices];
-constexpr int kDefaultGemmThreshold = 64;
+constexpr int kDefaultGemmThreshold = 4;
 std::atomic<int> g_gemm_threshold{kDefaultGemmThreshold};
 constexpr int kDefaultDecodeRows = 4;
 std::atomic<int> g_decode_max_rows{kDefaultDecodeRows};
@@ -514,9 +514,12 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
                [&] { return launch_router_logits(X, d->Wr, part, T, H, E, L.nsplit, st); });
     if (e == cudaSuccess) {
       if (small) {
-        e = staged(QMOE_STAGE_ROUTE, 1, st, [&] {
-          return launch_route_small(part, L.nsplit, nullptr, T, E, k, has_shared, ws_ids, ws_w,
-                                    offsets, perm, active, n_active, status, st);
+        // top-k over many CTAs, then the permutation in one
+        e = staged(QMOE_STAGE_ROUTE, 2, st, [&] {
+          cudaError_t e2 = launch_topk(part, L.nsplit, T, E, k, ws_ids, ws_w, st);
+          if (e2 != cudaSuccess) return e2;
+          return launch_route_small(nullptr, 0, ws_ids, T, E, k, has_shared, ws_ids, ws_w, offsets, perm,
+                                    active, n_active, status, st);
         });
       } else {
         e = staged(QMOE_STAGE_ROUTE, 4, st, [&] {

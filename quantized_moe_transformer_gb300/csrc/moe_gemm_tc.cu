@@ -37,7 +37,8 @@
 //               shared-memory tile (one lane, 2-D tensor copies);
 //   warp 22     copies the packed weight rows into the super-block ring (one
 //               lane, 2-D tensor copies).
-// Four stages (A in TMEM, token tile in shared memory) decouple the roles.
+// Four A stages in TMEM and five or six token stages in shared memory, each
+// ring with its own full/empty barriers, decouple the roles.
 // Every wait is bounded: on time-out the CTA records QMOE_ERR_TIMEOUT, drains
 // its MMAs, frees its TMEM and returns.
 #include <cuda.h>
@@ -68,12 +69,16 @@ constexpr uint32_t TC_A_STAGE_COLS = 64;
 
 // Packed weights are staged per super-block: RS ring stages of 256 rows (A0
 // rows, then A1 rows), each filled by one or two 2-D tensor copies.
+// Token tiles have their own ring of TS stages (deeper than the TMEM A ring)
+// so that their loads run ahead of the MMAs instead of inside the A ring's
+// round trip.
 template <int QT>
 struct TcCfg {
   static constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
-  static constexpr int RS = QT == QMOE_Q5K ? 3 : 4;
+  static constexpr int RS = 3;
+  static constexpr int TS = QT == QMOE_Q5K ? 5 : 6;
   static constexpr int RAW_STAGE = 256 * BYTES;
-  static constexpr int SMEM = TC_STAGES * TC_B_BYTES + RS * RAW_STAGE + 4 * TC_EPI_BYTES + 1024 /*align*/ +
+  static constexpr int SMEM = TS * TC_B_BYTES + RS * RAW_STAGE + 4 * TC_EPI_BYTES + 1024 /*align*/ +
                               256 /*barriers*/;
 };
 
@@ -185,14 +190,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   uint8_t* smem = smem_raw + (((s0 + 1023u) & ~1023u) - s0);
   constexpr int S = TC_STAGES;
   using Cfg = TcCfg<QT>;
-  constexpr int RS = Cfg::RS, BYTES = Cfg::BYTES;
-  uint8_t* sB = smem;                                         // [S][TC_N][128 B] token tiles
-  uint8_t* sRaw = smem + S * TC_B_BYTES;                      // [RS][256][BYTES] packed rows
+  constexpr int RS = Cfg::RS, TS = Cfg::TS, BYTES = Cfg::BYTES;
+  uint8_t* sB = smem;                                         // [TS][TC_N][128 B] token tiles
+  uint8_t* sRaw = smem + TS * TC_B_BYTES;                     // [RS][256][BYTES] packed rows
   uint8_t* sEpi = sRaw + RS * Cfg::RAW_STAGE;                 // [4][TC_EPI_BYTES]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + 4 * TC_EPI_BYTES);
-  uint64_t* full = bars;                // [S]  A stage stored + token tile landed
+  uint64_t* full = bars;                // [S]  A stage stored
   uint64_t* empty = bars + S;           // [S]  MMAs of the stage done
-  uint64_t* raw_full = bars + 2 * S;    // [RS] packed rows landed
+  uint64_t* tok_full = bars + 2 * S;    // [TS] token tile landed
+  uint64_t* tok_empty = tok_full + TS;  // [TS] MMAs reading the token tile done
+  uint64_t* raw_full = tok_empty + TS;  // [RS] packed rows landed
   uint64_t* raw_empty = raw_full + RS;  // [RS] packed rows consumed
   uint64_t* acc_full = raw_empty + RS;  // [1]
   uint64_t* acc_empty = acc_full + 1;   // [1]
@@ -209,8 +216,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      tc::mbar_init(&full[i], TC_PRODUCER_WARPS + 1);  // + the token loader's arrive (with its bytes)
+      tc::mbar_init(&full[i], TC_PRODUCER_WARPS);
       tc::mbar_init(&empty[i], 2);  // one commit per MMA warp
+    }
+    for (int i = 0; i < TS; ++i) {
+      tc::mbar_init(&tok_full[i], 1);   // the token loader's arrive, with its bytes
+      tc::mbar_init(&tok_empty[i], 2);  // one commit per MMA warp
     }
     for (int i = 0; i < RS; ++i) {
       tc::mbar_init(&raw_full[i], 1);
@@ -318,15 +329,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     // ------------------------------------------------------------ producers
     // Warp 4 + pw covers TMEM lane quarter pw % 4 of matrix (pw / 4) % 2, and
     // sub-block s = pw / 8 of each k-tile's two: thread = one weight row, 32
-    // weights per k-tile. The dequantisation of the next k-tile overlaps the
-    // TMEM stores of the current one.
+    // weights per k-tile. A k-tile is stored and its stage released before
+    // the next one is dequantised, so that the stage round trip (MMA commit ->
+    // producers -> MMA) stays short.
     const int pw = warp - 4;
     const int mat = (pw >> 2) & 1, s = pw >> 3;
     const int r = 32 * (pw & 3) + lane;
     const uint32_t ta0 = tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * 32 + s * 16);
     const uint8_t* my_row = sRaw + (size_t)(mat * 128 + r) * BYTES;
     const int NU = n_mine * KB;
-    uint32_t wa[16], wb[16];
+    uint32_t wa[16];
     uint4 hdr = make_uint4(0, 0, 0, 0), hq0 = hdr, hq1 = hdr;
     // loads the super-block header (and Q5_K high bits) of ring slot u % RS
     auto open_sb = [&](int u) -> bool {
@@ -352,18 +364,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     for (int u = 0; u < NU && ok; ++u) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t* cur = (kk & 1) ? wb : wa;
-        uint32_t* nxt = (kk & 1) ? wa : wb;
         const int stage = kg % S;
         // warp-uniform outcome: the TMEM stores below are warp-collective
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], ((kg / S) & 1) ^ 1, abort_flag))) {
           ok = false;
           break;
         }
+        // store and release the stage first: this is the path the MMAs wait on
         tc::tc_fence_after();
-        tc::tmem_st16(ta0 + (uint32_t)stage * TC_A_STAGE_COLS, cur);
+        tc::tmem_st16(ta0 + (uint32_t)stage * TC_A_STAGE_COLS, wa);
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&full[stage]);
+        ++kg;
+        // then dequantise the next k-tile while the MMAs run
         if (kk < 3) {
-          deq(u, kk + 1, nxt);
+          deq(u, kk + 1, wa);
         } else {
           // every read of slot u is done: release it to the weight loader
           tc::fence_proxy_async_smem();
@@ -371,14 +388,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
           if (lane == 0) tc::mbar_arrive(&raw_empty[u % RS]);
           if (u + 1 < NU) {
             if (!open_sb(u + 1)) ok = false;
-            else deq(u + 1, 0, nxt);
+            else deq(u + 1, 0, wa);
           }
         }
-        tc::tmem_wait_st();
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&full[stage]);
-        ++kg;
         if (!ok) break;
       }
     }
@@ -444,15 +456,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         const int n16 = (ch.n + 15) >> 4;
         const int pos0 = g.offsets[ch.e] + ch.c0;
         for (int kt = 0; kt < KT; ++kt, ++kg) {
-          const int stage = kg % S;
-          if (!tc::mbar_wait(&empty[stage], ((kg / S) & 1) ^ 1, abort_flag)) {
+          const int stage = kg % TS;
+          if (!tc::mbar_wait(&tok_empty[stage], ((kg / TS) & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* b_st = sB + stage * TC_B_BYTES;
-          tc::mbar_expect_tx(&full[stage], (uint32_t)n16 * 16 * 128);
+          tc::mbar_expect_tx(&tok_full[stage], (uint32_t)n16 * 16 * 128);
           for (int i = 0; i < n16; ++i)
-            tma_load_2d(b_st + i * 2048, &maps.tok, kt * TC_BK, pos0 + 16 * i, &full[stage]);
+            tma_load_2d(b_st + i * 2048, &maps.tok, kt * TC_BK, pos0 + 16 * i, &tok_full[stage]);
         }
       }
     }
@@ -460,40 +472,45 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   } else if (warp == TC_MMA_WARP || warp == TC_MMA_WARP2) {
     // ------------------------------------------------------------ MMA issuers
     // Two warps, one per accumulator (D0 from A0, D1 from A1), each issuing
-    // from one lane and committing its own MMAs: a commit holds up the
+    // from its lane 0 and committing its own MMAs: a commit holds up the
     // issuing thread for a while, and the other warp's MMAs fill that gap.
+    // The other lanes wait at the end; operand descriptors are precomputed.
     const int which = warp == TC_MMA_WARP ? 0 : 1;
-    const uint32_t d_tmem = tmem + (uint32_t)which * TC_D1_COL;
-    int kg = 0;
-    int it = 0;
-    bool ok = true;
-    for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x, ++it) {
-      const Chunk ch = chunk_at(g.chunks, wi / NB);
-      const uint32_t idesc = tc::idesc_bf16_f32(128, (ch.n + 15) & ~15);
-      if (!tc::mbar_wait(acc_empty, (it & 1) ^ 1, abort_flag)) break;
-      tc::tc_fence_after();
-      for (int kt = 0; kt < KT; ++kt, ++kg) {
-        const int stage = kg % S;
-        if (!tc::mbar_wait(&full[stage], (kg / S) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+    if (lane == 0) {
+      const uint32_t d_tmem = tmem + (uint32_t)which * TC_D1_COL;
+      // descriptor of token stage 0; stage t starts t * TC_B_BYTES / 16 units later
+      const uint64_t bdesc0 = tc::sw128_desc(tc::smem_u32(sB));
+      int kg = 0;
+      int it = 0;
+      bool ok = true;
+      for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x, ++it) {
+        const Chunk ch = chunk_at(g.chunks, wi / NB);
+        const uint32_t idesc = tc::idesc_bf16_f32(128, (ch.n + 15) & ~15);
+        if (!tc::mbar_wait(acc_empty, (it & 1) ^ 1, abort_flag)) break;
         tc::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t b_addr = tc::smem_u32(sB + stage * TC_B_BYTES);
+        int stage = kg % S, ts = kg % TS;
+        for (int kt = 0; kt < KT; ++kt, ++kg) {
+          if (!tc::mbar_wait_spin(&tok_full[ts], (kg / TS) & 1, abort_flag) ||
+              !tc::mbar_wait_spin(&full[stage], (kg / S) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
           const uint32_t a = tmem + TC_A_COL + (uint32_t)stage * TC_A_STAGE_COLS + (uint32_t)which * 32;
+          // the descriptor's start address (16-byte units, low bits) advances by
+          // 32 bytes per K step of 16
+          const uint64_t bd = bdesc0 + (uint64_t)(ts * (TC_B_BYTES >> 4));
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk)
-            tc::mma_bf16_ts(d_tmem, a + 8 * kk, tc::sw128_desc(b_addr + 32 * kk), idesc, (kt | kk) != 0);
+            tc::mma_bf16_ts(d_tmem, a + 8 * kk, bd + 2 * kk, idesc, (kt | kk) != 0);
           tc::mma_commit(&empty[stage]);
+          tc::mma_commit(&tok_empty[ts]);
+          if (++stage == S) stage = 0;
+          if (++ts == TS) ts = 0;
         }
-        __syncwarp();
+        if (ok) tc::mma_commit(acc_full);
       }
-      if (ok && lane == 0) tc::mma_commit(acc_full);
-      __syncwarp();
-    }
-    // drain: every MMA this thread issued has completed before TMEM is freed
-    if (lane == 0) {
+      // drain: every MMA this thread issued has completed before TMEM is freed
       tc::mma_commit(&drain[which]);
       volatile int never = 0;
       tc::mbar_wait(&drain[which], 0, &never);

@@ -72,6 +72,99 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------
+// Router logits for large T: 128 rows x 128 experts per CTA, 256 threads,
+// each thread an 8 x 8 block (two 4-row by two 4-expert sub-blocks, so that
+// its shared-memory reads are 16-byte vectors without bank conflicts), K
+// staged in slices of 16 through double-buffered shared memory. Same H-split
+// partials as above: part[s][t][e].
+// ---------------------------------------------------------------------------
+constexpr int RG_BT = 128, RG_BE = 128, RG_BK = 16;
+
+__global__ void __launch_bounds__(256) router_gemm_kernel(const float* __restrict__ X, const float* __restrict__ Wr,
+                                                          float* __restrict__ part, int T, int H, int E,
+                                                          int h_per_split) {
+  __shared__ __align__(16) float xs[2][RG_BK][RG_BT + 4];  // X slice, transposed: [h][t]
+  __shared__ __align__(16) float ws[2][RG_BK][RG_BE];      // Wr slice: [h][e]
+  const int t0 = blockIdx.y * RG_BT, e0 = blockIdx.x * RG_BE;
+  const int hs0 = blockIdx.z * h_per_split;
+  const int tid = threadIdx.x;
+  const int ty = tid >> 4, tx = tid & 15;
+  // loader mapping: X 128 rows x 16 h = 512 float4 (2 per thread, along h);
+  // Wr 16 h x 128 e = 512 float4 (2 per thread, along e)
+  float4 xr[2], wr[2];
+  auto load = [&](int hk) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int q = tid + 256 * i;
+      const int r = q >> 2, c4 = (q & 3) * 4;  // row r, h offset c4
+      const int t = t0 + r;
+      xr[i] = t < T ? __ldg(reinterpret_cast<const float4*>(X + (size_t)t * H + hk + c4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const int hr = q >> 5, e4 = (q & 31) * 4;  // h row, expert offset
+      const int e = e0 + e4;
+      if ((E & 3) == 0 && e + 3 < E) {
+        wr[i] = __ldg(reinterpret_cast<const float4*>(Wr + (size_t)(hk + hr) * E + e));
+      } else {
+        const float* w = Wr + (size_t)(hk + hr) * E;
+        wr[i] = make_float4(e < E ? w[e] : 0.f, e + 1 < E ? w[e + 1] : 0.f, e + 2 < E ? w[e + 2] : 0.f,
+                            e + 3 < E ? w[e + 3] : 0.f);
+      }
+    }
+  };
+  auto store = [&](int b) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int q = tid + 256 * i;
+      const int r = q >> 2, c4 = (q & 3) * 4;
+      xs[b][c4 + 0][r] = xr[i].x;
+      xs[b][c4 + 1][r] = xr[i].y;
+      xs[b][c4 + 2][r] = xr[i].z;
+      xs[b][c4 + 3][r] = xr[i].w;
+      const int hr = q >> 5, e4 = (q & 31) * 4;
+      *reinterpret_cast<float4*>(&ws[b][hr][e4]) = wr[i];
+    }
+  };
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  const int nk = h_per_split / RG_BK;
+  load(hs0);
+  store(0);
+  __syncthreads();
+  for (int kb = 0; kb < nk; ++kb) {
+    const int b = kb & 1;
+    if (kb + 1 < nk) load(hs0 + (kb + 1) * RG_BK);
+#pragma unroll
+    for (int kk = 0; kk < RG_BK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&xs[b][kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&xs[b][kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&ws[b][kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&ws[b][kk][64 + tx * 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (kb + 1 < nk) store(b ^ 1);
+    __syncthreads();
+  }
+  float* dst = part + (size_t)blockIdx.z * T * E;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = e0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
+      if (e < E) dst[(size_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Top-k of one row by one warp. Lane l holds experts l, l+32, ...; each round
 // takes the largest remaining logit, the lower index on ties.
 // ---------------------------------------------------------------------------
@@ -351,18 +444,29 @@ __global__ void perm_scatter_kernel(const int32_t* __restrict__ ids, int P, int 
 // ---------------------------------------------------------------------------
 // Host-side launchers
 // ---------------------------------------------------------------------------
+// Rows from which the 128 x 128 register-tiled kernel is used.
+constexpr int kRouterGemmRows = 256;
+
 int router_splits(int T, int H, int E) {
-  // enough CTAs to spread the read of Wr at small T; one split at large T
-  int tiles = ((E + RL_BE - 1) / RL_BE) * ((T + RL_BT - 1) / RL_BT);
+  // enough CTAs to fill the GPU, at most 8 partials per logit (the top-k
+  // kernels add them up)
+  const bool big = T >= kRouterGemmRows;
+  const int bt = big ? RG_BT : RL_BT, be = big ? RG_BE : RL_BE, bk = big ? RG_BK : RL_BK;
+  const int tiles = ((E + be - 1) / be) * ((T + bt - 1) / bt);
   int s = 1;
-  while (tiles * s * 2 <= 256 && (H / (s * 2)) % RL_BK == 0 && H / (s * 2) >= 64) s *= 2;
+  while (s < 8 && tiles * s * 2 <= 304 && (H / (s * 2)) % bk == 0 && H / (s * 2) >= 128) s *= 2;
   return s;
 }
 
 cudaError_t launch_router_logits(const float* X, const float* Wr, float* part, int T, int H, int E,
                                  int nsplit, cudaStream_t st) {
-  dim3 grid((E + RL_BE - 1) / RL_BE, (T + RL_BT - 1) / RL_BT, nsplit);
-  router_logits_kernel<<<grid, 256, 0, st>>>(X, Wr, part, T, H, E, H / nsplit);
+  if (T >= kRouterGemmRows) {
+    dim3 grid((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT, nsplit);
+    router_gemm_kernel<<<grid, 256, 0, st>>>(X, Wr, part, T, H, E, H / nsplit);
+  } else {
+    dim3 grid((E + RL_BE - 1) / RL_BE, (T + RL_BT - 1) / RL_BT, nsplit);
+    router_logits_kernel<<<grid, 256, 0, st>>>(X, Wr, part, T, H, E, H / nsplit);
+  }
   return cudaGetLastError();
 }
 

@@ -81,15 +81,21 @@ def test_block_prefill_4096(oracle, blk_pair):
 
 def test_decode_after_prefill_matches_prefill(blk_pair):
     """Prefill 20 rows, then decode row 20 alone: equals row 20 of a 21-row
-    prefill (same kernels for the projections at these sizes)."""
+    prefill (the fp32 GEMV kernels for the projections and the MoE layer at
+    every size here, the threshold raised for the test)."""
     arr, blk = blk_pair
     X = torch.from_numpy(inputs.hidden(80, 21, 2048)).cuda()
-    k1, v1 = qb.cache_from_bits(arr["k_cache"]), qb.cache_from_bits(arr["v_cache"])
-    full = qb.block_forward(blk, X, k1, v1, 0)
-    k2, v2 = qb.cache_from_bits(arr["k_cache"]), qb.cache_from_bits(arr["v_cache"])
-    qb.block_forward(blk, X[:20].contiguous(), k2, v2, 0)
-    last = qb.block_forward(blk, X[20:].contiguous(), k2, v2, 20)
-    torch.cuda.synchronize()
+    old = qb.get_gemm_threshold()
+    qb.set_gemm_threshold(64)
+    try:
+        k1, v1 = qb.cache_from_bits(arr["k_cache"]), qb.cache_from_bits(arr["v_cache"])
+        full = qb.block_forward(blk, X, k1, v1, 0)
+        k2, v2 = qb.cache_from_bits(arr["k_cache"]), qb.cache_from_bits(arr["v_cache"])
+        qb.block_forward(blk, X[:20].contiguous(), k2, v2, 0)
+        last = qb.block_forward(blk, X[20:].contiguous(), k2, v2, 20)
+        torch.cuda.synchronize()
+    finally:
+        qb.set_gemm_threshold(old)
     assert_close(last.cpu().numpy(), full[20:].cpu().numpy(), TOL_GEMV)
 
 
@@ -109,8 +115,22 @@ def _slice_block(arr, r):
                     d(arr["Wv"][kv_rows]), d(arr["Wo"][:, 4 * r:4 * (r + 1)]), half)
 
 
+@pytest.fixture
+def fp32_path():
+    """The fp32 GEMV kernels at every size the test uses: the split invariant
+    is checked at the fp32 tolerance. (With random weights the block's
+    attention scores are large, so bf16 rounding of the K/V projections on the
+    tensor-core path moves the softmax by more than that; the tensor-core path
+    is checked against the oracle in test_block_ragged and
+    test_block_prefill_4096.)"""
+    old = qb.get_gemm_threshold()
+    qb.set_gemm_threshold(64)
+    yield
+    qb.set_gemm_threshold(old)
+
+
 @pytest.mark.parametrize("T,pos0", [(1, 4095), (8, 200)])
-def test_rank_partials_sum_to_block(oracle, blk_pair, T, pos0):
+def test_rank_partials_sum_to_block(oracle, blk_pair, fp32_path, T, pos0):
     arr, blk = blk_pair
     X = inputs.hidden(90 + T, T, 2048)
     Xd = torch.from_numpy(X).cuda()
