@@ -165,6 +165,88 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------------------
+// Router logits for moderate T: a CTA (256 threads) covers 8 experts x one
+// quarter of H x a block of RR_ROWS rows. Thread t keeps Wr rows h0 + t +
+// 256 j of the 8 experts in registers; the block's X slice is staged in
+// shared memory with all loads in flight at once; each warp's 8 partial sums
+// per row are reduced by recursive halving across the lanes (9 shuffles), the
+// 8 warps' through shared memory. part[q][t][e] for the 4 quarters q.
+// ---------------------------------------------------------------------------
+// rows per CTA: the staged X slice stays within 32 KB
+__host__ __device__ constexpr int rr_rows(int rpt) { return rpt >= 4 ? 8 : 16; }
+
+template <int RPT>
+__global__ void __launch_bounds__(256) router_rows_kernel(const float* __restrict__ X, const float* __restrict__ Wr,
+                                                          float* __restrict__ part, int T, int H, int E) {
+  constexpr int HQ = 256 * RPT;  // H / 4
+  constexpr int RR_ROWS = rr_rows(RPT);
+  __shared__ __align__(16) float xs[RR_ROWS][HQ];
+  __shared__ float red[RR_ROWS][8][8];  // [row][warp][expert]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int e0 = (blockIdx.x >> 2) * 8, hq = blockIdx.x & 3;
+  const int h0 = hq * HQ;
+  const int r0 = blockIdx.y * RR_ROWS;
+  const int nr = T - r0 < RR_ROWS ? T - r0 : RR_ROWS;
+  // X slice: nr rows x HQ floats, 16-byte loads
+  for (int i = tid; i < nr * (HQ / 4); i += 256) {
+    const int r = i / (HQ / 4), c = i % (HQ / 4);
+    reinterpret_cast<float4*>(&xs[r][0])[c] = __ldg(reinterpret_cast<const float4*>(X + (size_t)(r0 + r) * H + h0) + c);
+  }
+  float w[RPT][8];
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) {
+    const float4* src = reinterpret_cast<const float4*>(Wr + (size_t)(h0 + tid + 256 * j) * E + e0);
+    const float4 a = __ldg(src), b = __ldg(src + 1);
+    w[j][0] = a.x; w[j][1] = a.y; w[j][2] = a.z; w[j][3] = a.w;
+    w[j][4] = b.x; w[j][5] = b.y; w[j][6] = b.z; w[j][7] = b.w;
+  }
+  __syncthreads();
+  const int q_mine = (lane >> 2) & 7;  // expert this lane ends up holding
+  for (int r = 0; r < nr; ++r) {
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const float x = xs[r][tid + 256 * j];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = fmaf(x, w[j][q], v[q]);
+    }
+    // recursive halving: after the xor-16, -8 and -4 steps lane l holds the
+    // 4-lane partial of expert (l >> 2) & 7, then two more steps sum those
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool hi = lane & 16;
+      const float send = hi ? v[i] : v[i + 4];
+      const float keep = hi ? v[i + 4] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const bool hi = lane & 8;
+      const float send = hi ? v[i] : v[i + 2];
+      const float keep = hi ? v[i + 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    {
+      const bool hi = lane & 4;
+      const float send = hi ? v[0] : v[1];
+      const float keep = hi ? v[1] : v[0];
+      v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    if ((lane & 3) == 0) red[r][warp][q_mine] = v[0];
+  }
+  __syncthreads();
+  if (tid < nr * 8) {
+    const int r = tid >> 3, q = tid & 7;
+    float s2 = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) s2 += red[r][w8][q];
+    part[((size_t)hq * T + r0 + r) * E + e0 + q] = s2;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Top-k of one row by one warp. Lane l holds experts l, l+32, ...; each round
 // takes the largest remaining logit, the lower index on ties.
 // ---------------------------------------------------------------------------
@@ -179,15 +261,15 @@ __device__ __forceinline__ void warp_topk_row(const float* part, int nsplit, int
     const int e = lane + 32 * j;
     float s = 0.f;
     if (e < E) {
-      // the split partials are loaded 16 at a time (independent loads in
+      // the split partials are loaded 8 at a time (independent loads in
       // flight) and added in split order
-      for (int s0 = 0; s0 < nsplit; s0 += 16) {
-        float pv[16];
+      for (int s0 = 0; s0 < nsplit; s0 += 8) {
+        float pv[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
+        for (int q = 0; q < 8; ++q)
           pv[q] = (s0 + q < nsplit) ? __ldcg(part + ((size_t)(s0 + q) * T + t) * E + e) : 0.f;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) s += pv[q];
+        for (int q = 0; q < 8; ++q) s += pv[q];
       }
     }
     v[j] = (e < E) ? s : -INFINITY;
@@ -235,10 +317,10 @@ __device__ __forceinline__ void warp_topk_row(const float* part, int nsplit, int
 }
 
 template <int EPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int nsplit,
+__global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ part, int nsplit,
                                                    int T, int E, int k, int32_t* __restrict__ ids,
                                                    float* __restrict__ w) {
-  int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  int t = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (t >= T) return;
   warp_topk_row<EPL>(part, nsplit, T, E, k, t, ids, w, nullptr);
 }
@@ -447,7 +529,12 @@ __global__ void perm_scatter_kernel(const int32_t* __restrict__ ids, int P, int 
 // Rows from which the 128 x 128 register-tiled kernel is used.
 constexpr int kRouterGemmRows = 256;
 
+static bool rows_kernel_fits(int T, int H, int E) {
+  return T < kRouterGemmRows && E % 8 == 0 && (H == 1024 || H == 2048 || H == 4096);
+}
+
 int router_splits(int T, int H, int E) {
+  if (rows_kernel_fits(T, H, E)) return 4;  // one partial per quarter of H
   // enough CTAs to fill the GPU, at most 8 partials per logit (the top-k
   // kernels add them up)
   const bool big = T >= kRouterGemmRows;
@@ -460,7 +547,13 @@ int router_splits(int T, int H, int E) {
 
 cudaError_t launch_router_logits(const float* X, const float* Wr, float* part, int T, int H, int E,
                                  int nsplit, cudaStream_t st) {
-  if (T >= kRouterGemmRows) {
+  if (rows_kernel_fits(T, H, E) && nsplit == 4) {
+    const int rpt = H / 1024;
+    const dim3 grid((E / 8) * 4, (T + rr_rows(rpt) - 1) / rr_rows(rpt));
+    if (H == 1024) router_rows_kernel<1><<<grid, 256, 0, st>>>(X, Wr, part, T, H, E);
+    else if (H == 2048) router_rows_kernel<2><<<grid, 256, 0, st>>>(X, Wr, part, T, H, E);
+    else router_rows_kernel<4><<<grid, 256, 0, st>>>(X, Wr, part, T, H, E);
+  } else if (T >= kRouterGemmRows) {
     dim3 grid((E + RG_BE - 1) / RG_BE, (T + RG_BT - 1) / RG_BT, nsplit);
     router_gemm_kernel<<<grid, 256, 0, st>>>(X, Wr, part, T, H, E, H / nsplit);
   } else {
@@ -473,7 +566,7 @@ cudaError_t launch_router_logits(const float* X, const float* Wr, float* part, i
 template <int EPL>
 static cudaError_t topk_dispatch(const float* part, int nsplit, int T, int E, int k, int32_t* ids,
                                  float* w, cudaStream_t st) {
-  topk_kernel<EPL><<<(T + 7) / 8, 256, 0, st>>>(part, nsplit, T, E, k, ids, w);
+  topk_kernel<EPL><<<(T + 3) / 4, 128, 0, st>>>(part, nsplit, T, E, k, ids, w);
   return cudaGetLastError();
 }
 
