@@ -70,6 +70,10 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=str, default=None, help=argparse.SUPPRESS)
+    p.add_argument("--record-traffic", type=str, default=None, metavar="CSV",
+                   help="read an ncu --csv log with dram__bytes_read.sum / dram__bytes_write.sum of this "
+                        "workload's kernels and store the dominant kernel's DRAM bytes per launch in "
+                        "profiles/ncu_traffic.json (no GPU work)")
     return p.parse_args()
 
 
@@ -479,8 +483,54 @@ def ours_main(args, rank, world, local_rank):
         print(json.dumps(line))
 
 
+# kernels whose DRAM bytes make up the dominant unit of each path: the decode
+# path's chained kernels per step, the grouped gate/up kernel otherwise
+TRAFFIC_KERNELS = {
+    "decode": ("decode_router_kernel", ("decode_router_kernel", "decode_route_kernel", "decode_gateup_kernel",
+                                        "decode_down_kernel")),
+    "gemm_tc": ("moe_tc_kernel<1,", ("moe_tc_kernel<1,",)),
+    "gemv": ("gateup_gemv_kernel", ("gateup_gemv_kernel",)),
+}
+
+
+def record_traffic(args):
+    """profiles/ncu_traffic.json["path:workload"] = DRAM bytes per dominant
+    launch (per step for the decode chain), from an ncu CSV log."""
+    import csv
+    path = "decode" if WORKLOADS[args.workload].get("T", 1) <= 4 else "gemm_tc"
+    first, names = TRAFFIC_KERNELS[path]
+    per_launch = {}
+    with open(args.record_traffic) as f:
+        rows = [r for r in csv.reader(f) if len(r) > 5]
+    hdr = rows[0]
+    ki, mi, vi, ii = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value"), hdr.index("ID")
+    for r in rows[1:]:
+        name = r[ki].replace(" ", "")
+        if not any(n.replace(" ", "") in name for n in names):
+            continue
+        if r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        d = per_launch.setdefault(r[ii], {"name": name, "bytes": 0.0})
+        d["bytes"] += float(r[vi].replace(",", ""))
+    units = sum(1 for d in per_launch.values() if first.replace(" ", "") in d["name"])
+    total = sum(d["bytes"] for d in per_launch.values())
+    if units == 0:
+        raise SystemExit(f"no {first} launch in {args.record_traffic}")
+    tf = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    data = json.load(open(tf)) if os.path.exists(tf) else {}
+    data[f"{path}:{args.workload}"] = {"dram_bytes_per_launch": total / units, "launches": units,
+                                       "source_sha": source_sha(KERNEL_SOURCES[path]),
+                                       "kernels": sorted({d["name"][:60] for d in per_launch.values()})}
+    with open(tf, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+    print(json.dumps(data[f"{path}:{args.workload}"]))
+
+
 def main():
     args = parse()
+    if args.record_traffic:
+        record_traffic(args)
+        return
     if args.cpu_sample:
         cpu_sample_main(args.cpu_sample)
         return
