@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     }
     for (int i = 0; i < TS; ++i) {
       tc::mbar_init(&tok_full[i], 1);   // the token loader's arrive, with its bytes
-      tc::mbar_init(&tok_empty[i], 2);  // one commit per MMA warp
+      tc::mbar_init(&tok_empty[i], 1);  // forwarded by producer warp 4, see below
     }
     for (int i = 0; i < RS; ++i) {
       tc::mbar_init(&raw_full[i], 1);
@@ -370,6 +370,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
           ok = false;
           break;
         }
+        // The empty phase just seen certifies that the MMAs of k-tile kg - S
+        // have completed: warp 4 forwards that to the token ring, which saves
+        // the MMA warps a second commit per k-tile.
+        if (pw == 0 && lane == 0 && kg >= S) tc::mbar_arrive(&tok_empty[(kg - S) % TS]);
         // store and release the stage first: this is the path the MMAs wait on
         tc::tc_fence_after();
         tc::tmem_st16(ta0 + (uint32_t)stage * TC_A_STAGE_COLS, wa);
@@ -504,7 +508,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
           for (int kk = 0; kk < TC_BK / 16; ++kk)
             tc::mma_bf16_ts(d_tmem, a + 8 * kk, bd + 2 * kk, idesc, (kt | kk) != 0);
           tc::mma_commit(&empty[stage]);
-          tc::mma_commit(&tok_empty[ts]);
           if (++stage == S) stage = 0;
           if (++ts == TS) ts = 0;
         }

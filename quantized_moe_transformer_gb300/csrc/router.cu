@@ -449,13 +449,19 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
                                                          int32_t* __restrict__ n_active) {
   extern __shared__ int32_t tot[];  // [E+1]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // per expert: exclusive running sum over chunks (in place), total
+  // per expert: exclusive running sum over chunks (in place), total; the
+  // counts are read 8 chunks at a time so that the loads overlap
   for (int e = tid; e < E; e += blockDim.x) {
     int run = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      int v = chunk_cnt[(size_t)c * E + e];
-      chunk_cnt[(size_t)c * E + e] = run;
-      run += v;
+    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = c0 + i < n_chunks ? chunk_cnt[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (c0 + i < n_chunks) chunk_cnt[(size_t)(c0 + i) * E + e] = run;
+        run += v[i];
+      }
     }
     tot[e] = run;
   }
@@ -491,7 +497,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   }
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) {
-    int base = offsets[e];
+    const int base = offsets[e];
+#pragma unroll 8
     for (int c = 0; c < n_chunks; ++c) chunk_cnt[(size_t)c * E + e] += base;
   }
   const int P = T * k;
