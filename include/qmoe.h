@@ -158,9 +158,10 @@ void qmoe_set_decode_max_rows(int rows);
  * Byte offsets of the intermediates inside a moe_forward workspace, for
  * stagewise checks: ids [T][k] int32, w [T][k] fp32, offsets [E+2] int32
  * (row ranges per expert, the shared expert last), perm [T*k + T] int32 (pair
- * index t*k+s grouped by expert, stable), y [T*k + T][H] (per pair, shared
- * rows last; fp32 on the GEMV path, bf16 on the tensor-core path). Valid after
- * the forward has completed.
+ * index t*k+s grouped by expert, stable), y [T*k + T][H] (fp32 per pair,
+ * shared rows last, on the GEMV path; bf16 in permutation order, row i for
+ * pair perm[i], on the tensor-core path). Valid after the forward has
+ * completed.
  */
 typedef struct {
   size_t ids, w, offsets, perm, y;

@@ -87,7 +87,7 @@ inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace carve-up (every piece 256-byte aligned).
 struct MoeWs {
-  size_t part, ids, w, route, offsets, perm, active, n_active, chunk, chunks, n_chunks, xb, h, y, total;
+  size_t part, ids, w, route, offsets, perm, inv, active, n_active, chunk, chunks, n_chunks, xb, h, y, total;
   int nsplit;
 };
 
@@ -103,6 +103,7 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   L.route = o;    o += up256(sizeof(int32_t) * (P + 1));
   L.offsets = o;  o += up256(sizeof(int32_t) * (E + 2));
   L.perm = o;     o += up256(sizeof(int32_t) * rows);
+  L.inv = o;      o += up256(sizeof(int32_t) * rows);
   L.active = o;   o += up256(sizeof(int32_t) * (E + 1));
   L.n_active = o; o += 256;
   L.chunk = o;    o += up256(sizeof(int32_t) * (size_t)perm_chunks((int)P) * E);
@@ -203,7 +204,7 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
     int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
     __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
     if ((e = launch_build_chunks(offsets, 1, chunks, n_chunks, st)) != cudaSuccess) return e;
-    if ((e = launch_to_bf16(x, xb, T, K, nullptr, T, 1, st)) != cudaSuccess) return e;
+    if ((e = launch_to_bf16(x, xb, T, K, nullptr, T, 1, nullptr, st)) != cudaSuccess) return e;
     GroupedTcArgs p{};
     p.W = static_cast<const uint8_t*>(W);
     p.qt = qt;
@@ -467,6 +468,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
   float* ws_w = reinterpret_cast<float*>(base + L.w);
   int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
   int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+  int32_t* inv = reinterpret_cast<int32_t*>(base + L.inv);
   int32_t* active = reinterpret_cast<int32_t*>(base + L.active);
   int32_t* n_active = reinterpret_cast<int32_t*>(base + L.n_active);
   int32_t* chunk = reinterpret_cast<int32_t*>(base + L.chunk);
@@ -555,7 +557,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     e = staged(QMOE_STAGE_ROUTE, 2, st, [&] {
       cudaError_t e2 = launch_build_chunks(offsets, E, chunks, n_chunks, st);
       if (e2 != cudaSuccess) return e2;
-      return launch_to_bf16(X, xb, (int)(P + (has_shared ? T : 0)), H, perm, T, k, st);
+      return launch_to_bf16(X, xb, (int)(P + (has_shared ? T : 0)), H, perm, T, k, inv, st);
     });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
     GroupedTcArgs p{};
@@ -591,7 +593,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     e = staged(QMOE_STAGE_DOWN, 1, st, [&] { return launch_down_tc(p, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
     e = staged(QMOE_STAGE_COMBINE, 1, st,
-               [&] { return launch_combine_bf16(y16, w_use, R, out, T, H, k, has_shared, st); });
+               [&] { return launch_combine_bf16(y16, inv, w_use, R, out, T, H, k, has_shared, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
     g_last_path = QMOE_PATH_GEMM_TC;
     return QMOE_OK;

@@ -63,9 +63,9 @@ cudaError_t launch_build_chunks(const int32_t* offsets, int E, int2* chunks, int
 cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st);
 cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st);
 cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, int rows, int K, const int32_t* perm, int T, int k,
-                           cudaStream_t st);
-cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* w, const float* R, float* out,
-                                int T, int H, int k, int has_shared, cudaStream_t st);
+                           int32_t* inv, cudaStream_t st);
+cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const int32_t* inv, const float* w, const float* R,
+                                float* out, int T, int H, int k, int has_shared, cudaStream_t st);
 
 // block.cu: the attention + MoE block's other kernels.
 cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, float* y, int T, int H, cudaStream_t st);

@@ -94,7 +94,7 @@ struct TcArgs {
   const __nv_bfloat16* xb;      // gate/up token source, [P+T][H] bf16: X rows in permutation order
   const __nv_bfloat16* hin;     // down token source, [P+T][F] bf16
   __nv_bfloat16* hout;          // gate/up output, [P+T][F] bf16
-  __nv_bfloat16* yout;          // down output, [P+T][H] bf16
+  __nv_bfloat16* yout;          // down output, [P+T][H] bf16, rows in permutation order
   float* yout_f32;              // down output in fp32 instead, when not null
   int T, k, E, H, F;
   int* status;
@@ -171,10 +171,6 @@ __device__ __forceinline__ void dequant_sub(const uint4 hdr, const uint4 qv, uin
       o[4 * n + i] = *reinterpret_cast<uint32_t*>(&v);
     }
   }
-}
-
-__device__ __forceinline__ int pick_row(const int (&p)[4], int i) {
-  return i == 0 ? p[0] : (i == 1 ? p[1] : (i == 2 ? p[2] : p[3]));
 }
 
 __device__ __forceinline__ uint32_t pick_word(const uint4 v, int i) {
@@ -256,13 +252,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       const Chunk ch = chunk_at(g.chunks, wi / NB);
       const int blk = wi % NB;
       const int pos0 = g.offsets[ch.e] + ch.c0;
-      // down: destination rows of the chunk's tokens, lane l holding tokens l + 32q
-      int prow[4] = {0, 0, 0, 0};
-      if (!GATEUP) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (lane + 32 * q < ch.n) prow[q] = g.perm[pos0 + lane + 32 * q];
-      }
 #pragma unroll 1
       for (int c = 0; c < ch.n; c += 16) {
         uint32_t a[16], b[16];
@@ -297,9 +286,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
               for (int q = 0; q < 4; ++q) {
                 const int id = lane + 32 * q, i = id >> 3, part = id & 7;
                 const int t = c + i;
-                const int row = __shfl_sync(0xffffffffu, pick_row(prow, c >> 5), t & 31);
                 if (t < ch.n)
-                  *reinterpret_cast<uint4*>(g.yout_f32 + (size_t)row * g.H + col0 + 4 * part) =
+                  *reinterpret_cast<uint4*>(g.yout_f32 + (size_t)(pos0 + t) * g.H + col0 + 4 * part) =
                       reinterpret_cast<const uint4*>(stg)[id];
               }
             } else {
@@ -311,9 +299,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
               for (int q = 0; q < 2; ++q) {
                 const int id = lane + 32 * q, i = id >> 2, part = id & 3;
                 const int t = c + i;
-                const int row = __shfl_sync(0xffffffffu, pick_row(prow, c >> 5), t & 31);
                 if (t < ch.n)
-                  *reinterpret_cast<uint4*>(g.yout + (size_t)row * g.H + col0 + 8 * part) =
+                  *reinterpret_cast<uint4*>(g.yout + (size_t)(pos0 + t) * g.H + col0 + 8 * part) =
                       reinterpret_cast<const uint4*>(stg)[id];
               }
             }
@@ -567,8 +554,10 @@ __global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __res
   }
 }
 
-// out_t = R_t + y_shared,t + sum_s w_{t,s} y_{t,s} with bf16 y, in slot order.
+// out_t = R_t + y_shared,t + sum_s w_{t,s} y_{t,s} with bf16 y, in slot order;
+// y's rows are in permutation order, inv[pair] is the row of a pair.
 __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* __restrict__ y,
+                                                           const int32_t* __restrict__ inv,
                                                            const float* __restrict__ w, const float* R,
                                                            float* out, int T, int H, int k,
                                                            int has_shared) {
@@ -587,7 +576,7 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
       for (int j = 0; j < 8; ++j) acc[j] = 0.f;
     }
     if (has_shared) {
-      uint4 v = reinterpret_cast<const uint4*>(y + ((size_t)T * k + t) * H)[c];
+      uint4 v = reinterpret_cast<const uint4*>(y + (size_t)inv[T * k + t] * H)[c];
       const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -598,7 +587,7 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
     }
     for (int s = 0; s < k; ++s) {
       const float ws = w[(size_t)t * k + s];
-      uint4 v = reinterpret_cast<const uint4*>(y + ((size_t)t * k + s) * H)[c];
+      uint4 v = reinterpret_cast<const uint4*>(y + (size_t)inv[t * k + s] * H)[c];
       const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -616,15 +605,18 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
 // y[i] = bf16(x[row(i)]) (round to nearest even) for the rows i of y, in the
 // operand K order (kPerm8 inside each group of 8): the token operand of the
 // tensor-core path. row(i) = i, or with ``perm`` the token of permutation
-// position i (pairs t*k + s, then the shared expert's rows t).
+// position i (pairs t*k + s, then the shared expert's rows t); then also
+// inv[perm[i]] = i, the position of each pair.
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y,
                                                       int rows, int K, const int32_t* __restrict__ perm, int T,
-                                                      int k) {
+                                                      int k, int32_t* __restrict__ inv) {
   const int K8 = K / 8;
   const size_t n8 = (size_t)rows * K8;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const int r = (int)(i / K8), c = (int)(i % K8);
-    const int src = perm ? tc_pair_row(perm[r], T, k) : r;
+    const int pr = perm ? perm[r] : r;
+    const int src = perm ? tc_pair_row(pr, T, k) : r;
+    if (inv != nullptr && c == 0) inv[pr] = r;
     const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)src * K) + 2 * c;
     const float4 a = x4[0];
     const float4 b = x4[1];
@@ -639,12 +631,12 @@ __global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ 
 }
 
 cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, int rows, int K, const int32_t* perm, int T, int k,
-                           cudaStream_t st) {
+                           int32_t* inv, cudaStream_t st) {
   const size_t n8 = (size_t)rows * (K / 8);
   int blocks = (int)((n8 + 255) / 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
   if (blocks < 1) blocks = 1;
-  to_bf16_kernel<<<blocks, 256, 0, st>>>(x, y, rows, K, perm, T, k);
+  to_bf16_kernel<<<blocks, 256, 0, st>>>(x, y, rows, K, perm, T, k, inv);
   return cudaGetLastError();
 }
 
@@ -814,12 +806,12 @@ cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
   return p.qt == QMOE_Q5K ? tc_launch_t<false, QMOE_Q5K>(a, m, items, st) : tc_launch_t<false, QMOE_Q4K>(a, m, items, st);
 }
 
-cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const float* w, const float* R, float* out, int T, int H,
-                                int k, int has_shared, cudaStream_t st) {
+cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const int32_t* inv, const float* w, const float* R, float* out,
+                                int T, int H, int k, int has_shared, cudaStream_t st) {
   const size_t n = (size_t)T * (H / 8);
   int blocks = (int)((n + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
-  combine_bf16_kernel<<<blocks, 256, 0, st>>>(y, w, R, out, T, H, k, has_shared);
+  combine_bf16_kernel<<<blocks, 256, 0, st>>>(y, inv, w, R, out, T, H, k, has_shared);
   return cudaGetLastError();
 }
 
