@@ -196,141 +196,6 @@ __global__ void attn_merge_kernel(const float* __restrict__ part, float* __restr
   }
 }
 
-// ---------------------------------------------------------------------------
-// Causal attention for many query rows: CTA (64-row q tile, head) walks 64-key
-// tiles with an online softmax. fp32 SIMT; K and V come from the bf16 caches.
-// ---------------------------------------------------------------------------
-constexpr int PF_BQ = 64, PF_BK = 64, PF_HD = 128;
-
-__global__ void __launch_bounds__(256) attn_prefill_kernel(const float* __restrict__ q,
-                                                           const __nv_bfloat16* __restrict__ kc,
-                                                           const __nv_bfloat16* __restrict__ vc,
-                                                           float* __restrict__ o, int T, int pos0, int nh, int nkv) {
-  extern __shared__ float sm[];
-  float* Qs = sm;                          // [64][128]
-  float* Ks = Qs + PF_BQ * PF_HD;          // [64][129]
-  float* Vs = Ks + PF_BK * (PF_HD + 1);    // [64][128]
-  float* Ps = Vs + PF_BK * PF_HD;          // [64][65]
-  float* mrow = Ps + PF_BQ * (PF_BK + 1);  // [64]
-  float* lrow = mrow + PF_BQ;              // [64]
-  float* arow = lrow + PF_BQ;              // [64]
-  const int tid = threadIdx.x;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // heavy (late) tiles first
-  const int h = blockIdx.y, g = h / (nh / nkv);
-  const int t0 = qt * PF_BQ;
-  const float scale = rsqrtf((float)PF_HD);
-  for (int i = tid; i < PF_BQ * PF_HD; i += 256) {
-    const int r = i / PF_HD, d = i % PF_HD;
-    const int t = t0 + r;
-    Qs[i] = t < T ? q[((size_t)t * nh + h) * PF_HD + d] * scale : 0.f;
-  }
-  if (tid < PF_BQ) {
-    mrow[tid] = -INFINITY;
-    lrow[tid] = 0.f;
-  }
-  const int ro = tid >> 2, co = (tid & 3) * 32;  // output row and 32 columns of this thread
-  float acc[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-  const int last_row = min(T - 1, t0 + PF_BQ - 1);
-  const int kend = pos0 + last_row + 1;  // keys [0, kend)
-  const int tr = tid >> 4, tc = tid & 15;  // S block: rows tr*4.., keys tc*4..
-  for (int k0 = 0; k0 < kend; k0 += PF_BK) {
-    __syncthreads();
-    for (int i = tid; i < PF_BK * PF_HD / 8; i += 256) {
-      const int r = i / (PF_HD / 8), c8 = i % (PF_HD / 8);
-      const int j = k0 + r;
-      float kv[8], vv[8];
-      if (j < kend) {
-        const uint4 ku = __ldg(reinterpret_cast<const uint4*>(kc + ((size_t)j * nkv + g) * PF_HD) + c8);
-        const uint4 vu = __ldg(reinterpret_cast<const uint4*>(vc + ((size_t)j * nkv + g) * PF_HD) + c8);
-        const __nv_bfloat162* kb = reinterpret_cast<const __nv_bfloat162*>(&ku);
-        const __nv_bfloat162* vb = reinterpret_cast<const __nv_bfloat162*>(&vu);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float2 a = __bfloat1622float2(kb[m]), b = __bfloat1622float2(vb[m]);
-          kv[2 * m] = a.x;
-          kv[2 * m + 1] = a.y;
-          vv[2 * m] = b.x;
-          vv[2 * m + 1] = b.y;
-        }
-      } else {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) kv[m] = vv[m] = 0.f;
-      }
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        Ks[r * (PF_HD + 1) + 8 * c8 + m] = kv[m];
-        Vs[r * PF_HD + 8 * c8 + m] = vv[m];
-      }
-    }
-    __syncthreads();
-    // S = Q K^T for a 4x4 block
-    float s[4][4] = {};
-    for (int d = 0; d < PF_HD; ++d) {
-      float qa[4], kb[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        qa[i] = Qs[(tr * 4 + i) * PF_HD + d];
-        kb[i] = Ks[(tc * 4 + i) * (PF_HD + 1) + d];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qa[i], kb[j], s[i][j]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = tr * 4 + i, key = k0 + tc * 4 + j;
-        const bool ok = (t0 + r < T) && (key <= pos0 + t0 + r) && (key < kend);
-        Ps[r * (PF_BK + 1) + tc * 4 + j] = ok ? s[i][j] : -INFINITY;
-      }
-    __syncthreads();
-    if (tid < PF_BQ) {
-      const int r = tid;
-      float mx = mrow[r];
-      for (int j = 0; j < PF_BK; ++j) mx = fmaxf(mx, Ps[r * (PF_BK + 1) + j]);
-      const float alpha = (mrow[r] == -INFINITY) ? 0.f : __expf(mrow[r] - mx);
-      float lsum = 0.f;
-      for (int j = 0; j < PF_BK; ++j) {
-        const float sv = Ps[r * (PF_BK + 1) + j];
-        const float p = (sv == -INFINITY) ? 0.f : __expf(sv - mx);
-        Ps[r * (PF_BK + 1) + j] = p;
-        lsum += p;
-      }
-      lrow[r] = lrow[r] * alpha + lsum;
-      mrow[r] = mx;
-      arow[r] = alpha;
-    }
-    __syncthreads();
-    const float al = arow[ro];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] *= al;
-    for (int j = 0; j < PF_BK; ++j) {
-      const float p = Ps[ro * (PF_BK + 1) + j];
-      const float4* v4 = reinterpret_cast<const float4*>(Vs + j * PF_HD + co);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 v = v4[i];
-        acc[4 * i] = fmaf(p, v.x, acc[4 * i]);
-        acc[4 * i + 1] = fmaf(p, v.y, acc[4 * i + 1]);
-        acc[4 * i + 2] = fmaf(p, v.z, acc[4 * i + 2]);
-        acc[4 * i + 3] = fmaf(p, v.w, acc[4 * i + 3]);
-      }
-    }
-  }
-  __syncthreads();
-  const int t = t0 + ro;
-  if (t < T) {
-    const float inv = 1.f / lrow[ro];
-    float* dst = o + ((size_t)t * nh + h) * PF_HD + co;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) dst[i] = acc[i] * inv;
-  }
-}
-
 __global__ void add_kernel(const float* __restrict__ a, const float* __restrict__ b, float* __restrict__ y, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     y[i] = a[i] + b[i];
@@ -371,17 +236,8 @@ cudaError_t launch_attention(const float* q, const __nv_bfloat16* kc, const __nv
     attn_merge_kernel<<<T * nh, 128, 0, st>>>(part, o, nc, hd);
     return cudaGetLastError();
   }
-  if (hd != PF_HD) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(float) * (PF_BQ * PF_HD + PF_BK * (PF_HD + 1) + PF_BK * PF_HD + PF_BQ * (PF_BK + 1) +
-                                       3 * PF_BQ);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  attn_prefill_kernel<<<dim3((T + PF_BQ - 1) / PF_BQ, nh), 256, smem, st>>>(q, kc, vc, o, T, pos0, nh, nkv);
-  return cudaGetLastError();
+  if (hd != 128) return cudaErrorInvalidValue;
+  return launch_attention_prefill(q, kc, vc, o, T, pos0, nh, nkv, st);
 }
 
 cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaStream_t st) {

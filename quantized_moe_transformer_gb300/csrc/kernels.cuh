@@ -78,6 +78,10 @@ cudaError_t launch_attention(const float* q, const __nv_bfloat16* kc, const __nv
                              int T, int pos0, int nh, int nkv, int hd, bool chunked, cudaStream_t st);
 cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaStream_t st);
 
+// attn_prefill.cu: causal attention for many query rows (head_dim 128), bf16 mma.sync.
+cudaError_t launch_attention_prefill(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
+                                     int T, int pos0, int nh, int nkv, cudaStream_t st);
+
 // moe_decode.cu: three PDL-chained kernels for T <= 4.
 struct DecodeLaunch {
   const float* X;
