@@ -188,32 +188,42 @@ int check_block(const qmoe_block_desc* b) {
   return QMOE_OK;
 }
 
-// y [T][N] fp32 = x [T][K] fp32 . W^T for a packed Q4_K/Q5_K matrix W [N][K/256]:
-// the grouped kernels with one "expert" holding all rows.
-cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int N, float* y, char* base,
-                       const AttnWs& L, int* status, cudaStream_t st) {
+// y [T][N] fp32 = x [T][K] fp32 . W^T for packed Q4_K/Q5_K matrices W [N][K/256]:
+// the grouped kernels with one "expert" holding all rows. dense_prep sets up
+// the routing of that expert (and, on the tensor-core path, the chunk list and
+// the bf16 copy of x) once for every projection of the same x.
+bool dense_uses_tc(int T) { return T > g_gemm_threshold.load(); }
+
+cudaError_t dense_prep(const float* x, int T, int K, char* base, const AttnWs& L, cudaStream_t st) {
   int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
   int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
   int32_t* active = reinterpret_cast<int32_t*>(base + L.active);
   int32_t* n_active = reinterpret_cast<int32_t*>(base + L.n_active);
   cudaError_t e = launch_dense_route(offsets, perm, active, n_active, T, st);
   g_launches.fetch_add(1);
-  if (e != cudaSuccess) return e;
-  if (T > g_gemm_threshold.load() && N % 256 == 0) {
-    int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
-    int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
-    __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
-    if ((e = launch_build_chunks(offsets, 1, chunks, n_chunks, st)) != cudaSuccess) return e;
-    if ((e = launch_to_bf16(x, xb, T, K, nullptr, T, 1, nullptr, st)) != cudaSuccess) return e;
+  if (e != cudaSuccess || !dense_uses_tc(T)) return e;
+  int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
+  int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
+  __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
+  if ((e = launch_build_chunks(offsets, 1, chunks, n_chunks, st)) != cudaSuccess) return e;
+  g_launches.fetch_add(2);
+  return launch_to_bf16(x, xb, T, K, nullptr, T, 1, nullptr, st);
+}
+
+cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int N, float* y, char* base,
+                       const AttnWs& L, int* status, cudaStream_t st) {
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+  if (dense_uses_tc(T) && N % 256 == 0) {
     GroupedTcArgs p{};
     p.W = static_cast<const uint8_t*>(W);
     p.qt = qt;
     p.offsets = offsets;
     p.perm = perm;
-    p.chunks = chunks;
-    p.n_chunks = n_chunks;
+    p.chunks = reinterpret_cast<int2*>(base + L.chunks);
+    p.n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
     p.max_chunks = tc_max_chunks(T, 1, 1, 0);
-    p.hin = xb;
+    p.hin = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
     p.tok_rows = T;
     p.yout_f32 = y;
     p.T = T;
@@ -222,7 +232,7 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
     p.H = N;
     p.F = K;
     p.status = status;
-    g_launches.fetch_add(3);
+    g_launches.fetch_add(1);
     return launch_down_tc(p, st);
   }
   GroupedArgs g{};
@@ -230,8 +240,8 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
   g.S = nullptr;
   g.offsets = offsets;
   g.perm = perm;
-  g.active = active;
-  g.n_active = n_active;
+  g.active = reinterpret_cast<int32_t*>(base + L.active);
+  g.n_active = reinterpret_cast<int32_t*>(base + L.n_active);
   g.T = T;
   g.k = 1;
   g.E = 1;
@@ -269,6 +279,7 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
   __nv_bfloat16* vcb = reinterpret_cast<__nv_bfloat16*>(vc);
   cudaError_t e = launch_rmsnorm(X, b->g1, b->eps, rr, T, H, st);
   g_launches.fetch_add(1);
+  if (e == cudaSuccess) e = dense_prep(rr, T, H, base, L, st);
   if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wq, QMOE_Q4K, nh * hd, q, base, L, status, st);
   if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wk, QMOE_Q4K, nkv * hd, k, base, L, status, st);
   if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wv, QMOE_Q4K, nkv * hd, v, base, L, status, st);
@@ -281,6 +292,7 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
     g_launches.fetch_add(L.chunked ? 2 : 1);
   }
   float* proj_out = R ? rr : out;  // rr is free once Q, K, V exist
+  if (e == cudaSuccess) e = dense_prep(o, T, nh * hd, base, L, st);
   if (e == cudaSuccess) e = dense_proj(o, T, nh * hd, b->Wo, QMOE_Q4K, H, proj_out, base, L, status, st);
   if (e == cudaSuccess && R) {
     e = launch_add(R, proj_out, out, (size_t)T * H, st);

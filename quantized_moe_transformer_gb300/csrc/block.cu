@@ -7,6 +7,8 @@
 // Parallelism", "Two-Dimensional Attention at Long Context": attention over
 // context shards merged exactly from each shard's (max, normaliser, weighted
 // output) -- used here inside one GPU by the split-context decode kernel.
+#include <cmath>
+
 #include "kernels.cuh"
 
 namespace qmoe {
@@ -50,19 +52,29 @@ __global__ void dense_route_kernel(int32_t* offsets, int32_t* perm, int32_t* act
 // Angles pos * theta^(-2i/hd) and their sines and cosines are taken in double
 // (positions reach thousands of radians).
 // ---------------------------------------------------------------------------
+// Inverse frequencies theta^(-2i/hd), computed on the host in double.
+struct RopeFreq {
+  double inv[128];
+};
+
 __global__ void __launch_bounds__(256) rope_cache_kernel(float* __restrict__ q, const float* __restrict__ k,
                                                          const float* __restrict__ v, __nv_bfloat16* __restrict__ kc,
                                                          __nv_bfloat16* __restrict__ vc, int pos0, int nh, int nkv,
-                                                         int hd, double theta) {
+                                                         int hd, const __grid_constant__ RopeFreq fr) {
   extern __shared__ float cs[];  // [hd/2] cos, [hd/2] sin
   const int t = blockIdx.x, tid = threadIdx.x, half = hd / 2;
   const int pos = pos0 + t;
   for (int i = tid; i < half; i += 256) {
-    const double inv = pow(theta, -2.0 * (double)i / (double)hd);
-    double sn, cn;
-    sincos((double)pos * inv, &sn, &cn);
-    cs[i] = (float)cn;
-    cs[half + i] = (float)sn;
+    // the angle pos * inv in double, reduced to [-pi, pi] by n turns with 2 pi
+    // split into the double nearest to it and the remainder (two fused
+    // multiply-adds), then sine and cosine in single precision
+    const double a = (double)pos * fr.inv[i];
+    const double n = rint(a * 0.15915494309189535);
+    const double r = fma(-n, 2.4492935982947064e-16, fma(-n, 6.283185307179586, a));
+    float sn, cn;
+    sincosf((float)r, &sn, &cn);
+    cs[i] = cn;
+    cs[half + i] = sn;
   }
   __syncthreads();
   for (int idx = tid; idx < nh * half; idx += 256) {
@@ -219,7 +231,10 @@ cudaError_t launch_dense_route(int32_t* offsets, int32_t* perm, int32_t* active,
 
 cudaError_t launch_rope_cache(float* q, const float* k, const float* v, __nv_bfloat16* kc, __nv_bfloat16* vc, int T,
                               int pos0, int nh, int nkv, int hd, double theta, cudaStream_t st) {
-  rope_cache_kernel<<<T, 256, sizeof(float) * hd, st>>>(q, k, v, kc, vc, pos0, nh, nkv, hd, theta);
+  if (hd > 256) return cudaErrorInvalidValue;
+  RopeFreq fr{};
+  for (int i = 0; i < hd / 2; ++i) fr.inv[i] = std::pow(theta, -2.0 * (double)i / (double)hd);
+  rope_cache_kernel<<<T, 256, sizeof(float) * hd, st>>>(q, k, v, kc, vc, pos0, nh, nkv, hd, fr);
   return cudaGetLastError();
 }
 
