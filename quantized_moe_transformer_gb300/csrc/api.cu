@@ -205,7 +205,7 @@ cudaError_t dense_prep(const float* x, int T, int K, char* base, const AttnWs& L
   int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
   int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
-  if ((e = launch_build_chunks(offsets, 1, chunks, n_chunks, st)) != cudaSuccess) return e;
+  if ((e = launch_build_chunks(offsets, 1, 128, chunks, n_chunks, st)) != cudaSuccess) return e;
   g_launches.fetch_add(2);
   return launch_to_bf16(x, xb, T, K, nullptr, T, 1, nullptr, st);
 }
@@ -225,6 +225,7 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
     p.max_chunks = tc_max_chunks(T, 1, 1, 0);
     p.hin = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
     p.tok_rows = T;
+    p.nmax = 128;
     p.yout_f32 = y;
     p.T = T;
     p.k = 1;
@@ -567,7 +568,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     __nv_bfloat16* y16 = reinterpret_cast<__nv_bfloat16*>(y);
     __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
     e = staged(QMOE_STAGE_ROUTE, 2, st, [&] {
-      cudaError_t e2 = launch_build_chunks(offsets, E, chunks, n_chunks, st);
+      cudaError_t e2 = launch_build_chunks(offsets, E, tc_chunk_cap(T, k, E), chunks, n_chunks, st);
       if (e2 != cudaSuccess) return e2;
       return launch_to_bf16(X, xb, (int)(P + (has_shared ? T : 0)), H, perm, T, k, inv, st);
     });
@@ -578,6 +579,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     p.chunks = chunks;
     p.n_chunks = n_chunks;
     p.max_chunks = tc_max_chunks(T, k, E, has_shared);
+    p.nmax = tc_chunk_cap(T, k, E);
     p.T = T;
     p.k = k;
     p.E = E;

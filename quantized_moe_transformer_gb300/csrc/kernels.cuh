@@ -54,11 +54,13 @@ struct GroupedTcArgs {
   __nv_bfloat16* yout;
   float* yout_f32;  // down pass: write fp32 instead of bf16 when not null
   int tok_rows;     // rows of the token matrix (xb for gate/up, hin for down)
+  int nmax;         // chunk cap the chunk list was built with (64 or 128)
   int T, k, E, H, F;
   int* status;
 };
 int tc_max_chunks(int T, int k, int E, int has_shared);
-cudaError_t launch_build_chunks(const int32_t* offsets, int E, int2* chunks, int32_t* n_chunks,
+int tc_chunk_cap(int T, int k, int E);
+cudaError_t launch_build_chunks(const int32_t* offsets, int E, int cap, int2* chunks, int32_t* n_chunks,
                                 cudaStream_t st);
 cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st);
 cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st);

@@ -52,34 +52,38 @@
 
 namespace qmoe {
 
-constexpr int TC_N = 128;       // tokens per chunk (largest MMA N used)
 constexpr int TC_BK = 64;       // K per stage
-constexpr int TC_STAGES = 4;
 constexpr int TC_PRODUCER_WARPS = 16;
 constexpr int TC_MMA_WARP = 4 + TC_PRODUCER_WARPS;  // 20
 constexpr int TC_LOAD_WARP = TC_MMA_WARP + 1;       // 21: token tiles
 constexpr int TC_RAW_WARP = TC_MMA_WARP + 2;        // 22: packed weights
 constexpr int TC_MMA_WARP2 = TC_MMA_WARP + 3;       // 23: MMAs of the second accumulator
 constexpr int TC_THREADS = 32 * (TC_MMA_WARP2 + 1); // 768
-constexpr int TC_B_BYTES = TC_N * TC_BK * 2;  // 16 KB token tile per stage
 constexpr int TC_EPI_BYTES = 2048;            // per epilogue warp: 16 tokens x 32 values x 4 B
-constexpr uint32_t TC_D1_COL = 128;      // D0 at column 0, D1 at 128
-constexpr uint32_t TC_A_COL = 256;       // A stage s: A0 at 256 + 64 s, A1 at + 32
 constexpr uint32_t TC_A_STAGE_COLS = 64;
+constexpr int TC_N_MIN = 64;                  // the smaller chunk cap (bounds the chunk count)
 
 // Packed weights are staged per super-block: RS ring stages of 256 rows (A0
 // rows, then A1 rows), each filled by one or two 2-D tensor copies.
 // Token tiles have their own ring of TS stages (deeper than the TMEM A ring)
 // so that their loads run ahead of the MMAs instead of inside the A ring's
 // round trip.
-template <int QT>
+// NMAX is the chunk cap (largest MMA N): the two accumulators take 2 NMAX of
+// the 512 TMEM columns and the A stages (64 columns each) the rest, so a cap
+// of 64 rows buys 6 A stages instead of 4; it is chosen when experts get few
+// rows (T * k / E <= 32), where the ring's depth, not the MMAs, sets the pace.
+template <int QT, int NMAX>
 struct TcCfg {
   static constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
+  static constexpr int S = (512 - 2 * NMAX) / TC_A_STAGE_COLS;  // A stages in TMEM
+  static constexpr uint32_t D1_COL = NMAX;                     // D0 at column 0
+  static constexpr uint32_t A_COL = 2 * NMAX;                  // A stage s at A_COL + 64 s
+  static constexpr int B_BYTES = NMAX * TC_BK * 2;             // token tile per stage
   static constexpr int RS = 3;
-  static constexpr int TS = QT == QMOE_Q5K ? 5 : 6;
+  static constexpr int TS = NMAX == 64 ? 10 : (QT == QMOE_Q5K ? 5 : 6);
   static constexpr int RAW_STAGE = 256 * BYTES;
-  static constexpr int SMEM = TS * TC_B_BYTES + RS * RAW_STAGE + 4 * TC_EPI_BYTES + 1024 /*align*/ +
-                              256 /*barriers*/;
+  static constexpr int SMEM = TS * B_BYTES + RS * RAW_STAGE + 4 * TC_EPI_BYTES + 1024 /*align*/ +
+                              512 /*barriers*/;
 };
 
 struct TcArgs {
@@ -177,17 +181,18 @@ __device__ __forceinline__ uint32_t pick_word(const uint4 v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-template <bool GATEUP, int QT>
+template <bool GATEUP, int QT, int NMAX>
 __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, const __grid_constant__ TcMaps maps) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned start, reached by pointer arithmetic on the shared
   // array so that accesses stay shared-memory instructions
   const uint32_t s0 = tc::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((s0 + 1023u) & ~1023u) - s0);
-  constexpr int S = TC_STAGES;
-  using Cfg = TcCfg<QT>;
-  constexpr int RS = Cfg::RS, TS = Cfg::TS, BYTES = Cfg::BYTES;
-  uint8_t* sB = smem;                                         // [TS][TC_N][128 B] token tiles
+  using Cfg = TcCfg<QT, NMAX>;
+  constexpr int S = Cfg::S, RS = Cfg::RS, TS = Cfg::TS, BYTES = Cfg::BYTES;
+  constexpr int TC_B_BYTES = Cfg::B_BYTES;
+  constexpr uint32_t TC_D1_COL = Cfg::D1_COL, TC_A_COL = Cfg::A_COL;
+  uint8_t* sB = smem;                                         // [TS][NMAX][128 B] token tiles
   uint8_t* sRaw = smem + TS * TC_B_BYTES;                     // [RS][256][BYTES] packed rows
   uint8_t* sEpi = sRaw + RS * Cfg::RAW_STAGE;                 // [4][TC_EPI_BYTES]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + 4 * TC_EPI_BYTES);
@@ -519,7 +524,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
 // last) is cut into ceil(rows / 128) chunks of near-equal size (first row
 // below 2^24, packed with the row count). One CTA; the scan of chunk counts
 // runs in warp 0.
-__global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __restrict__ offsets, int E,
+__global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __restrict__ offsets, int E, int cap,
                                                             int2* __restrict__ chunks,
                                                             int32_t* __restrict__ n_chunks) {
   extern __shared__ int32_t start[];  // [E+1] exclusive scan of chunk counts
@@ -528,7 +533,7 @@ __global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __res
     int run = 0;
     for (int b = 0; b <= E; b += 32) {
       const int e = b + lane;
-      const int c = e <= E ? (offsets[e + 1] - offsets[e] + TC_N - 1) / TC_N : 0;
+      const int c = e <= E ? (offsets[e + 1] - offsets[e] + cap - 1) / cap : 0;
       int incl = c;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -544,7 +549,7 @@ __global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __res
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     const int Me = offsets[e + 1] - offsets[e];
     if (Me <= 0) continue;
-    const int nc = (Me + TC_N - 1) / TC_N;
+    const int nc = (Me + cap - 1) / cap;
     for (int i = 0; i < nc; ++i) {
       // rows [i*Me/nc, (i+1)*Me/nc): between 1 and 128 of them
       const int c0 = (int)((long long)i * Me / nc);
@@ -654,11 +659,15 @@ int tc_num_sms() {
 
 int tc_max_chunks(int T, int k, int E, int has_shared) {
   const int P = T * k;
-  return (P + (has_shared ? T : 0)) / TC_N + E + 1;
+  return (P + (has_shared ? T : 0)) / TC_N_MIN + E + 1;
 }
 
-cudaError_t launch_build_chunks(const int32_t* offsets, int E, int2* chunks, int32_t* n_chunks, cudaStream_t st) {
-  build_chunks_kernel<<<1, 1024, sizeof(int32_t) * (E + 1), st>>>(offsets, E, chunks, n_chunks);
+int tc_chunk_cap(int T, int k, int E) { return (long long)T * k <= 32LL * E ? 64 : 128; }
+
+cudaError_t launch_build_chunks(const int32_t* offsets, int E, int cap, int2* chunks, int32_t* n_chunks,
+                                cudaStream_t st) {
+  if (cap != 64 && cap != 128) return cudaErrorInvalidValue;
+  build_chunks_kernel<<<1, 1024, sizeof(int32_t) * (E + 1), st>>>(offsets, E, cap, chunks, n_chunks);
   return cudaGetLastError();
 }
 
@@ -720,20 +729,26 @@ static bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_
   return true;
 }
 
-template <bool GATEUP, int QT>
-static cudaError_t tc_launch_t(const TcArgs& a, const TcMaps& maps, int max_items, cudaStream_t st) {
+template <bool GATEUP, int QT, int NMAX>
+static cudaError_t tc_launch_n(const TcArgs& a, const TcMaps& maps, int max_items, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(moe_tc_kernel<GATEUP, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcCfg<QT>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(moe_tc_kernel<GATEUP, QT, NMAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<QT, NMAX>::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   int grid = tc_num_sms();
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
-  moe_tc_kernel<GATEUP, QT><<<grid, TC_THREADS, TcCfg<QT>::SMEM, st>>>(a, maps);
+  moe_tc_kernel<GATEUP, QT, NMAX><<<grid, TC_THREADS, TcCfg<QT, NMAX>::SMEM, st>>>(a, maps);
   return cudaGetLastError();
+}
+
+template <bool GATEUP, int QT>
+static cudaError_t tc_launch_t(const TcArgs& a, const TcMaps& maps, int max_items, int nmax, cudaStream_t st) {
+  return nmax == 64 ? tc_launch_n<GATEUP, QT, 64>(a, maps, max_items, st)
+                    : tc_launch_n<GATEUP, QT, 128>(a, maps, max_items, st);
 }
 
 static TcArgs tc_args(const GroupedTcArgs& p) {
@@ -788,7 +803,8 @@ cudaError_t launch_gateup_tc(const GroupedTcArgs& p, cudaStream_t st) {
       !encode_tokens(&m.tok, p.xb, (uint64_t)p.tok_rows, (uint64_t)p.H))
     return cudaErrorInvalidValue;
   const int items = p.max_chunks * (p.F / 128);
-  return p.qt == QMOE_Q5K ? tc_launch_t<true, QMOE_Q5K>(a, m, items, st) : tc_launch_t<true, QMOE_Q4K>(a, m, items, st);
+  return p.qt == QMOE_Q5K ? tc_launch_t<true, QMOE_Q5K>(a, m, items, p.nmax, st)
+                          : tc_launch_t<true, QMOE_Q4K>(a, m, items, p.nmax, st);
 }
 
 cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
@@ -803,7 +819,8 @@ cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
   memset(&m.w2, 0, sizeof(m.w2));
   memset(&m.s2, 0, sizeof(m.s2));
   const int items = p.max_chunks * (p.H / 256);
-  return p.qt == QMOE_Q5K ? tc_launch_t<false, QMOE_Q5K>(a, m, items, st) : tc_launch_t<false, QMOE_Q4K>(a, m, items, st);
+  return p.qt == QMOE_Q5K ? tc_launch_t<false, QMOE_Q5K>(a, m, items, p.nmax, st)
+                          : tc_launch_t<false, QMOE_Q4K>(a, m, items, p.nmax, st);
 }
 
 cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const int32_t* inv, const float* w, const float* R, float* out,
