@@ -52,7 +52,7 @@
 
 namespace qmoe {
 
-constexpr int TC_BK = 64;       // K per stage
+constexpr int TC_BK = 128;      // K per stage: half a super-block
 constexpr int TC_PRODUCER_WARPS = 16;
 constexpr int TC_MMA_WARP = 4 + TC_PRODUCER_WARPS;  // 20
 constexpr int TC_LOAD_WARP = TC_MMA_WARP + 1;       // 21: token tiles
@@ -60,7 +60,7 @@ constexpr int TC_RAW_WARP = TC_MMA_WARP + 2;        // 22: packed weights
 constexpr int TC_MMA_WARP2 = TC_MMA_WARP + 3;       // 23: MMAs of the second accumulator
 constexpr int TC_THREADS = 32 * (TC_MMA_WARP2 + 1); // 768
 constexpr int TC_EPI_BYTES = 2048;            // per epilogue warp: 16 tokens x 32 values x 4 B
-constexpr uint32_t TC_A_STAGE_COLS = 64;
+constexpr uint32_t TC_A_STAGE_COLS = TC_BK;  // two matrices x TC_BK / 2 columns
 constexpr int TC_N_MIN = 64;                  // the smaller chunk cap (bounds the chunk count)
 
 // Packed weights are staged per super-block: RS ring stages of 256 rows (A0
@@ -69,18 +69,19 @@ constexpr int TC_N_MIN = 64;                  // the smaller chunk cap (bounds t
 // so that their loads run ahead of the MMAs instead of inside the A ring's
 // round trip.
 // NMAX is the chunk cap (largest MMA N): the two accumulators take 2 NMAX of
-// the 512 TMEM columns and the A stages (64 columns each) the rest, so a cap
-// of 64 rows buys 6 A stages instead of 4; it is chosen when experts get few
-// rows (T * k / E <= 32), where the ring's depth, not the MMAs, sets the pace.
+// the 512 TMEM columns and the A stages (128 columns each: K = 128 for both
+// matrices) the rest, so a cap of 64 rows buys 3 A stages instead of 2; it is
+// chosen when experts get few rows (T * k / E <= 32).
 template <int QT, int NMAX>
 struct TcCfg {
   static constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
-  static constexpr int S = (512 - 2 * NMAX) / TC_A_STAGE_COLS;  // A stages in TMEM
-  static constexpr uint32_t D1_COL = NMAX;                     // D0 at column 0
-  static constexpr uint32_t A_COL = 2 * NMAX;                  // A stage s at A_COL + 64 s
-  static constexpr int B_BYTES = NMAX * TC_BK * 2;             // token tile per stage
-  static constexpr int RS = 3;
-  static constexpr int TS = NMAX == 64 ? 10 : (QT == QMOE_Q5K ? 5 : 6);
+  static constexpr int S = (512 - 2 * NMAX) / (int)TC_A_STAGE_COLS;  // A stages in TMEM
+  static constexpr uint32_t D1_COL = NMAX;                          // D0 at column 0
+  static constexpr uint32_t A_COL = 2 * NMAX;                       // A stage s at A_COL + 128 s
+  static constexpr int B_HALF = NMAX * 128;                         // K 64 x NMAX rows, one swizzle atom row each
+  static constexpr int B_BYTES = 2 * B_HALF;                        // token tile per stage: two K halves
+  static constexpr int RS = (QT == QMOE_Q5K && NMAX == 128) ? 2 : 3;
+  static constexpr int TS = NMAX == 64 ? 5 : 3;
   static constexpr int RAW_STAGE = 256 * BYTES;
   static constexpr int SMEM = TS * B_BYTES + RS * RAW_STAGE + 4 * TC_EPI_BYTES + 1024 /*align*/ +
                               512 /*barriers*/;
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   uint8_t* smem = smem_raw + (((s0 + 1023u) & ~1023u) - s0);
   using Cfg = TcCfg<QT, NMAX>;
   constexpr int S = Cfg::S, RS = Cfg::RS, TS = Cfg::TS, BYTES = Cfg::BYTES;
-  constexpr int TC_B_BYTES = Cfg::B_BYTES;
+  constexpr int TC_B_BYTES = Cfg::B_BYTES, TC_B_HALF = Cfg::B_HALF;
   constexpr uint32_t TC_D1_COL = Cfg::D1_COL, TC_A_COL = Cfg::A_COL;
   uint8_t* sB = smem;                                         // [TS][NMAX][128 B] token tiles
   uint8_t* sRaw = smem + TS * TC_B_BYTES;                     // [RS][256][BYTES] packed rows
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NB = GATEUP ? g.F / 128 : g.H / 256;      // weight blocks per chunk
   const int KT = GATEUP ? g.H / TC_BK : g.F / TC_BK;  // k-tiles
-  const int KB = KT / 4;                              // super-blocks along K
+  const int KB = KT / 2;                              // super-blocks along K
   const int total = g.n_chunks[0] * NB;
   const int n_mine = (int)blockIdx.x < total ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
 
@@ -319,18 +320,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     }
   } else if (warp < 4 + TC_PRODUCER_WARPS) {
     // ------------------------------------------------------------ producers
-    // Warp 4 + pw covers TMEM lane quarter pw % 4 of matrix (pw / 4) % 2, and
-    // sub-block s = pw / 8 of each k-tile's two: thread = one weight row, 32
-    // weights per k-tile. A k-tile is stored and its stage released before
-    // the next one is dequantised, so that the stage round trip (MMA commit ->
-    // producers -> MMA) stays short.
+    // Warp 4 + pw covers TMEM lane quarter pw % 4 of matrix (pw / 4) % 2 and
+    // sub-blocks 2 sp, 2 sp + 1 (sp = pw / 8) of each k-tile's four: thread =
+    // one weight row, 64 weights per k-tile. A k-tile is stored and its stage
+    // released before the next one is dequantised, so that the stage round
+    // trip (MMA commit -> producers -> MMA) stays short.
     const int pw = warp - 4;
-    const int mat = (pw >> 2) & 1, s = pw >> 3;
+    const int mat = (pw >> 2) & 1, sp = pw >> 3;
     const int r = 32 * (pw & 3) + lane;
-    const uint32_t ta0 = tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * 32 + s * 16);
+    const uint32_t ta0 =
+        tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * (TC_BK / 2) + sp * 32);
     const uint8_t* my_row = sRaw + (size_t)(mat * 128 + r) * BYTES;
     const int NU = n_mine * KB;
-    uint32_t wa[16];
+    uint32_t wa[16], wb[16];
     uint4 hdr = make_uint4(0, 0, 0, 0), hq0 = hdr, hq1 = hdr;
     // loads the super-block header (and Q5_K high bits) of ring slot u % RS
     auto open_sb = [&](int u) -> bool {
@@ -343,19 +345,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       }
       return true;
     };
-    auto deq = [&](int u, int kk, uint32_t* o) {
-      const int j = 2 * kk + s;
+    // sub-blocks 4 hh + 2 sp and + 1 of super-block u
+    auto deq = [&](int u, int hh) {
       const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
-      const uint4 qv = rp[(QT == QMOE_Q5K ? 3 : 1) + j];
-      const uint32_t hb = QT == QMOE_Q5K ? pick_word((j >> 2) ? hq1 : hq0, j & 3) : 0u;
-      dequant_sub<QT>(hdr, qv, hb, j, o);
+      const int j0 = 4 * hh + 2 * sp;
+      const uint4 q0 = rp[(QT == QMOE_Q5K ? 3 : 1) + j0];
+      const uint4 q1 = rp[(QT == QMOE_Q5K ? 3 : 1) + j0 + 1];
+      const uint4 hq = hh ? hq1 : hq0;  // high bits of sub-blocks 4 hh .. 4 hh + 3
+      dequant_sub<QT>(hdr, q0, QT == QMOE_Q5K ? pick_word(hq, 2 * sp) : 0u, j0, wa);
+      dequant_sub<QT>(hdr, q1, QT == QMOE_Q5K ? pick_word(hq, 2 * sp + 1) : 0u, j0 + 1, wb);
     };
     bool ok = NU > 0 && open_sb(0);
-    if (ok) deq(0, 0, wa);
+    if (ok) deq(0, 0);
     int kg = 0;
     for (int u = 0; u < NU && ok; ++u) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
+      for (int hh = 0; hh < 2; ++hh) {
         const int stage = kg % S;
         // warp-uniform outcome: the TMEM stores below are warp-collective
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], ((kg / S) & 1) ^ 1, abort_flag))) {
@@ -368,15 +373,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         if (pw == 0 && lane == 0 && kg >= S) tc::mbar_arrive(&tok_empty[(kg - S) % TS]);
         // store and release the stage first: this is the path the MMAs wait on
         tc::tc_fence_after();
-        tc::tmem_st16(ta0 + (uint32_t)stage * TC_A_STAGE_COLS, wa);
+        const uint32_t ta = ta0 + (uint32_t)stage * TC_A_STAGE_COLS;
+        tc::tmem_st16(ta, wa);
+        tc::tmem_st16(ta + 16, wb);
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&full[stage]);
         ++kg;
         // then dequantise the next k-tile while the MMAs run
-        if (kk < 3) {
-          deq(u, kk + 1, wa);
+        if (hh == 0) {
+          deq(u, 1);
         } else {
           // every read of slot u is done: release it to the weight loader
           tc::fence_proxy_async_smem();
@@ -384,7 +391,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
           if (lane == 0) tc::mbar_arrive(&raw_empty[u % RS]);
           if (u + 1 < NU) {
             if (!open_sb(u + 1)) ok = false;
-            else deq(u + 1, 0, wa);
+            else deq(u + 1, 0);
           }
         }
         if (!ok) break;
@@ -458,9 +465,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
             break;
           }
           uint8_t* b_st = sB + stage * TC_B_BYTES;
-          tc::mbar_expect_tx(&tok_full[stage], (uint32_t)n16 * 16 * 128);
-          for (int i = 0; i < n16; ++i)
-            tma_load_2d(b_st + i * 2048, &maps.tok, kt * TC_BK, pos0 + 16 * i, &tok_full[stage]);
+          tc::mbar_expect_tx(&tok_full[stage], (uint32_t)n16 * 2 * 16 * 128);
+          for (int half = 0; half < 2; ++half)
+            for (int i = 0; i < n16; ++i)
+              tma_load_2d(b_st + half * TC_B_HALF + i * 2048, &maps.tok, kt * TC_BK + 64 * half, pos0 + 16 * i,
+                          &tok_full[stage]);
         }
       }
     }
@@ -492,13 +501,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a = tmem + TC_A_COL + (uint32_t)stage * TC_A_STAGE_COLS + (uint32_t)which * 32;
+          const uint32_t a = tmem + TC_A_COL + (uint32_t)stage * TC_A_STAGE_COLS + (uint32_t)which * (TC_BK / 2);
           // the descriptor's start address (16-byte units, low bits) advances by
-          // 32 bytes per K step of 16
+          // 32 bytes per K step of 16 within a K half, by TC_B_HALF per half
           const uint64_t bd = bdesc0 + (uint64_t)(ts * (TC_B_BYTES >> 4));
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk)
-            tc::mma_bf16_ts(d_tmem, a + 8 * kk, bd + 2 * kk, idesc, (kt | kk) != 0);
+            tc::mma_bf16_ts(d_tmem, a + 8 * kk, bd + (uint64_t)((kk >> 2) * (TC_B_HALF >> 4) + 2 * (kk & 3)), idesc,
+                            (kt | kk) != 0);
           tc::mma_commit(&empty[stage]);
           if (++stage == S) stage = 0;
           if (++ts == TS) ts = 0;
