@@ -18,7 +18,8 @@
 // chunk of 20 tokens costs the tensor core 32 columns, not 128 rows.
 //
 // A work item is (token chunk, weight block). A weight block is two 128-row
-// matrices A0, A1 with accumulators D0, D1 (TMEM columns 0-127, 128-255):
+// matrices A0, A1 with accumulators D0, D1 (TMEM columns [0, NMAX) and
+// [NMAX, 2 NMAX), NMAX = the chunk cap, 64 or 128):
 // gate rows and the matching up rows (gate/up pass: SwiGLU pairs lane f of D0
 // with lane f of D1 in one thread), or two consecutive 128-row blocks of the
 // down matrix. One persistent CTA per SM walks the items; warp roles (768
@@ -27,18 +28,20 @@
 //               SwiGLU to bf16 h (gate/up) or the y store (down), leaving
 //               through a small shared-memory transpose in 16-byte stores;
 //   warps 4-19  producers: warp 4 + pw covers lane quarter pw % 4 of A0
-//               (pw / 4 even) or A1, and sub-block pw / 8 of each k-tile; a
-//               thread dequantises 32 weights of its row per k-tile in bf16x2
+//               (pw / 4 even) or A1, and sub-blocks 2 (pw / 8), 2 (pw / 8) + 1
+//               of each k-tile's four (k-tile = K 128, half a super-block); a
+//               thread dequantises 64 weights of its row per k-tile in bf16x2
 //               arithmetic from the packed super-block ring and stores them
-//               into the k-tile's A stage in TMEM (columns 256 + 64 s ..);
+//               into the k-tile's A stage in TMEM (columns 2 NMAX + 128 s ..);
 //   warps 20,23 issue the MMAs of D0 and D1 (one lane each); warp 20 also
 //               allocates the 512 TMEM columns;
 //   warp 21     copies each k-tile's token rows into the stage's
 //               shared-memory tile (one lane, 2-D tensor copies);
 //   warp 22     copies the packed weight rows into the super-block ring (one
 //               lane, 2-D tensor copies).
-// Four A stages in TMEM and five or six token stages in shared memory, each
-// ring with its own full/empty barriers, decouple the roles.
+// Two A stages in TMEM (three when NMAX is 64), three or five token stages
+// and two or three packed super-block stages in shared memory, each ring with
+// its own full/empty barriers, decouple the roles.
 // Every wait is bounded: on time-out the CTA records QMOE_ERR_TIMEOUT, drains
 // its MMAs, frees its TMEM and returns.
 #include <cuda.h>
@@ -109,7 +112,7 @@ struct TcArgs {
 // w/w2 the routed experts' gate/up (or down in w), s/s2 the shared expert's.
 struct TcMaps {
   CUtensorMap w, w2, s, s2;
-  CUtensorMap tok;  // token rows [rows][K] bf16, 128-byte swizzled boxes of 16 rows x 64
+  CUtensorMap tok;  // token rows [rows][K] bf16, 128-byte swizzled boxes of 32 rows x 64
 };
 
 __device__ __forceinline__ int tc_pair_row(int p, int T, int k) { return p < T * k ? p / k : p - T * k; }
@@ -176,6 +179,17 @@ __device__ __forceinline__ void dequant_sub(const uint4 hdr, const uint4 qv, uin
       o[4 * n + i] = *reinterpret_cast<uint32_t*>(&v);
     }
   }
+}
+
+// silu(g) * u with silu(g) = g * sigmoid(g) = g/2 + (g/2) tanh(g/2): one
+// hardware tanh approximation (tanh.approx.f32, maximum relative error about
+// 2^-11) instead of an exponential and a reciprocal; the result is rounded to
+// bf16 (relative step 2^-8) right after.
+__device__ __forceinline__ float silu_mul_tanh(float g, float u) {
+  const float hg = 0.5f * g;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hg));
+  return fmaf(hg, t, hg) * u;
 }
 
 __device__ __forceinline__ uint32_t pick_word(const uint4 v, int i) {
@@ -268,7 +282,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
           const int col = kperm_slot(lane);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            st16[i * 32 + col] = __float2bfloat16_rn(silu_mul(__uint_as_float(a[i]), __uint_as_float(b[i])));
+            st16[i * 32 + col] = __float2bfloat16_rn(silu_mul_tanh(__uint_as_float(a[i]), __uint_as_float(b[i])));
           __syncwarp();
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
@@ -401,11 +415,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     // ------------------------------------------------------------ weight loader
     // One lane: super-block u of the CTA's item sequence goes to ring slot
     // u % RS as 2-D tensor copies of 128 (gate/up: A0 from the gate matrix, A1
-    // from the up matrix) or 256 (down) rows x one super-block column; the
-    // next item's rows are prefetched into L2 when an item starts.
+    // from the up matrix) or 256 (down) rows x one super-block column. (An L2
+    // prefetch of the next item's rows, tried here, cost more in tensor-copy
+    // queue time than it saved.)
     if (lane == 0) {
       const int NU = n_mine * KB;
-      const size_t rb = (size_t)KB * BYTES;
       auto block_of = [&](int j, int& e, int& y0) {
         const int wi = (int)blockIdx.x + j * (int)gridDim.x;
         const Chunk ch = chunk_at(g.chunks, wi / NB);
@@ -413,24 +427,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         e = ch.e;
         y0 = GATEUP ? (e < g.E ? e * g.F : 0) + blk * 128 : (e < g.E ? e * g.H : 0) + blk * 256;
       };
-      // the item that starts about RS super-blocks after item j does
-      const int lead = (RS + KB - 1) / KB;
-      auto prefetch_item = [&](int j) {
-        if (j >= n_mine) return;
-        int e, y0;
-        block_of(j, e, y0);
-        const uint32_t rows = GATEUP ? 128u : 256u;
-        tc::prefetch_l2((e < g.E ? g.W : g.S) + (size_t)y0 * rb, rows * (uint32_t)rb);
-        if (GATEUP) tc::prefetch_l2((e < g.E ? g.W2 : g.S2) + (size_t)y0 * rb, rows * (uint32_t)rb);
-      };
-      for (int j = 0; j < lead; ++j) prefetch_item(j);
       for (int u = 0; u < NU; ++u) {
         const int slot = u % RS;
         if (!tc::mbar_wait(&raw_empty[slot], ((u / RS) & 1) ^ 1, abort_flag)) break;
         const int j = u / KB, sb = u % KB;
         int e, y0;
         block_of(j, e, y0);
-        if (sb == 0) prefetch_item(j + lead);
         uint8_t* dst = sRaw + (size_t)slot * Cfg::RAW_STAGE;
         tc::mbar_expect_tx(&raw_full[slot], 256 * BYTES);
         const int x = sb * BYTES;
@@ -447,16 +449,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     // ------------------------------------------------------------ token loader
     // The chunk's rows are consecutive rows of the token matrix (X in
     // permutation order, or h): per k-tile one lane copies them as boxes of
-    // 16 rows x 64 values with 128-byte swizzle, which is the layout the MMA's
-    // operand descriptor describes. Rows past the chunk (up to the MMA N) are
-    // the next rows of the matrix or zero fill past its end; their outputs
-    // are never stored.
+    // 32 rows x 64 values with 128-byte swizzle, which is the layout the MMA's
+    // operand descriptor describes. Rows past the chunk (up to the MMA N, or
+    // to the next multiple of 32) are the next rows of the matrix or zero fill
+    // past its end; their outputs are never stored. (Boxes of 16 rows took
+    // twice the copy instructions and queued behind the weight copies.)
     if (lane == 0) {
       int kg = 0;
       bool ok = true;
       for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x) {
         const Chunk ch = chunk_at(g.chunks, wi / NB);
-        const int n16 = (ch.n + 15) >> 4;
+        const int n32 = (ch.n + 31) >> 5;  // NMAX is a multiple of 32
         const int pos0 = g.offsets[ch.e] + ch.c0;
         for (int kt = 0; kt < KT; ++kt, ++kg) {
           const int stage = kg % TS;
@@ -465,10 +468,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
             break;
           }
           uint8_t* b_st = sB + stage * TC_B_BYTES;
-          tc::mbar_expect_tx(&tok_full[stage], (uint32_t)n16 * 2 * 16 * 128);
+          tc::mbar_expect_tx(&tok_full[stage], (uint32_t)n32 * 2 * 32 * 128);
           for (int half = 0; half < 2; ++half)
-            for (int i = 0; i < n16; ++i)
-              tma_load_2d(b_st + half * TC_B_HALF + i * 2048, &maps.tok, kt * TC_BK + 64 * half, pos0 + 16 * i,
+            for (int i = 0; i < n32; ++i)
+              tma_load_2d(b_st + half * TC_B_HALF + i * 4096, &maps.tok, kt * TC_BK + 64 * half, pos0 + 32 * i,
                           &tok_full[stage]);
         }
       }
@@ -770,7 +773,7 @@ static TcArgs tc_args(const GroupedTcArgs& p) {
   return a;
 }
 
-// Token matrix [rows][K] bf16 as boxes of 16 rows x 64 values, 128-byte swizzle.
+// Token matrix [rows][K] bf16 as boxes of 32 rows x 64 values, 128-byte swizzle.
 static bool encode_tokens(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
   struct Entry {
     const void* base;
@@ -790,7 +793,7 @@ static bool encode_tokens(CUtensorMap* m, const void* base, uint64_t rows, uint6
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {K, rows};
   const cuuint64_t strides[1] = {K * 2};
-  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t box[2] = {64, 32};
   const cuuint32_t estr[2] = {1, 1};
   if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

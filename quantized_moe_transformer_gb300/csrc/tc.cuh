@@ -195,12 +195,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t ta, const uint32_t* v) {
 // Blocks until this thread's earlier tcgen05.st have completed.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Asks for ``bytes`` (a multiple of 16, 16-byte aligned) at ``p`` to be brought
-// into L2; nothing is written.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // 16-byte read-only global load that does not allocate in L1.
 __device__ __forceinline__ uint4 ldg_na(const void* p) {
   uint4 v;
