@@ -22,11 +22,13 @@
 // [NMAX, 2 NMAX), NMAX = the chunk cap, 64 or 128):
 // gate rows and the matching up rows (gate/up pass: SwiGLU pairs lane f of D0
 // with lane f of D1 in one thread), or two consecutive 128-row blocks of the
-// down matrix. One persistent CTA per SM walks the items; warp roles (768
+// down matrix. One persistent CTA per SM walks the items; warp roles (896
 // threads):
-//   warps 0-3   epilogue: TMEM -> registers (warp w reads lanes 32w..32w+31),
-//               SwiGLU to bf16 h (gate/up) or the y store (down), leaving
-//               through a small shared-memory transpose in 16-byte stores;
+//   warps 0-3, 24-27  epilogue: TMEM -> registers (warp w reads lanes
+//               32 (w % 4) .. + 31; the two warps of a lane quarter take
+//               alternate groups of 16 tokens), SwiGLU to bf16 h (gate/up) or
+//               the y store (down), leaving through a small shared-memory
+//               transpose in 16-byte stores;
 //   warps 4-19  producers: warp 4 + pw covers lane quarter pw % 4 of A0
 //               (pw / 4 even) or A1, and sub-blocks 2 (pw / 8), 2 (pw / 8) + 1
 //               of each k-tile's four (k-tile = K 128, half a super-block); a
@@ -61,7 +63,9 @@ constexpr int TC_MMA_WARP = 4 + TC_PRODUCER_WARPS;  // 20
 constexpr int TC_LOAD_WARP = TC_MMA_WARP + 1;       // 21: token tiles
 constexpr int TC_RAW_WARP = TC_MMA_WARP + 2;        // 22: packed weights
 constexpr int TC_MMA_WARP2 = TC_MMA_WARP + 3;       // 23: MMAs of the second accumulator
-constexpr int TC_THREADS = 32 * (TC_MMA_WARP2 + 1); // 768
+constexpr int TC_EPI_WARP2 = TC_MMA_WARP2 + 1;      // 24-27: second epilogue warp per lane quarter
+constexpr int TC_EPI_WARPS = 8;
+constexpr int TC_THREADS = 32 * (TC_EPI_WARP2 + 4); // 896
 constexpr int TC_EPI_BYTES = 2048;            // per epilogue warp: 16 tokens x 32 values x 4 B
 constexpr uint32_t TC_A_STAGE_COLS = TC_BK;  // two matrices x TC_BK / 2 columns
 constexpr int TC_N_MIN = 64;                  // the smaller chunk cap (bounds the chunk count)
@@ -84,9 +88,9 @@ struct TcCfg {
   static constexpr int B_HALF = NMAX * 128;                         // K 64 x NMAX rows, one swizzle atom row each
   static constexpr int B_BYTES = 2 * B_HALF;                        // token tile per stage: two K halves
   static constexpr int RS = (QT == QMOE_Q5K && NMAX == 128) ? 2 : 3;
-  static constexpr int TS = NMAX == 64 ? 5 : 3;
+  static constexpr int TS = NMAX == 64 ? (QT == QMOE_Q5K ? 4 : 5) : 3;
   static constexpr int RAW_STAGE = 256 * BYTES;
-  static constexpr int SMEM = TS * B_BYTES + RS * RAW_STAGE + 4 * TC_EPI_BYTES + 1024 /*align*/ +
+  static constexpr int SMEM = TS * B_BYTES + RS * RAW_STAGE + TC_EPI_WARPS * TC_EPI_BYTES + 1024 /*align*/ +
                               512 /*barriers*/;
 };
 
@@ -168,11 +172,15 @@ __device__ __forceinline__ void dequant_sub(const uint4 hdr, const uint4 qv, uin
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
   for (int n = 0; n < 4; ++n) {
+    // Q5_K: the high bits of weights 8n .. 8n+7 copied to bits 4-11 and
+    // 16-23, so that (u >> i) holds that of weight 8n+i at bit 4 and that of
+    // weight 8n+i+4 at bit 20 (the 16s of the two bf16 mantissas below)
+    const uint32_t u = QT == QMOE_Q5K ? ((hb >> (8 * n)) & 0xFFu) * 0x10010u : 0u;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       // quants of weights 8n+i and 8n+i+4 as bf16 128+q in the two halves
       uint32_t x = ((w[n] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-      if (QT == QMOE_Q5K) x |= (((hb >> (8 * n + i)) & 0x11u) * 0x10010u) & 0x00100010u;
+      if (QT == QMOE_Q5K) x |= (u >> i) & 0x00100010u;
       __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
       v = __hadd2(v, m128);             // q, exact
       v = __hfma2(v, ds2, ndm2);        // q*d*s - dmin*m, one rounding
@@ -209,8 +217,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   constexpr uint32_t TC_D1_COL = Cfg::D1_COL, TC_A_COL = Cfg::A_COL;
   uint8_t* sB = smem;                                         // [TS][NMAX][128 B] token tiles
   uint8_t* sRaw = smem + TS * TC_B_BYTES;                     // [RS][256][BYTES] packed rows
-  uint8_t* sEpi = sRaw + RS * Cfg::RAW_STAGE;                 // [4][TC_EPI_BYTES]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + 4 * TC_EPI_BYTES);
+  uint8_t* sEpi = sRaw + RS * Cfg::RAW_STAGE;                 // [TC_EPI_WARPS][TC_EPI_BYTES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + TC_EPI_WARPS * TC_EPI_BYTES);
   uint64_t* full = bars;                // [S]  A stage stored
   uint64_t* empty = bars + S;           // [S]  MMAs of the stage done
   uint64_t* tok_full = bars + 2 * S;    // [TS] token tile landed
@@ -244,7 +252,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       tc::mbar_init(&raw_empty[i], TC_PRODUCER_WARPS);
     }
     tc::mbar_init(acc_full, 2);
-    tc::mbar_init(acc_empty, 4);
+    tc::mbar_init(acc_empty, TC_EPI_WARPS);
     tc::mbar_init(&drain[0], 1);
     tc::mbar_init(&drain[1], 1);
     *abort_flag = 0;
@@ -256,14 +264,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < 4 || warp >= TC_EPI_WARP2) {
     // ------------------------------------------------------------ epilogue
     // Per 16 tokens: TMEM -> registers, the values of the warp's 32 rows are
     // transposed through shared memory so that each token's 32 outputs leave
     // in 16-byte stores.
-    const int r = 32 * warp + lane;  // row of A0/A1 = TMEM lane
-    const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
-    uint8_t* stg = sEpi + warp * TC_EPI_BYTES;
+    // Two warps per TMEM lane quarter lq (warps lq and TC_EPI_WARP2 + lq)
+    // take alternate groups of 16 tokens.
+    const int lq = warp & 3, par = warp < 4 ? 0 : 1;
+    const uint32_t tq = tmem + ((uint32_t)(32 * lq) << 16);
+    uint8_t* stg = sEpi + (4 * par + lq) * TC_EPI_BYTES;
     int it = 0;
     for (int wi = blockIdx.x; wi < total; wi += gridDim.x, ++it) {
       // warp-uniform outcome: the TMEM loads below are warp-collective
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       const int blk = wi % NB;
       const int pos0 = g.offsets[ch.e] + ch.c0;
 #pragma unroll 1
-      for (int c = 0; c < ch.n; c += 16) {
+      for (int c = 16 * par; c < ch.n; c += 32) {
         uint32_t a[16], b[16];
         tc::tmem_ld16x2(tq + c, tq + TC_D1_COL + c, a, b);
         if (GATEUP) {
@@ -285,10 +295,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
             st16[i * 32 + col] = __float2bfloat16_rn(silu_mul_tanh(__uint_as_float(a[i]), __uint_as_float(b[i])));
           __syncwarp();
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int id = lane + 32 * q, i = id >> 2, part = id & 3;
+          for (int j = 0; j < 2; ++j) {
+            const int id = lane + 32 * j, i = id >> 2, part = id & 3;
             if (c + i < ch.n)
-              *reinterpret_cast<uint4*>(g.hout + (size_t)(pos0 + c + i) * g.F + blk * 128 + 32 * warp + 8 * part) =
+              *reinterpret_cast<uint4*>(g.hout + (size_t)(pos0 + c + i) * g.F + blk * 128 + 32 * lq + 8 * part) =
                   reinterpret_cast<const uint4*>(stg)[id];
           }
           __syncwarp();
@@ -296,15 +306,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const uint32_t* v = half ? b : a;
-            const int col0 = blk * 256 + half * 128 + 32 * warp;
+            const int col0 = blk * 256 + half * 128 + 32 * lq;
             if (g.yout_f32 != nullptr) {
               float* s32 = reinterpret_cast<float*>(stg);
 #pragma unroll
               for (int i = 0; i < 16; ++i) s32[i * 32 + lane] = __uint_as_float(v[i]);
               __syncwarp();
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int id = lane + 32 * q, i = id >> 3, part = id & 7;
+              for (int j = 0; j < 4; ++j) {
+                const int id = lane + 32 * j, i = id >> 3, part = id & 7;
                 const int t = c + i;
                 if (t < ch.n)
                   *reinterpret_cast<uint4*>(g.yout_f32 + (size_t)(pos0 + t) * g.H + col0 + 4 * part) =
@@ -316,8 +326,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
               for (int i = 0; i < 16; ++i) s16[i * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[i]));
               __syncwarp();
 #pragma unroll
-              for (int q = 0; q < 2; ++q) {
-                const int id = lane + 32 * q, i = id >> 2, part = id & 3;
+              for (int j = 0; j < 2; ++j) {
+                const int id = lane + 32 * j, i = id >> 2, part = id & 3;
                 const int t = c + i;
                 if (t < ch.n)
                   *reinterpret_cast<uint4*>(g.yout + (size_t)(pos0 + t) * g.H + col0 + 8 * part) =
