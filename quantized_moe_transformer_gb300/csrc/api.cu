@@ -518,7 +518,8 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     D.w = ws_w;
     D.route = reinterpret_cast<int32_t*>(base + L.route);
     D.status = status;
-    e = staged(QMOE_STAGE_DECODE, 3, st, [&] { return launch_decode(D, st); });
+    // router, routing, gate/up, down+combine
+    e = staged(QMOE_STAGE_DECODE, 4, st, [&] { return launch_decode(D, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
     g_last_path = QMOE_PATH_DECODE;
     return QMOE_OK;
