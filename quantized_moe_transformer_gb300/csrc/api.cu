@@ -87,7 +87,7 @@ inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace carve-up (every piece 256-byte aligned).
 struct MoeWs {
-  size_t part, ids, w, route, offsets, perm, inv, active, n_active, chunk, chunks, n_chunks, xb, h, y, total;
+  size_t part, wr3, ids, w, route, offsets, perm, inv, active, n_active, chunk, chunks, n_chunks, xb, h, y, total;
   int nsplit;
 };
 
@@ -98,6 +98,7 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   size_t o = 0;
   const int parts = L.nsplit > 4 ? L.nsplit : 4;  // the decode router writes 4 partials
   L.part = o;     o += up256(sizeof(float) * (size_t)parts * T * E);
+  L.wr3 = o;      o += up256(router_tc_ws_bytes(T, H, E));  // tensor-core router's Wr parts
   L.ids = o;      o += up256(sizeof(int32_t) * P);
   L.w = o;        o += up256(sizeof(float) * P);
   L.route = o;    o += up256(sizeof(int32_t) * (P + 1));
@@ -407,7 +408,7 @@ void qmoe_set_decode_max_rows(int rows) {
 size_t qmoe_moe_route_workspace_bytes(int T, int H, int E, int k) {
   (void)k;
   if (T <= 0 || H <= 0 || E <= 0) return 0;
-  return up256(sizeof(float) * (size_t)router_splits(T, H, E) * T * E);
+  return up256(sizeof(float) * (size_t)router_splits(T, H, E) * T * E) + up256(router_tc_ws_bytes(T, H, E));
 }
 
 int qmoe_moe_route(const float* X, const float* Wr, int T, int H, int E, int k, int32_t* ids,
@@ -423,9 +424,10 @@ int qmoe_moe_route(const float* X, const float* Wr, int T, int H, int E, int k, 
   if (r != QMOE_OK) return r;
   const int ns = router_splits(T, H, E);
   float* part = static_cast<float*>(ws);
+  void* wr3 = static_cast<char*>(ws) + up256(sizeof(float) * (size_t)ns * T * E);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = staged(QMOE_STAGE_ROUTER, 1, st,
-                         [&] { return launch_router_logits(X, Wr, part, T, H, E, ns, st); });
+  cudaError_t e = staged(QMOE_STAGE_ROUTER, router_launches(T, H, E), st,
+                         [&] { return launch_router_logits(X, Wr, part, T, H, E, ns, wr3, status, st); });
   if (e == cudaSuccess)
     e = staged(QMOE_STAGE_ROUTE, 1, st, [&] { return launch_topk(part, ns, T, E, k, ids, w, st); });
   return launch_status(e);
@@ -526,8 +528,9 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
   }
   const bool small = P <= 2048;
   if (ids == nullptr) {
-    e = staged(QMOE_STAGE_ROUTER, 1, st,
-               [&] { return launch_router_logits(X, d->Wr, part, T, H, E, L.nsplit, st); });
+    e = staged(QMOE_STAGE_ROUTER, router_launches(T, H, E), st, [&] {
+      return launch_router_logits(X, d->Wr, part, T, H, E, L.nsplit, base + L.wr3, status, st);
+    });
     if (e == cudaSuccess) {
       if (small) {
         // top-k over many CTAs, then the permutation in one

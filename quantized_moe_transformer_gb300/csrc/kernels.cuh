@@ -7,8 +7,17 @@ namespace qmoe {
 
 // router.cu
 int router_splits(int T, int H, int E);
+// ``wr3``: scratch of router_tc_ws_bytes(T, H, E) bytes, used (with ``status``)
+// by the tensor-core router when router_tc_eligible(T, H, E)
 cudaError_t launch_router_logits(const float* X, const float* Wr, float* part, int T, int H, int E,
-                                 int nsplit, cudaStream_t st);
+                                 int nsplit, void* wr3, int* status, cudaStream_t st);
+int router_launches(int T, int H, int E);
+// router_tc.cu
+bool router_tc_eligible(int T, int H, int E);
+int router_tc_splits(int T, int H, int E);
+size_t router_tc_ws_bytes(int T, int H, int E);
+cudaError_t launch_router_tc(const float* X, const float* Wr, float* part, int T, int H, int E, int nsplit,
+                             void* wr3, int* status, cudaStream_t st);
 cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k, int32_t* ids, float* w,
                         cudaStream_t st);
 size_t route_small_smem(int T, int E, int k);

@@ -129,16 +129,6 @@ __device__ __forceinline__ Chunk chunk_at(const int2* chunks, int i) {
   return {c.x, c.y & 0xFFFFFF, (c.y >> 24) + 1};
 }
 
-// 2-D tensor copy of the box at (x, y) into shared memory, completing its
-// bytes on ``bar``.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          tc::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
-      : "memory");
-}
-
 // K order inside every group of 8 consecutive K values of the tensor-core
 // operands: element e of a group holds K offset kPerm8[e],
 //   kPerm8 = {0, 4, 1, 5, 2, 6, 3, 7}.
@@ -447,10 +437,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         tc::mbar_expect_tx(&raw_full[slot], 256 * BYTES);
         const int x = sb * BYTES;
         if (GATEUP) {
-          tma_load_2d(dst, e < g.E ? &maps.w : &maps.s, x, y0, &raw_full[slot]);
-          tma_load_2d(dst + 128 * BYTES, e < g.E ? &maps.w2 : &maps.s2, x, y0, &raw_full[slot]);
+          tc::tma_load_2d(dst, e < g.E ? &maps.w : &maps.s, x, y0, &raw_full[slot]);
+          tc::tma_load_2d(dst + 128 * BYTES, e < g.E ? &maps.w2 : &maps.s2, x, y0, &raw_full[slot]);
         } else {
-          tma_load_2d(dst, e < g.E ? &maps.w : &maps.s, x, y0, &raw_full[slot]);
+          tc::tma_load_2d(dst, e < g.E ? &maps.w : &maps.s, x, y0, &raw_full[slot]);
         }
       }
     }
@@ -481,7 +471,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
           tc::mbar_expect_tx(&tok_full[stage], (uint32_t)n32 * 2 * 32 * 128);
           for (int half = 0; half < 2; ++half)
             for (int i = 0; i < n32; ++i)
-              tma_load_2d(b_st + half * TC_B_HALF + i * 4096, &maps.tok, kt * TC_BK + 64 * half, pos0 + 32 * i,
+              tc::tma_load_2d(b_st + half * TC_B_HALF + i * 4096, &maps.tok, kt * TC_BK + 64 * half, pos0 + 32 * i,
                           &tok_full[stage]);
         }
       }

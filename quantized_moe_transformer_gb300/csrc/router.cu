@@ -542,6 +542,7 @@ static bool rows_kernel_fits(int T, int H, int E) {
 
 int router_splits(int T, int H, int E) {
   if (rows_kernel_fits(T, H, E)) return 4;  // one partial per quarter of H
+  if (router_tc_eligible(T, H, E)) return router_tc_splits(T, H, E);
   // enough CTAs to fill the GPU, at most 8 partials per logit (the top-k
   // kernels add them up)
   const bool big = T >= kRouterGemmRows;
@@ -552,8 +553,12 @@ int router_splits(int T, int H, int E) {
   return s;
 }
 
+int router_launches(int T, int H, int E) { return router_tc_eligible(T, H, E) ? 2 : 1; }
+
 cudaError_t launch_router_logits(const float* X, const float* Wr, float* part, int T, int H, int E,
-                                 int nsplit, cudaStream_t st) {
+                                 int nsplit, void* wr3, int* status, cudaStream_t st) {
+  if (router_tc_eligible(T, H, E) && wr3 != nullptr && nsplit == router_tc_splits(T, H, E))
+    return launch_router_tc(X, Wr, part, T, H, E, nsplit, wr3, status, st);
   if (rows_kernel_fits(T, H, E) && nsplit == 4) {
     const int rpt = H / 1024;
     const dim3 grid((E / 8) * 4, (T + rr_rows(rpt) - 1) / rr_rows(rpt));

@@ -3,6 +3,8 @@
 // tcgen05.commit and tcgen05.ld.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace qmoe {
@@ -80,6 +82,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
+}
+
+// 2-D tensor copy of the box at (x, y) of ``map`` into shared memory,
+// completing its bytes on ``bar``.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // Bulk copy global -> shared (contiguous, 16-byte aligned, size % 16 == 0),
