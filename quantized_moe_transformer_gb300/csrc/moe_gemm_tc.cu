@@ -540,13 +540,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
 __global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __restrict__ offsets, int E, int cap,
                                                             int2* __restrict__ chunks,
                                                             int32_t* __restrict__ n_chunks) {
-  extern __shared__ int32_t start[];  // [E+1] exclusive scan of chunk counts
+  extern __shared__ int32_t start[];  // [E+1] chunk counts, then their exclusive scan
   const int lane = threadIdx.x & 31;
+  // the counts first, all loads in flight at once
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) start[e] = (offsets[e + 1] - offsets[e] + cap - 1) / cap;
+  __syncthreads();
   if (threadIdx.x < 32) {
     int run = 0;
     for (int b = 0; b <= E; b += 32) {
       const int e = b + lane;
-      const int c = e <= E ? (offsets[e + 1] - offsets[e] + cap - 1) / cap : 0;
+      const int c = e <= E ? start[e] : 0;
       int incl = c;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {

@@ -442,28 +442,44 @@ __global__ void perm_count_kernel(const int32_t* __restrict__ ids, int P, int E,
 
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_cnt,
                                                          int n_chunks, int T, int E, int k,
-                                                         int has_shared,
+                                                         int has_shared, int staged,
                                                          int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ perm,
                                                          int32_t* __restrict__ active,
                                                          int32_t* __restrict__ n_active) {
-  extern __shared__ int32_t tot[];  // [E+1]
+  extern __shared__ int32_t tot[];  // [E+1], then (staged) [n_chunks][E] counts
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // per expert: exclusive running sum over chunks (in place), total; the
-  // counts are read 8 chunks at a time so that the loads overlap
-  for (int e = tid; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
-      int v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = c0 + i < n_chunks ? chunk_cnt[(size_t)(c0 + i) * E + e] : 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (c0 + i < n_chunks) chunk_cnt[(size_t)(c0 + i) * E + e] = run;
-        run += v[i];
+  int32_t* cs = tot + ((E + 1 + 3) & ~3);
+  if (staged) {
+    // all counts in one coalesced sweep, the scans in shared memory
+    for (int i = tid; i < n_chunks * E; i += blockDim.x) cs[i] = chunk_cnt[i];
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+      int run = 0;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int v = cs[c * E + e];
+        cs[c * E + e] = run;
+        run += v;
       }
+      tot[e] = run;
     }
-    tot[e] = run;
+  } else {
+    // per expert: exclusive running sum over chunks (in place), total; the
+    // counts are read 8 chunks at a time so that the loads overlap
+    for (int e = tid; e < E; e += blockDim.x) {
+      int run = 0;
+      for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = c0 + i < n_chunks ? chunk_cnt[(size_t)(c0 + i) * E + e] : 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (c0 + i < n_chunks) chunk_cnt[(size_t)(c0 + i) * E + e] = run;
+          run += v[i];
+        }
+      }
+      tot[e] = run;
+    }
   }
   if (tid == 0) tot[E] = has_shared ? T : 0;
   __syncthreads();
@@ -496,10 +512,14 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    const int base = offsets[e];
+  if (staged) {
+    for (int i = tid; i < n_chunks * E; i += blockDim.x) chunk_cnt[i] = cs[i] + offsets[i % E];
+  } else {
+    for (int e = tid; e < E; e += blockDim.x) {
+      const int base = offsets[e];
 #pragma unroll 8
-    for (int c = 0; c < n_chunks; ++c) chunk_cnt[(size_t)c * E + e] += base;
+      for (int c = 0; c < n_chunks; ++c) chunk_cnt[(size_t)c * E + e] += base;
+    }
   }
   const int P = T * k;
   if (has_shared)
@@ -514,9 +534,19 @@ __global__ void perm_scatter_kernel(const int32_t* __restrict__ ids, int P, int 
   for (int i = lane; i < E; i += 32) cur[i] = chunk_base[(size_t)c * E + i];
   __syncwarp();
   int p0 = c * PERM_CHUNK, p1 = min(P, p0 + PERM_CHUNK);
-  for (int base = p0; base < p1; base += 32) {
+  // the chunk's expert ids, all loads in flight at once
+  int ev[PERM_CHUNK / 32];
+#pragma unroll
+  for (int i = 0; i < PERM_CHUNK / 32; ++i) {
+    const int p = p0 + 32 * i + lane;
+    ev[i] = p < p1 ? ids[p] : -1;
+  }
+#pragma unroll
+  for (int i = 0; i < PERM_CHUNK / 32; ++i) {
+    const int base = p0 + 32 * i;
+    if (base >= p1) break;
     int p = base + lane;
-    int e = (p < p1) ? ids[p] : -1;
+    int e = ev[i];
     if (p < p1 && (e < 0 || e >= E)) e = 0;  // already recorded by the count pass
     unsigned mask = __match_any_sync(0xffffffffu, e);
     int rank = __popc(mask & ((1u << lane) - 1u));
@@ -628,8 +658,19 @@ cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_s
                               int32_t* active, int32_t* n_active, int* status, cudaStream_t st) {
   const int P = T * k, nc = perm_chunks(P);
   perm_count_kernel<<<nc, 256, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, status);
-  perm_scan_kernel<<<1, 1024, sizeof(int32_t) * (E + 1), st>>>(chunk_cnt, nc, T, E, k, has_shared,
-                                                               offsets, perm, active, n_active);
+  // the scan stages every chunk count in shared memory when they fit
+  const size_t base_smem = sizeof(int32_t) * (size_t)((E + 1 + 3) & ~3);
+  const size_t staged_smem = base_smem + sizeof(int32_t) * (size_t)nc * E;
+  const int staged = staged_smem <= 160 * 1024 ? 1 : 0;
+  const size_t smem = staged ? staged_smem : base_smem;
+  static size_t smem_set = 48 * 1024;
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(perm_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (e != cudaSuccess) return e;
+    smem_set = 160 * 1024;
+  }
+  perm_scan_kernel<<<1, 1024, smem, st>>>(chunk_cnt, nc, T, E, k, has_shared, staged, offsets, perm, active,
+                                          n_active);
   perm_scatter_kernel<<<nc, 32, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, perm);
   return cudaGetLastError();
 }
