@@ -51,6 +51,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.cuh"
 #include "tc.cuh"
@@ -339,25 +340,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     // one weight row, 64 weights per k-tile. A k-tile is stored and its stage
     // released before the next one is dequantised, so that the stage round
     // trip (MMA commit -> producers -> MMA) stays short.
+    // (sp is a compile-time constant in each of the two copies of the body, so
+    // that the sub-block indices, and with them the scale-field extraction,
+    // fold into constants)
     const int pw = warp - 4;
-    const int mat = (pw >> 2) & 1, sp = pw >> 3;
-    const int r = 32 * (pw & 3) + lane;
-    const uint32_t ta0 =
-        tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * (TC_BK / 2) + sp * 32);
-    const uint8_t* my_row = sRaw + (size_t)(mat * 128 + r) * BYTES;
-    const int NU = n_mine * KB;
-    uint32_t wa[16], wb[16];
-    uint4 hdr = make_uint4(0, 0, 0, 0), hq0 = hdr, hq1 = hdr;
-    // loads the super-block header (and Q5_K high bits) of ring slot u % RS
-    auto open_sb = [&](int u) -> bool {
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag))) return false;
-      const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
-      hdr = rp[0];
-      if (QT == QMOE_Q5K) {
-        hq0 = rp[1];
-        hq1 = rp[2];
-      }
-      return true;
+    auto producer = [&](auto sp_c) {
+      constexpr int sp = decltype(sp_c)::value;
+      const int mat = (pw >> 2) & 1;
+      const int r = 32 * (pw & 3) + lane;
+      const uint32_t ta0 =
+          tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * (TC_BK / 2) + sp * 32);
+      const uint8_t* my_row = sRaw + (size_t)(mat * 128 + r) * BYTES;
+      const int NU = n_mine * KB;
+      uint32_t wa[16], wb[16];
+      uint4 hdr = make_uint4(0, 0, 0, 0), hq0 = hdr, hq1 = hdr;
+      // loads the super-block header (and Q5_K high bits) of ring slot u % RS
+      auto open_sb = [&](int u) -> bool {
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag))) return false;
+        const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
+        hdr = rp[0];
+        if (QT == QMOE_Q5K) {
+          hq0 = rp[1];
+          hq1 = rp[2];
+        }
+        return true;
     };
     // sub-blocks 4 hh + 2 sp and + 1 of super-block u
     auto deq = [&](int u, int hh) {
@@ -411,6 +417,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         if (!ok) break;
       }
     }
+    };
+    if ((pw >> 3) == 0)
+      producer(std::integral_constant<int, 0>{});
+    else
+      producer(std::integral_constant<int, 1>{});
   } else if (warp == TC_RAW_WARP) {
     // ------------------------------------------------------------ weight loader
     // One lane: super-block u of the CTA's item sequence goes to ring slot
