@@ -131,6 +131,20 @@ def test_route_entry_point(oracle):
         np.testing.assert_allclose(w.cpu().numpy()[ok], ow[ok], rtol=0, atol=2e-6)
 
 
+@pytest.mark.parametrize("T", [256, 300, 1000])
+@pytest.mark.parametrize("routing", ["uniform", "zipf"])
+def test_route_entry_point_tensor_core_router(oracle, T, routing):
+    """From 256 rows the router runs on the tensor cores (three-part bf16 split,
+    several H slices); row tiles of 128 end ragged at T = 300 and 1000."""
+    arr, lay, k = layer_pair(0, routing=routing)
+    X = inputs.hidden(11 + T, T, 2048, routing=routing)
+    ids, w = qb.moe_route(torch.from_numpy(X).cuda(), lay.Wr, k)
+    torch.cuda.synchronize()
+    oids, ow, gap, logits = oracle.route(X, arr["Wr"], k)
+    ok = check_routes(ids.cpu().numpy(), oids, gap, logits)
+    np.testing.assert_allclose(w.cpu().numpy()[ok], ow[ok], rtol=0, atol=2e-6)
+
+
 def test_caller_supplied_routes(oracle):
     """One routing decision fed to the layer (the synchronised-router case)."""
     arr, lay, k = layer_pair(0)
