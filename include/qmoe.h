@@ -102,6 +102,11 @@ typedef struct {
  * logits: the lower expert index first), in descending-logit slot order, with
  * weights w_s = exp(l_s - l_0) / sum_{j<k} exp(l_j - l_0), which is the
  * softmax over all E renormalised over the selected k.
+ * The logits are fp32-accurate: summed on the CUDA cores, or, from T = 256
+ * rows when E is a multiple of 128 and H of 256, on the bf16 tensor cores with
+ * every fp32 value of X and Wr split exactly into three bf16 parts (six part
+ * products accumulated in fp32, over at least 4 slices of H); the workspace
+ * then also holds Wr's parts, 3 * E * H * 2 bytes.
  * ([CKE-Zip] "What The First Prototype Split": selected top-k indices and
  * routing weights; "What PR #382 Now Splits": one synchronised router decision.)
  *   X [T][H] fp32, Wr [H][E] fp32 -> ids [T][k] int32, w [T][k] fp32.

@@ -111,6 +111,20 @@ def test_route_argument_checks(lib):
     assert lib.qmoe_moe_route(None, None, 1, 2048, 256, 8, None, None, None, 0, None) == -2
 
 
+def test_route_workspace_holds_router_parts(lib):
+    """From 256 rows the router runs on the tensor cores: the workspace holds
+    Wr's three bf16 parts and at least 4 slices of partial logits."""
+    T, H, E = 4096, 2048, 256
+    parts = 3 * E * H * 2
+    big = lib.qmoe_moe_route_workspace_bytes(T, H, E, 8)
+    assert big >= parts + 4 * T * E * 4
+    small = lib.qmoe_moe_route_workspace_bytes(64, H, E, 8)
+    assert small < parts
+    # E not a multiple of 128: the CUDA-core router, partial logits only
+    up256 = lambda n: (n + 255) // 256 * 256
+    assert lib.qmoe_moe_route_workspace_bytes(T, H, 200, 8) in {up256(sp * T * 200 * 4) for sp in (1, 2, 4, 8)}
+
+
 def test_threshold_roundtrip(lib):
     old = qb.get_gemm_threshold()
     qb.set_gemm_threshold(77)
