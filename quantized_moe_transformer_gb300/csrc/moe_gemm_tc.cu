@@ -699,7 +699,7 @@ cudaError_t launch_build_chunks(const int32_t* offsets, int E, int cap, int2* ch
 }
 
 // cuTensorMapEncodeTiled, taken from the driver through the runtime once.
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -739,7 +739,7 @@ static bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_
       return true;
     }
   }
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {row_bytes, rows};
   const cuuint64_t strides[1] = {row_bytes};
@@ -803,7 +803,7 @@ static bool encode_tokens(CUtensorMap* m, const void* base, uint64_t rows, uint6
       *m = cache[i].map;
       return true;
     }
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {K, rows};
   const cuuint64_t strides[1] = {K * 2};

@@ -4,10 +4,16 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 
 namespace qmoe {
+
+// cuTensorMapEncodeTiled from the driver, looked up once (null if the driver
+// does not provide it); defined in moe_gemm_tc.cu.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 namespace tc {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
