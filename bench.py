@@ -254,6 +254,23 @@ def block_moe_ws_offset(qb, blk, T, pos0):
     return a + 2 * row
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's timed-region milliseconds (every rank gets it)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(rows_per_step, steps, world, ms):
+    """Whole-job rows per second: every rank runs its own replica of the
+    workload (rows_per_step rows per step), timed by the slowest rank."""
+    return rows_per_step * steps * world / (ms / 1e3)
+
+
 def source_sha(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -352,13 +369,10 @@ def ours_main(args, rank, world, local_rank):
             singles[i].replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, device)
     if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
-    value = T * args.steps * world / (ms / 1e3)
+    value = job_throughput(T, args.steps, world, ms)
 
     # dominant kernel, timed per launch with events the library records on the
     # launching stream: the decode path's chained kernels as one unit, else the

@@ -1,0 +1,59 @@
+"""The multi-rank host logic of bench.py on CPU: two gloo ranks, each timing its
+own replica; the job's time is the slowest rank's and its throughput counts
+every rank's rows. The reference arm prints from rank 0 only."""
+
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = 10.0 + 5.0 * rank                  # rank 1 is the slow one
+        got = bench.max_over_ranks(ms, world, torch.device("cpu"))
+        dist.barrier()
+        out[rank] = (got, bench.job_throughput(4, 100, world, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0][0] == res[1][0] == 15.0
+    # 4 rows x 100 steps on each of 2 ranks in 15 ms
+    assert res[0][1] == pytest.approx(4 * 100 * 2 / 0.015)
+
+
+def test_single_rank_needs_no_process_group():
+    assert bench.max_over_ranks(12.5, 1, None) == 12.5
+    assert bench.job_throughput(1, 1000, 1, 23.4) == pytest.approx(1000 / 0.0234)
+
+
+def test_reference_arm_prints_from_rank_zero_only(capsys):
+    class A:  # the fields reference_main reads
+        workload, steps, warmup, gpus = "decode", 1, 0, 2
+    bench.reference_main(A, rank=1, world=2)
+    assert capsys.readouterr().out == ""
