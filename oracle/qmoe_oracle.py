@@ -31,6 +31,9 @@ taken here are:
   2b low nibble, 2b+1 high nibble). Q5_K (176 B): the same header, 32 bytes of
   high bits (bit i = weight i), then the nibbles. Weight i of sub-block
   j = i // 32 is d*s_j*q_i - dmin*m_j with q_i = nibble (+16*high bit for Q5_K).
+* Q6_K super-block (210 B; no GPU kernel takes it yet): fp16 d, sixteen signed
+  8-bit scales (16 weights each), 64 bytes of 2-bit high parts, 128 bytes of
+  low nibbles; w_i = d*s_{i//16}*(q_i - 32), q_i = nibble + 16*high part.
 * Routing: logits l = x Wr; the k experts with the largest logits (ties to the
   lower index), in descending-logit slot order, with weights softmax over the
   whole row renormalised over the selected k, which equals
@@ -56,6 +59,7 @@ QK = 256
 SUB = 32
 Q4K_BYTES = 144
 Q5K_BYTES = 176
+Q6K_BYTES = 210
 
 
 # --------------------------------------------------------------------------
@@ -108,13 +112,34 @@ def dequant_q5k(blocks: np.ndarray) -> np.ndarray:
     return _apply_scales(q, d, dmin, s, m)
 
 
+def dequant_q6k(blocks: np.ndarray) -> np.ndarray:
+    """[..., 210] uint8 -> [..., 256] float64.
+
+    Q6_K, the format a Q4_K_M model file ([CKE-Zip], opening paragraphs: "a
+    real Qwen3.5-35B-A3B Q4_K_M prefill") keeps some of its tensors in. The
+    pages print no layout; the library's own reading: fp16 d, sixteen signed
+    8-bit sub-block scales s_0..s_15 (16 weights each), 64 bytes of 2-bit high
+    parts (weight i: bits 2(i % 4), 2(i % 4) + 1 of byte i // 4), 128 bytes of
+    low nibbles (byte b: weight 2b low, 2b+1 high); q_i = low + 16 * high in
+    0..63 and w_i = d * s_{i // 16} * (q_i - 32). No min, no second scale."""
+    assert blocks.shape[-1] == Q6K_BYTES and blocks.dtype == np.uint8
+    d = np.ascontiguousarray(blocks[..., 0:2]).view(np.float16)[..., 0].astype(np.float64)
+    s = np.ascontiguousarray(blocks[..., 2:18]).view(np.int8).astype(np.int64)
+    hb = blocks[..., 18:82]
+    high = np.stack([(hb >> (2 * r)) & 3 for r in range(4)], axis=-1)
+    high = high.reshape(*hb.shape[:-1], QK).astype(np.int64)
+    q = _nibbles(blocks[..., 82:210]) + 16 * high
+    j = np.arange(QK) // 16                        # sub-block of each weight
+    return d[..., None] * s[..., j].astype(np.float64) * (q - 32).astype(np.float64)
+
+
 def dequant_matrix(W: np.ndarray) -> np.ndarray:
     """Packed [..., rows, n_blocks, bytes] -> dense [..., rows, n_blocks*256].
 
     Row r of the result is output feature r; its columns run along the input
     axis, which is the axis the super-blocks cover."""
     nb = W.shape[-1]
-    dense = dequant_q4k(W) if nb == Q4K_BYTES else dequant_q5k(W)
+    dense = {Q4K_BYTES: dequant_q4k, Q5K_BYTES: dequant_q5k, Q6K_BYTES: dequant_q6k}[nb](W)
     return dense.reshape(*W.shape[:-2], W.shape[-2] * QK)
 
 

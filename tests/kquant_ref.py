@@ -86,6 +86,41 @@ def decode(blocks: np.ndarray) -> np.ndarray:
     return d[..., None] * s * q - dmin[..., None] * m
 
 
+def encode_q6k(d, s, q) -> np.ndarray:
+    """Q6_K super-block (210 B) from d, sixteen signed scales and 256 quants
+    in 0..63, packed with Python integers."""
+    assert len(s) == 16 and all(-128 <= v < 128 for v in s)
+    assert len(q) == 256 and all(0 <= v < 64 for v in q)
+    scales = bytes(int(v) & 0xFF for v in s)
+    high = 0
+    for i in range(256):
+        high |= (int(q[i]) >> 4) << (2 * i)
+    low = bytes((int(q[2 * b]) & 15) | ((int(q[2 * b + 1]) & 15) << 4) for b in range(128))
+    raw = np.float16(d).tobytes() + scales + high.to_bytes(64, "little") + low
+    return np.frombuffer(raw, dtype=np.uint8).copy()
+
+
+def expected_weights_q6k(d, s, q) -> np.ndarray:
+    """w_i = d * s_{i // 16} * (q_i - 32), from the fields."""
+    d64 = float(np.float16(d))
+    return np.array([d64 * s[i // 16] * (q[i] - 32) for i in range(256)])
+
+
+def decode_q6k(blocks: np.ndarray) -> np.ndarray:
+    """[..., 210] uint8 -> [..., 256] float64 (second implementation: the
+    high parts read as eight little-endian 64-bit words)."""
+    d = blocks[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    sc = blocks[..., 2:18].astype(np.int64)
+    sc = np.where(sc >= 128, sc - 256, sc)
+    words = [_le_u64(blocks[..., 18 + 8 * w:26 + 8 * w]) for w in range(8)]
+    i = np.arange(256)
+    high = np.stack([(words[n // 32] >> np.uint64(2 * (n % 32))) & np.uint64(3) for n in range(256)],
+                    axis=-1).astype(np.int64)
+    low = (blocks[..., 82 + i // 2].astype(np.int64) >> (4 * (i % 2))) & 15
+    q = low + 16 * high
+    return d[..., None] * sc[..., i // 16] * (q - 32)
+
+
 def dense(W: np.ndarray) -> np.ndarray:
     """[..., rows, nblk, bytes] -> [..., rows, nblk*256] via ``decode``."""
     v = decode(W)

@@ -102,6 +102,63 @@ def test_dequant_matches_second_decoder(oracle):
         assert np.array_equal(fn(blocks), kq.decode(blocks))
 
 
+# Q6_K (the format a Q4_K_M file keeps some tensors in; no GPU kernel takes it
+# yet): the oracle's reading of the library's layout, pinned the same way.
+
+def test_q6k_hand_block(oracle):
+    s = [j - 8 for j in range(16)]
+    q = [i % 64 for i in range(256)]
+    w = oracle.dequant_q6k(kq.encode_q6k(0.5, s, q))
+    for idx, val in _golden("q6k_hand_block.txt"):
+        assert w[int(idx)] == float(val), idx
+    assert np.array_equal(w, kq.expected_weights_q6k(0.5, s, q))
+
+
+def test_q6k_zero_and_midpoint(oracle):
+    assert np.all(oracle.dequant_q6k(np.zeros(210, np.uint8)) == 0.0)
+    # q = 32 is the zero of every sub-block, whatever d and the scales
+    blk = kq.encode_q6k(3.0, [127, -128] * 8, [32] * 256)
+    assert np.all(oracle.dequant_q6k(blk) == 0.0)
+
+
+@pytest.mark.parametrize("d", [65504.0, 2.0**-14, -1.5])
+def test_q6k_scale_extremes(oracle, d):
+    s = [127, -128, 1, -1] * 4
+    q = [0, 63, 31, 33] * 64
+    blk = kq.encode_q6k(d, s, q)
+    assert np.array_equal(oracle.dequant_q6k(blk), kq.expected_weights_q6k(d, s, q))
+
+
+def test_q6k_quant_bit_and_scale_walk(oracle):
+    """Every one of the 6 quant bits of every weight alone (the others at the
+    zero point 32), and every sub-block scale alone."""
+    for i in range(256):
+        for b in range(6):
+            q = [32] * 256
+            q[i] = 1 << b
+            w = oracle.dequant_q6k(kq.encode_q6k(1.0, [1] * 16, q))
+            exp = np.zeros(256)
+            exp[i] = (1 << b) - 32
+            assert np.array_equal(w, exp), (i, b)
+    for j in range(16):
+        s = [0] * 16
+        s[j] = -3
+        w = oracle.dequant_q6k(kq.encode_q6k(1.0, s, [33] * 256)).reshape(16, 16)
+        exp = np.zeros((16, 16))
+        exp[j, :] = -3.0
+        assert np.array_equal(w, exp), j
+
+
+def test_q6k_matches_second_decoder(oracle):
+    rng = np.random.default_rng(66)
+    blocks = rng.integers(0, 256, (64, 3, 210), dtype=np.uint8)
+    blocks[..., 1] &= 0x3B  # keep d a finite fp16
+    assert np.array_equal(oracle.dequant_q6k(blocks), kq.decode_q6k(blocks))
+    dense = oracle.dequant_matrix(blocks)
+    assert dense.shape == (64, 3 * 256)
+    assert np.array_equal(dense, kq.decode_q6k(blocks).reshape(64, 768))
+
+
 def test_generator_ranges(oracle):
     blocks = inputs.packed_blocks(inputs.generator(0, "Wg"), (4096,), "q4k")
     d = blocks[:, 0:2].copy().view(np.float16).astype(np.float64)
