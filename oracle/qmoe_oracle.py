@@ -34,6 +34,8 @@ taken here are:
 * Q6_K super-block (210 B; no GPU kernel takes it yet): fp16 d, sixteen signed
   8-bit scales (16 weights each), 64 bytes of 2-bit high parts, 128 bytes of
   low nibbles; w_i = d*s_{i//16}*(q_i - 32), q_i = nibble + 16*high part.
+* MXFP4 super-block (136 B; no GPU kernel yet): eight E8M0 scales for the
+  32-weight blocks, 128 bytes of FP4 E2M1 codes; w_i = 2^(e - 127) * E2M1.
 * Routing: logits l = x Wr; the k experts with the largest logits (ties to the
   lower index), in descending-logit slot order, with weights softmax over the
   whole row renormalised over the selected k, which equals
@@ -60,6 +62,7 @@ SUB = 32
 Q4K_BYTES = 144
 Q5K_BYTES = 176
 Q6K_BYTES = 210
+MXFP4_BYTES = 136
 
 
 # --------------------------------------------------------------------------
@@ -133,13 +136,40 @@ def dequant_q6k(blocks: np.ndarray) -> np.ndarray:
     return d[..., None] * s[..., j].astype(np.float64) * (q - 32).astype(np.float64)
 
 
+# FP4 E2M1 (sign, 2 exponent bits with bias 1, 1 mantissa bit; exponent 0 is
+# subnormal): the value of each 4-bit code
+_E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                  -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+
+def dequant_mxfp4(blocks: np.ndarray) -> np.ndarray:
+    """[..., 136] uint8 -> [..., 256] float64.
+
+    The MXFP4-class format that "Distributed CPU: Zip Fusion Beyond Tensor
+    Parallelism", section "Decode vs Prefill: Same Weights, Different
+    Bottlenecks", names for the packed weights of the model class it targets,
+    with the element and scale types of the OCP microscaling format (blocks of
+    32 FP4 E2M1 values sharing one E8M0 scale), in the library's own
+    256-weight super-block: eight E8M0 scales
+    (one per 32 weights, value 2^(e - 127), e = 255 is NaN), then 128 bytes of
+    FP4 E2M1 codes (byte b: weight 2b low nibble, 2b+1 high);
+    w_i = 2^(e_{i//32} - 127) * E2M1(code_i)."""
+    assert blocks.shape[-1] == MXFP4_BYTES and blocks.dtype == np.uint8
+    e = blocks[..., 0:8].astype(np.int64)
+    scale = np.where(e == 255, np.nan, np.ldexp(1.0, e - 127))
+    codes = _nibbles(blocks[..., 8:136])
+    j = np.arange(QK) // 32
+    return scale[..., j] * _E2M1[codes]
+
+
 def dequant_matrix(W: np.ndarray) -> np.ndarray:
     """Packed [..., rows, n_blocks, bytes] -> dense [..., rows, n_blocks*256].
 
     Row r of the result is output feature r; its columns run along the input
     axis, which is the axis the super-blocks cover."""
     nb = W.shape[-1]
-    dense = {Q4K_BYTES: dequant_q4k, Q5K_BYTES: dequant_q5k, Q6K_BYTES: dequant_q6k}[nb](W)
+    dense = {Q4K_BYTES: dequant_q4k, Q5K_BYTES: dequant_q5k, Q6K_BYTES: dequant_q6k,
+             MXFP4_BYTES: dequant_mxfp4}[nb](W)
     return dense.reshape(*W.shape[:-2], W.shape[-2] * QK)
 
 

@@ -121,6 +121,37 @@ def decode_q6k(blocks: np.ndarray) -> np.ndarray:
     return d[..., None] * sc[..., i // 16] * (q - 32)
 
 
+def encode_mxfp4(e, codes) -> np.ndarray:
+    """MXFP4 super-block (136 B) from eight E8M0 exponents and 256 4-bit codes."""
+    assert len(e) == 8 and all(0 <= v < 256 for v in e)
+    assert len(codes) == 256 and all(0 <= c < 16 for c in codes)
+    nib = bytes(int(codes[2 * b]) | (int(codes[2 * b + 1]) << 4) for b in range(128))
+    return np.frombuffer(bytes(int(v) for v in e) + nib, dtype=np.uint8).copy()
+
+
+def e2m1_value(code: int) -> float:
+    """FP4 E2M1 from its definition: sign, exponent (2 bits, bias 1), mantissa
+    (1 bit); exponent 0 is subnormal (0.m * 2^0)."""
+    sign = -1.0 if code & 8 else 1.0
+    ex, man = (code >> 1) & 3, code & 1
+    mag = man * 0.5 if ex == 0 else (1.0 + 0.5 * man) * 2.0 ** (ex - 1)
+    return sign * mag
+
+
+def decode_mxfp4(blocks: np.ndarray) -> np.ndarray:
+    """[..., 136] uint8 -> [..., 256] float64 (second implementation, from the
+    bit-level definition of E2M1 and E8M0)."""
+    out = np.empty(blocks.shape[:-1] + (256,))
+    flat_b = blocks.reshape(-1, 136)
+    flat_o = out.reshape(-1, 256)
+    for r in range(flat_b.shape[0]):
+        for i in range(256):
+            e = int(flat_b[r, i // 32])
+            code = (int(flat_b[r, 8 + i // 2]) >> (4 * (i % 2))) & 15
+            flat_o[r, i] = float("nan") if e == 255 else e2m1_value(code) * 2.0 ** (e - 127)
+    return out
+
+
 def dense(W: np.ndarray) -> np.ndarray:
     """[..., rows, nblk, bytes] -> [..., rows, nblk*256] via ``decode``."""
     v = decode(W)

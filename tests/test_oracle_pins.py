@@ -159,6 +159,35 @@ def test_q6k_matches_second_decoder(oracle):
     assert np.array_equal(dense, kq.decode_q6k(blocks).reshape(64, 768))
 
 
+# MXFP4 (the MXFP4-class format the pages name for the target model class; no
+# GPU kernel takes it yet)
+
+def test_mxfp4_code_table(oracle):
+    """All 16 E2M1 codes at scale 1 (e = 127): the format's value table."""
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    codes = [i % 16 for i in range(256)]
+    w = oracle.dequant_mxfp4(kq.encode_mxfp4([127] * 8, codes))
+    assert np.array_equal(w, np.array([table[c] for c in codes]))
+    assert all(kq.e2m1_value(c) == table[c] for c in range(16))
+
+
+def test_mxfp4_scale_walk(oracle):
+    """Every E8M0 exponent 0..254 is 2^(e - 127) exactly; 255 is NaN."""
+    for e in list(range(0, 255, 7)) + [254, 127, 0]:
+        w = oracle.dequant_mxfp4(kq.encode_mxfp4([e] + [127] * 7, [2] * 256))  # code 2 = 1.0
+        assert np.all(w[:32] == 2.0 ** (e - 127)) and np.all(w[32:] == 1.0), e
+    w = oracle.dequant_mxfp4(kq.encode_mxfp4([127, 255] + [127] * 6, [2] * 256))
+    assert np.all(np.isnan(w[32:64])) and np.all(w[:32] == 1.0) and np.all(w[64:] == 1.0)
+
+
+def test_mxfp4_matches_second_decoder(oracle):
+    rng = np.random.default_rng(77)
+    blocks = rng.integers(0, 256, (16, 2, 136), dtype=np.uint8)
+    blocks[..., 0:8] = rng.integers(100, 150, (16, 2, 8), dtype=np.uint8)
+    assert np.array_equal(oracle.dequant_mxfp4(blocks), kq.decode_mxfp4(blocks))
+    assert oracle.dequant_matrix(blocks).shape == (16, 512)
+
+
 def test_generator_ranges(oracle):
     blocks = inputs.packed_blocks(inputs.generator(0, "Wg"), (4096,), "q4k")
     d = blocks[:, 0:2].copy().view(np.float16).astype(np.float64)
