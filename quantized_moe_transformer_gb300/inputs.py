@@ -35,7 +35,7 @@ import numpy as np
 Q4K_BYTES = 144
 Q5K_BYTES = 176
 QK = 256  # weights per super-block
-QTYPE_BYTES = {"q4k": Q4K_BYTES, "q5k": Q5K_BYTES}
+QTYPE_BYTES = {"q4k": Q4K_BYTES, "q5k": Q5K_BYTES, "q6k": 210, "mxfp4": 136}
 
 # distinct streams per tensor so that changing one shape leaves the others alone
 _STREAM = {
@@ -52,13 +52,24 @@ def generator(seed: int, name: str) -> np.random.Generator:
 def packed_blocks(rng: np.random.Generator, shape: tuple, qtype: str) -> np.ndarray:
     """Uniform random super-blocks of ``qtype`` with ``shape`` = (..., n_blocks).
 
-    Returns uint8 with a trailing byte axis of 144 (q4k) or 176 (q5k)."""
+    Returns uint8 with a trailing byte axis of 144 (q4k), 176 (q5k), 210 (q6k)
+    or 136 (mxfp4). Every byte is uniform except the scales: fp16 d and dmin in
+    [2^-12, 2^-10] (q4k, q5k), fp16 d in [2^-14, 2^-12] (q6k, whose signed
+    8-bit scales and centred 6-bit quants span about 64 times the range of a
+    Q4_K field pair), E8M0 exponents 119..124 (mxfp4: block scales 2^-8..2^-3);
+    all four then give weights of similar size."""
     nb = QTYPE_BYTES[qtype]
     count = int(np.prod(shape, dtype=np.int64))
     raw = np.frombuffer(rng.bytes(count * nb), dtype=np.uint8).copy()
     raw = raw.reshape(count, nb)
-    scales = rng.uniform(2.0**-12, 2.0**-10, size=(count, 2)).astype(np.float16)
-    raw[:, 0:4] = scales.view(np.uint8).reshape(count, 4)
+    if qtype in ("q4k", "q5k"):
+        scales = rng.uniform(2.0**-12, 2.0**-10, size=(count, 2)).astype(np.float16)
+        raw[:, 0:4] = scales.view(np.uint8).reshape(count, 4)
+    elif qtype == "q6k":
+        d = rng.uniform(2.0**-14, 2.0**-12, size=(count, 1)).astype(np.float16)
+        raw[:, 0:2] = d.view(np.uint8).reshape(count, 2)
+    else:
+        raw[:, 0:8] = rng.integers(119, 125, size=(count, 8), dtype=np.uint8)
     return raw.reshape(*shape, nb)
 
 

@@ -194,6 +194,12 @@ def test_generator_ranges(oracle):
     assert d.min() >= 2.0**-12 and d.max() <= 2.0**-10
     w = oracle.dequant_q4k(blocks)
     assert np.isfinite(w).all()
+    # the formats without a kernel yet: finite, and weights of the same size
+    ref = np.abs(w).max()
+    for qt, fn in (("q6k", oracle.dequant_q6k), ("mxfp4", oracle.dequant_mxfp4)):
+        wq = fn(inputs.packed_blocks(inputs.generator(0, "Wg"), (4096,), qt))
+        assert np.isfinite(wq).all()
+        assert ref / 4 < np.abs(wq).max() < 4 * ref, qt
 
 
 # ------------------------------------------------------------------ router
