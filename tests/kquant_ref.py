@@ -153,6 +153,8 @@ def decode_mxfp4(blocks: np.ndarray) -> np.ndarray:
 
 
 def dense(W: np.ndarray) -> np.ndarray:
-    """[..., rows, nblk, bytes] -> [..., rows, nblk*256] via ``decode``."""
-    v = decode(W)
+    """[..., rows, nblk, bytes] -> [..., rows, nblk*256] via this module's
+    decoders (``decode`` for Q4_K/Q5_K, ``decode_q6k``, ``decode_mxfp4``)."""
+    nb = W.shape[-1]
+    v = decode_q6k(W) if nb == 210 else (decode_mxfp4(W) if nb == 136 else decode(W))
     return v.reshape(*W.shape[:-2], W.shape[-2] * 256)

@@ -280,7 +280,8 @@ def _brute_moe(X, layer, k, R=None, f_half=None):
     return out
 
 
-@pytest.mark.parametrize("shared,down,routing", [(False, "q4k", "uniform"), (True, "q5k", "uniform"),
+@pytest.mark.parametrize("shared,down,routing", [(True, "q6k", "uniform"), (False, "mxfp4", "uniform"),
+                                                  (False, "q4k", "uniform"), (True, "q5k", "uniform"),
                                                  (True, "q5k", "zipf")])
 def test_moe_brute_force(oracle, shared, down, routing):
     layer = inputs.moe_layer(3, 256, 8, 256, shared=shared, down_type=down, routing=routing)
