@@ -464,3 +464,94 @@ def test_block_rows_restriction(oracle):
     rows = np.array([0, 4, 6])
     part, _ = oracle.block_forward_rows(X, blk, 2, 3, kc.copy(), vc.copy(), rows)
     assert np.max(np.abs(part - full[rows])) <= 1e-12 * np.max(np.abs(full))
+
+
+# ------------------------------------------------------------------ block composition
+# The block is h1 = X + attn(X), out = h1 + moe(RMSNorm(h1; g2)) ("CKE Zip: From
+# Splitting Tokens To Splitting Qwen3.5 Weights", "What PR #382 Now Splits": attention
+# partials, then the residual, then the router and MoE on the new state, then the
+# residual). Each case below reduces the block to parts pinned above, so that a
+# composition slip fails one of them: the second norm reading X instead of h1, using
+# g1 instead of g2, or either residual dropped.
+
+def _zero_scales(packed):
+    packed[..., 0:4] = 0            # d = dmin = 0: every weight of the matrix is 0
+
+
+def _composition_cases(oracle, blk, X, pos0, rows=None):
+    kc = oracle.bf16_bits_to_f64(blk["k_cache"])
+    vc = oracle.bf16_bits_to_f64(blk["v_cache"])
+    if rows is None:
+        out, _ = oracle.block_forward(X, blk, 2, pos0, kc.copy(), vc.copy())
+        return out, kc, vc
+    out, _ = oracle.block_forward_rows(X, blk, 2, pos0, kc.copy(), vc.copy(), rows)
+    return out, kc, vc
+
+
+@pytest.mark.parametrize("rows", [None, np.array([1, 4, 5])])
+def test_block_zero_attention_is_residual_plus_moe(oracle, rows):
+    """Attention weights all zero: the attention branch is 0, so the block is
+    X + moe(RMSNorm(X; g2)) (with g1 != g2, a norm with g1 fails this)."""
+    blk, X = _small_block(4, T=6, ctx=32)
+    for name in ("Wq", "Wk", "Wv", "Wo"):
+        _zero_scales(blk[name])
+    assert not np.allclose(blk["g1"], blk["g2"])
+    out, _, _ = _composition_cases(oracle, blk, X, 10, rows)
+    sel = np.arange(6) if rows is None else rows
+    exp = X[sel].astype(np.float64) + oracle.moe_forward(
+        oracle.rmsnorm(X[sel], blk["g2"]), blk["moe"], 2)
+    assert np.max(np.abs(out - exp)) <= 1e-12 * np.max(np.abs(exp))
+    wrong = X[sel].astype(np.float64) + oracle.moe_forward(
+        oracle.rmsnorm(X[sel], blk["g1"]), blk["moe"], 2)
+    assert np.max(np.abs(out - wrong)) > 1e-6 * np.max(np.abs(exp))
+
+
+@pytest.mark.parametrize("rows", [None, np.array([0, 5])])
+def test_block_zero_moe_is_residual_plus_attention(oracle, rows):
+    """Every routed and shared expert weight zero: the MoE branch is 0, so the
+    block is X + attn(X)."""
+    blk, X = _small_block(5, T=6, ctx=32)
+    for name in ("Wg", "Wu", "Wd", "Sg", "Su", "Sd"):
+        _zero_scales(blk["moe"][name])
+    out, kc, vc = _composition_cases(oracle, blk, X, 10, rows)
+    a = oracle.attn_sublayer(X, blk, 10, kc.copy(), vc.copy(), rows=rows)
+    sel = np.arange(6) if rows is None else rows
+    exp = X[sel].astype(np.float64) + a
+    assert np.max(np.abs(out - exp)) <= 1e-12 * np.max(np.abs(exp))
+    assert np.max(np.abs(a)) > 1e-3 * np.max(np.abs(X))
+
+
+def _constant_moe(blk, a, b, c):
+    """Every gate weight a, up weight b, down weight c (routed and shared)."""
+    from tests import kquant_ref as kq2
+    moe = blk["moe"]
+    for name, val in (("Wg", a), ("Wu", b), ("Sg", a), ("Su", b)):
+        moe[name][...] = kq2.encode_q4k(val, 0.0, [1] * 8, [0] * 8, [1] * 256)
+    for name in ("Wd", "Sd"):
+        moe[name][...] = kq2.encode_q5k(c, 0.0, [1] * 8, [0] * 8, [1] * 256)
+
+
+@pytest.mark.parametrize("rows", [None, np.array([2, 3])])
+def test_block_second_norm_reads_h1(oracle, rows):
+    """Attention live, every expert with constant weights a (gate), b (up),
+    c (down): each expert maps a row r to c F silu(a S) b S in every output,
+    S = sum_i r_i, and the renormalised weights sum to 1, so with the shared
+    expert the block is h1 + 2 c F silu(a S) b S with S summed over
+    RMSNorm(h1; g2), h1 = X + attn(X). Norming X instead of h1 fails this."""
+    blk, X = _small_block(6, T=6, ctx=32)
+    a, b, c = 2.0**-4, 2.0**-4, 2.0**-6
+    _constant_moe(blk, a, b, c)
+    F = blk["moe"]["F"]
+    out, kc, vc = _composition_cases(oracle, blk, X, 10, rows)
+    att = oracle.attn_sublayer(X, blk, 10, kc.copy(), vc.copy(), rows=rows)
+    sel = np.arange(6) if rows is None else rows
+    h1 = X[sel].astype(np.float64) + att
+
+    def closed(state):
+        S = oracle.rmsnorm(state, blk["g2"]).sum(axis=1, keepdims=True)
+        return 2.0 * c * F * (a * S) / (1.0 + np.exp(-a * S)) * (b * S)
+
+    exp = h1 + closed(h1)
+    assert np.max(np.abs(out - exp)) <= 1e-12 * np.max(np.abs(exp))
+    wrong = h1 + closed(X[sel].astype(np.float64))
+    assert np.max(np.abs(out - wrong)) > 1e-6 * np.max(np.abs(exp))
