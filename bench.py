@@ -9,9 +9,14 @@ expert, Q4_K gate/up, Q5_K down, fp32 hidden rows, seeded synthetic weights.
 L2 (129 MB) is defeated with 16 distinct layer instances, rotated step by step,
 7.8 GB in total: the weights one step touches are evicted before that instance
 comes round again. Steps are CUDA-graph replays on one stream, timed with CUDA
-events; the dominant kernel is timed again with per-launch events around its
-own launches on the same stream. ``--impl reference`` times the fp64 CPU oracle
-on a bounded sample of the same workload instead.
+events. The dominant unit is timed inside the graph replay too: on the decode
+path it is the whole layer step (its kernels overlap by design); on the
+tensor-core path the gate/up kernel, between event-record nodes that the
+library places around its launches while the stream is capturing. The default
+run also measures the 64-row batched decode and the 4096-row prefill on the
+same layer instances and adds them to its line (``decode_t64``,
+``prefill_t4096``). ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
 """
 
 from __future__ import annotations
@@ -67,8 +72,10 @@ def parse():
     p.add_argument("--routing", choices=["uniform", "zipf"], default=None)
     p.add_argument("--gemm-threshold", type=int, default=None,
                    help="rows above which the tensor-core path is taken (library default if unset)")
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-seconds", type=float, default=24.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the T=64 and T=4096 points the default decode run adds to its line")
     p.add_argument("--cpu-sample", type=str, default=None, help=argparse.SUPPRESS)
     p.add_argument("--record-traffic", type=str, default=None, metavar="CSV",
                    help="read an ncu --csv log with dram__bytes_read.sum / dram__bytes_write.sum of this "
@@ -91,30 +98,37 @@ def workload_config(name, T, routing, layers):
 # ---------------------------------------------------------------- CPU oracle
 
 def cpu_sample_main(spec: str):
-    """Runs in a child process: times the oracle on ``n`` single-row forwards
-    of layer instance 0 and prints timings and outputs as JSON."""
+    """Runs in a child process: times the oracle on forwards of ``T`` rows of
+    layer instance 0 for about ``seconds`` (at least one forward) and prints
+    timings, row counts and the single-row outputs as JSON."""
     from oracle import qmoe_oracle as oracle
     from quantized_moe_transformer_gb300 import inputs
     cfg = json.loads(spec)
+    T = cfg["T"]
     arr = inputs.moe_layer(0, H, E, F, shared=True, routing=cfg["routing"])
-    X = inputs.hidden(1000, cfg["rows"], H, cfg["routing"])
-    times, outs = [], []
+    X = inputs.hidden(1000, max(64, T), H, cfg["routing"])
+    times, rows, outs = [], [], []
     t_end = time.perf_counter() + cfg["seconds"]
-    for i in range(cfg["rows"]):
+    i = 0
+    while True:
+        x = X[i:i + 1] if T == 1 else X[:T]
         t0 = time.perf_counter()
-        out = oracle.moe_forward(X[i:i + 1], arr, K_TOP)
+        out = oracle.moe_forward(x, arr, K_TOP)
         times.append(time.perf_counter() - t0)
-        outs.append(out[0].tolist())
-        if time.perf_counter() > t_end and i >= 2:
+        rows.append(x.shape[0])
+        if T == 1:
+            outs.append(out[0].tolist())
+        i += 1
+        if T > 1 or time.perf_counter() > t_end or i >= 64:
             break
-    print(json.dumps({"times": times, "outs": outs}))
+    print(json.dumps({"times": times, "rows": rows, "outs": outs}))
 
 
-def run_cpu_sample(routing, rows, seconds, threads=1):
+def run_cpu_sample(routing, T, seconds, threads=1):
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = str(threads)
-    spec = json.dumps({"routing": routing, "rows": rows, "seconds": seconds})
+    spec = json.dumps({"routing": routing, "T": T, "seconds": seconds})
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", spec],
                        capture_output=True, text=True, env=env, cwd=ROOT)
     if r.returncode != 0:
@@ -147,7 +161,8 @@ def reference_main(args, rank, world):
             "config": workload_config(args.workload, wl["T"], wl["routing"], 1),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"one row per step of the {args.workload} workload "
-                                       f"(numpy fp64 oracle, {cores} cores visible)"},
+                                       f"(numpy fp64 oracle, {cores} cores visible)",
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -279,9 +294,210 @@ def source_sha(paths):
     return h.hexdigest()[:16]
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(routing, seconds):
+    """The oracle (numpy fp64) on the host cores: single-row forwards (T=1) and
+    one 64-row forward (T=64), each on one thread and on every core this
+    process may run on. Returns the cpu_baseline record and the T=1 outputs
+    (for the parity spot check)."""
+    cores = len(os.sched_getaffinity(0))
+    points, outs1 = [], None
+    for T in (1, 64):
+        for threads in sorted({1, cores}):
+            res = run_cpu_sample(routing, T, seconds / 4, threads=threads)
+            n_rows = sum(res["rows"])
+            tps = n_rows / sum(res["times"])
+            points.append({"T": T, "threads": threads, "tokens_per_s": tps, "rows": n_rows,
+                           "seconds": sum(res["times"])})
+            if T == 1 and threads == 1:
+                outs1 = res
+    best1 = max(p["tokens_per_s"] for p in points if p["T"] == 1)
+    cores_best = max((p for p in points if p["T"] == 1), key=lambda p: p["tokens_per_s"])["threads"]
+    rec = {"value": best1, "unit": "tokens/s", "cores": cores_best, "kind": "oracle",
+           "sample": "numpy fp64 oracle on layer instance 0: single-row forwards (T=1) for about "
+                     f"{seconds / 4:.0f} s and one 64-row forward (T=64), each on 1 thread and on all "
+                     f"{cores} cores; value = the faster T=1 rate",
+           "cpu_model": cpu_model(), "cores_visible": cores, "points": points}
+    return rec, outs1
+
+
+def make_inputs(torch, NL, T, H_, routing, device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    Xs = torch.randn((NL, T, H_), device=device, generator=g)
+    if routing == "zipf":
+        Xs[:, :, 0] = 1.0
+    return Xs
+
+
+def time_graphs(torch, step, NL, steps, warmup, stream, world, device, clock_index=None):
+    """Captures one graph of NL steps (and one per step for the remainder),
+    replays warmup steps, then times ``steps`` steps with CUDA events on
+    ``stream``. Returns (ms over the timed region, max over ranks; clocks)."""
+    import torch.distributed as dist
+    macro = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(macro, stream=stream):
+        for i in range(NL):
+            step(i, stream)
+    singles = []
+    for i in range(steps % NL):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            step(i, stream)
+        singles.append(gph)
+    for _ in range(max(1, -(-warmup // NL))):
+        macro.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(clock_index) if clock_index is not None else None
+    if clk:
+        clk.__enter__()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps // NL):
+            macro.replay()
+        for gph in singles:
+            gph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if clk:
+        clk.__exit__()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, device)
+    if world > 1:
+        dist.barrier()
+    return ms, (clk.summary if clk else None)
+
+
+def gateup_in_graph_us(torch, qb, step, NL, stream, replays=3):
+    """Average duration of the gate/up kernel inside a graph replay: the
+    library brackets each gate/up launch with events, which stream capture turns
+    into event-record nodes of the graph; after each replay the times of that
+    replay's launches are read back."""
+    with torch.cuda.stream(stream):
+        qb.profile_start("gateup")          # events created outside the capture
+        for i in range(NL):
+            step(i, stream)
+        qb.profile_stop()
+        torch.cuda.synchronize()
+        qb.profile_start("gateup")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(NL):
+                step(i, stream)
+    tot, n = 0.0, 0
+    for _ in range(replays):
+        g.replay()
+        torch.cuda.synchronize()
+        ms, k = qb.profile_read()
+        tot += ms
+        n += k
+    qb.profile_stop()
+    return 1e3 * tot / n, n
+
+
+def distinct_experts(torch, qb, layers, step, ws, ws_off, T, NL, stream):
+    L = layers[0].workspace_layout(T)
+    U = []
+    with torch.cuda.stream(stream):
+        for i in range(NL):
+            step(i, stream)
+            o = ws_off + L.ids
+            ids = ws[o:o + 4 * T * K_TOP].view(torch.int32)
+            U.append(int(torch.unique(ids).numel()))
+    torch.cuda.synchronize()
+    return float(np.mean(U))
+
+
+def layer_bytes(u_mean, T):
+    return (u_mean + 1) * EXPERT_BYTES + H * E * 4 + 2 * T * H * 4
+
+
+def layer_flops(T):
+    return 2.0 * T * (H * E + 3 * H * F * (K_TOP + 1))
+
+
+def measure_layer(torch, qb, layers, T, routing, steps, warmup, stream, world, device, peaks, rank, clocks=False):
+    """One workload of the MoE layer: step time from graph replays, the
+    dominant unit's time, roofline fractions."""
+    NL = len(layers)
+    Xs = make_inputs(torch, NL, T, H, routing, device, 7 + rank + 131 * T)
+    outs = torch.empty_like(Xs)
+    ws = layers[0].workspace(T)
+
+    def step(i, s=None):
+        qb.moe_forward(layers[i % NL], Xs[i % NL], Xs[i % NL], out=outs[i % NL], ws=ws, stream=s)
+
+    with torch.cuda.stream(stream):
+        n0 = qb.launch_count()
+        step(0, stream)
+        launches_per_step = qb.launch_count() - n0
+        for i in range(max(warmup, 3)):
+            step(i, stream)
+    torch.cuda.synchronize()
+    if qb.query_status(stream) != 0:
+        raise RuntimeError("device status word set during warm-up")
+    path = qb.last_path()
+    ms, clk = time_graphs(torch, step, NL, steps, warmup, stream, world, device,
+                          clock_index=device.index if clocks else None)
+    step_s = ms / steps / 1e3
+    u_mean = distinct_experts(torch, qb, layers, step, ws, 0, T, NL, stream)
+    lb = layer_bytes(u_mean, T)
+    hbm_peak = peaks.get("hbm_gbs") or 6800.0
+    hbm_src = "measured hbm_gbs (burst copy)" if peaks.get("hbm_gbs") else "fallback 6.8 TB/s"
+    rows_h = T * K_TOP + T
+    rec = {"T": T, "routing": routing, "path": path, "steps": steps, "ms_per_step": ms / steps,
+           "tokens_per_s": T / step_s, "launches_per_step": launches_per_step,
+           "distinct_experts_mean": u_mean,
+           "layer_hbm": {"achieved": lb / step_s / 1e9, "unit": "GB/s", "frac": lb / step_s / 1e9 / hbm_peak,
+                         "alg_bytes_per_step": lb},
+           "layer_tflops": {"achieved": layer_flops(T) / step_s / 1e12, "unit": "TFLOP/s"}}
+    if path == "gemm_tc":
+        us, n = gateup_in_graph_us(torch, qb, step, NL, stream)
+        alg = 2.0 * rows_h * H * 2 * F
+        peak = peaks.get("bf16_tflops") or 1900.0
+        rec["roofline"] = {"bound": "tensor", "kernel": "moe_tc_kernel<gate/up> (tcgen05)",
+                           "achieved": alg / (us / 1e6) / 1e12, "peak": peak,
+                           "peak_source": "measured bf16_tflops (burst cuBLAS)" if peaks.get("bf16_tflops")
+                           else "fallback 1.9 PFLOP/s",
+                           "unit": "TFLOP/s", "frac": alg / (us / 1e6) / 1e12 / peak,
+                           "algorithmic_per_launch": alg, "avg_launch_us": us, "launches_timed": n,
+                           "timing": "event-record nodes around each gate/up launch inside the graph replay"}
+        rec["layer_tflops"]["frac"] = rec["layer_tflops"]["achieved"] / peak
+    else:
+        # the decode path's kernels overlap by design (programmatic dependent
+        # launch), so its dominant unit is the whole layer step
+        kname = ("decode chain: router + expert kernels (whole layer step inside the graph replay)"
+                 if path == "decode" else "whole layer step (grouped GEMV path) inside the graph replay")
+        rec["roofline"] = {"bound": "hbm", "kernel": kname, "achieved": lb / step_s / 1e9, "peak": hbm_peak,
+                           "peak_source": hbm_src, "unit": "GB/s", "frac": lb / step_s / 1e9 / hbm_peak,
+                           "algorithmic_per_launch": lb, "avg_launch_us": step_s * 1e6,
+                           "launches_timed": steps, "timing": "graph replay of the whole layer"}
+    return rec, clk, step, ws, outs
+
+
 def ours_main(args, rank, world, local_rank):
     import torch
-    import torch.distributed as dist
 
     from quantized_moe_transformer_gb300 import binding as qb
     from quantized_moe_transformer_gb300 import build, inputs
@@ -302,150 +518,33 @@ def ours_main(args, rank, world, local_rank):
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
         peaks = json.load(open(pk))
+    hbm_peak = peaks.get("hbm_gbs") or 6800.0
 
     is_block = wl.get("block", False)
     pos0 = wl.get("pos0", 0)
     arr0 = inputs.moe_layer(0, H, E, F, shared=True, routing=routing)
     layers = [make_layer_on_device(torch, 1000 * rank + i, routing, device,
                                    arr0 if i == 0 else None) for i in range(NL)]
-    gX = torch.Generator(device=device)
-    gX.manual_seed(7 + rank)
-    Xs = torch.randn((NL, T, H), device=device, generator=gX)
-    if routing == "zipf":
-        Xs[:, :, 0] = 1.0
-    outs = torch.empty_like(Xs)
     stream = torch.cuda.Stream(device=device)
+
     if is_block:
-        blocks_ = [make_block_on_device(torch, qb, 5000 * rank + i, layers[i], device) for i in range(NL)]
-        kcs = [torch.randn((CTX, 2, 128), device=device, generator=gX).to(torch.bfloat16) for _ in range(NL)]
-        vcs = [torch.randn((CTX, 2, 128), device=device, generator=gX).to(torch.bfloat16) for _ in range(NL)]
-        ws = blocks_[0].workspace(T, pos0)
-        moe_ws_off = block_moe_ws_offset(qb, blocks_[0], T, pos0)
-
-        def step(i, s=None):
-            j = i % NL
-            qb.block_forward(blocks_[j], Xs[j], kcs[j], vcs[j], pos0, out=outs[j], ws=ws, stream=s)
+        rec, clk, e2e = measure_block(torch, qb, layers, T, pos0, args, stream, world, device, rank, peaks)
+        path = rec["path"]
     else:
-        ws = layers[0].workspace(T)
-        moe_ws_off = 0
+        rec, clk, step, ws, outs = measure_layer(torch, qb, layers, T, routing, args.steps, args.warmup, stream,
+                                                 world, device, peaks, rank, clocks=True)
+        path = rec["path"]
+        traffic = None
+        tf = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+        kernel_sha = source_sha(KERNEL_SOURCES[path])
+        if os.path.exists(tf):
+            r = json.load(open(tf)).get(f"{path}:{args.workload}")
+            if r and r.get("source_sha") == kernel_sha:
+                traffic = r["dram_bytes_per_launch"]
+        rec["roofline"]["traffic"] = traffic
+        rec["roofline"]["kernel_source_sha"] = kernel_sha
 
-        def step(i, s=None):
-            qb.moe_forward(layers[i % NL], Xs[i % NL], Xs[i % NL], out=outs[i % NL], ws=ws, stream=s)
-
-    with torch.cuda.stream(stream):
-        n0 = qb.launch_count()
-        step(0, stream)
-        launches_per_step = qb.launch_count() - n0
-        for i in range(max(args.warmup, 3)):
-            step(i, stream)
-    torch.cuda.synchronize()
-    assert qb.query_status(stream) == 0
-    path = qb.last_path()
-
-    # one graph of NL steps and one graph per step
-    macro = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(macro, stream=stream):
-        for i in range(NL):
-            step(i, stream)
-    singles = []
-    for i in range(NL):
-        gph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gph, stream=stream):
-            step(i, stream)
-        singles.append(gph)
-    for _ in range(max(1, args.warmup // NL)):
-        macro.replay()
-    torch.cuda.synchronize()
-
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk, torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(args.steps // NL):
-            macro.replay()
-        for i in range(args.steps % NL):
-            singles[i].replay()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world, device)
-    if world > 1:
-        dist.barrier()
-    value = job_throughput(T, args.steps, world, ms)
-
-    # dominant kernel, timed per launch with events the library records on the
-    # launching stream: the decode path's chained kernels as one unit, else the
-    # grouped gate/up kernel (GEMV or tcgen05)
-    dom = "decode" if path == "decode" else "gateup"
-    prof_steps = 2 * NL
-    U = []
-    L = layers[0].workspace_layout(T)
-    with torch.cuda.stream(stream):
-        qb.profile_start(dom)
-        for i in range(prof_steps):
-            step(i, stream)
-            o_ids = moe_ws_off + L.ids
-            ids = ws[o_ids:o_ids + 4 * T * K_TOP].view(torch.int32)
-            U.append(int(torch.unique(ids).numel()))
-        dom_ms, dom_n = qb.profile_stop()
-    torch.cuda.synchronize()
-    dom_avg_ms = dom_ms / dom_n
-    u_mean = float(np.mean(U))
-    rows_h = T * K_TOP + T
-    layer_bytes = (u_mean + 1) * EXPERT_BYTES + H * E * 4 + 2 * T * H * 4
-    layer_gbs = layer_bytes / (ms / args.steps / 1e3) / 1e9
-    hbm_peak = peaks.get("hbm_gbs")
-    hbm_src = "measured hbm_gbs (burst copy)" if hbm_peak else "fallback 6.8 TB/s"
-    hbm_peak = hbm_peak or 6800.0
-    if path == "gemm_tc":
-        # FLOPs of one gate/up launch: gate and up for every routed pair and the shared rows
-        alg = 2.0 * rows_h * H * 2 * F
-        achieved = alg / (dom_avg_ms / 1e3) / 1e12
-        peak = peaks.get("bf16_tflops")
-        peak_src = "measured bf16_tflops (burst cuBLAS)" if peak else "fallback 1.9 PFLOP/s"
-        peak = peak or 1900.0
-        bound, unit, kname = "tensor", "TFLOP/s", "moe_tc_kernel<gate/up> (tcgen05)"
-    else:
-        if path == "decode":
-            alg = layer_bytes
-            kname = "decode chain: router + gate/up + down/combine kernels (PDL-overlapped, timed as one unit)"
-        else:
-            # each touched expert's packed gate and up rows once, X read, h written (fp32)
-            alg = (u_mean + 1) * GATEUP_EXPERT_BYTES + T * H * 4 + rows_h * F * 4
-            kname = "gateup_gemv_kernel"
-        achieved = alg / (dom_avg_ms / 1e3) / 1e9
-        peak, peak_src, bound, unit = hbm_peak, hbm_src, "hbm", "GB/s"
-    traffic = None
-    tf = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    kernel_sha = source_sha(KERNEL_SOURCES[path])
-    if os.path.exists(tf):
-        rec = json.load(open(tf)).get(f"{path}:{args.workload}")
-        if rec and rec.get("source_sha") == kernel_sha:
-            traffic = rec["dram_bytes_per_launch"]
-
-    # end to end through the C ABI on host buffers (pinned), copies inside
-    e2e = None
-    if is_block:
-        Xh = torch.randn((NL, T, H), generator=torch.Generator().manual_seed(11)).pin_memory()
-        Oh = torch.empty_like(Xh).pin_memory()
-        Xd = torch.empty((T, H), device=device)
-        n_e2e = min(args.steps, 200)
-        with torch.cuda.stream(stream):
-            for i in range(3 + n_e2e):
-                if i == 3:
-                    torch.cuda.synchronize()
-                    t0 = time.perf_counter()
-                j = i % NL
-                Xd.copy_(Xh[j], non_blocking=True)
-                qb.block_forward(blocks_[j], Xd, kcs[j], vcs[j], pos0, out=outs[j], ws=ws, stream=stream)
-                Oh[j].copy_(outs[j], non_blocking=True)
-                stream.synchronize()
-        dt = time.perf_counter() - t0
-        e2e = {"value": T * n_e2e * world / dt, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 4,
-               "d2h_bytes_per_step": T * H * 4, "steps": n_e2e,
-               "api": "binding.block_forward with pinned host copies on the same stream"}
-    else:
+        # end to end through the C ABI on host buffers (pinned), copies inside
         Xh = torch.randn((NL, T, H), generator=torch.Generator().manual_seed(11)).pin_memory()
         if routing == "zipf":
             Xh[:, :, 0] = 1.0
@@ -462,15 +561,26 @@ def ours_main(args, rank, world, local_rank):
                "d2h_bytes_per_step": T * H * 4, "steps": n_e2e,
                "api": "qmoe_moe_forward_host (pinned host buffers, one call per step)"}
 
+    ms = rec["ms_per_step"] * args.steps
+    value = job_throughput(T, args.steps, world, ms)
+
+    # the other two points of the metric (batched decode at 64 rows, prefill
+    # at 4096 rows) on the same layer instances, when the default runs
+    extras = {}
+    if not is_block and not args.no_extras and args.workload == "decode" and args.T is None:
+        for key, Tx, st in (("decode_t64", 64, 400), ("prefill_t4096", 4096, 48)):
+            r, _, _, _, _ = measure_layer(torch, qb, layers, Tx, routing, st, 3 * NL // 2, stream, world, device,
+                                          peaks, rank)
+            r["tokens_per_s"] *= world
+            extras[key] = r
+        torch.cuda.empty_cache()
+
     # CPU baseline and a parity spot check of instance 0 on the same rows
     cpu = None
     parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not is_block:
-        res = run_cpu_sample(routing, 64, args.cpu_seconds, threads=1)
-        n = len(res["times"])
-        cpu = {"value": n / sum(res["times"]), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} single-row forwards of layer instance 0 ({args.workload} shape, "
-                         f"fp64 numpy oracle, 1 thread)"}
+        cpu, res = cpu_baseline(routing, args.cpu_seconds)
+        n = len(res["outs"])
         Xp = torch.from_numpy(inputs.hidden(1000, 64, H, routing)[:n]).to(device)
         got = np.stack([qb.moe_forward(layers[0], Xp[i:i + 1]).cpu().numpy()[0] for i in range(n)])
         ref = np.array(res["outs"])
@@ -482,19 +592,65 @@ def ours_main(args, rank, world, local_rank):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if path == "gemm_tc" else "f32", "data": "synthetic",
                 "config": workload_config(args.workload, T, routing, NL),
-                "path": path,
-                "roofline": {"bound": bound, "kernel": kname, "achieved": achieved,
-                             "peak": peak, "peak_source": peak_src, "unit": unit,
-                             "frac": achieved / peak, "traffic": traffic,
-                             "algorithmic_per_launch": alg, "avg_launch_us": dom_avg_ms * 1e3,
-                             "launches_timed": dom_n, "distinct_experts_mean": u_mean,
-                             "kernel_source_sha": kernel_sha},
-                "layer_hbm": {"achieved": layer_gbs, "unit": "GB/s", "frac": layer_gbs / hbm_peak,
-                              "alg_bytes_per_step": layer_bytes},
-                "layer_tflops": 2.0 * T * (H * E + 3 * H * F * (K_TOP + 1)) / (ms / args.steps / 1e3) / 1e12,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "launches_per_step": launches_per_step, "clocks": clk.summary, "parity": parity}
+                "path": path, "roofline": rec["roofline"],
+                "layer_hbm": rec.get("layer_hbm"), "layer_tflops": rec.get("layer_tflops"),
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": rec["launches_per_step"] * args.steps,
+                "launches_per_step": rec["launches_per_step"], "clocks": clk, "parity": parity}
+        line.update(extras)
         print(json.dumps(line))
+
+
+def measure_block(torch, qb, layers, T, pos0, args, stream, world, device, rank, peaks):
+    """The attention + MoE block (config of the block workloads)."""
+    NL = len(layers)
+    blocks_ = [make_block_on_device(torch, qb, 5000 * rank + i, layers[i], device) for i in range(NL)]
+    g = torch.Generator(device=device)
+    g.manual_seed(7 + rank)
+    Xs = torch.randn((NL, T, H), device=device, generator=g)
+    outs = torch.empty_like(Xs)
+    kcs = [torch.randn((CTX, 2, 128), device=device, generator=g).to(torch.bfloat16) for _ in range(NL)]
+    vcs = [torch.randn((CTX, 2, 128), device=device, generator=g).to(torch.bfloat16) for _ in range(NL)]
+    ws = blocks_[0].workspace(T, pos0)
+
+    def step(i, s=None):
+        j = i % NL
+        qb.block_forward(blocks_[j], Xs[j], kcs[j], vcs[j], pos0, out=outs[j], ws=ws, stream=s)
+
+    with torch.cuda.stream(stream):
+        n0 = qb.launch_count()
+        step(0, stream)
+        launches_per_step = qb.launch_count() - n0
+        for i in range(max(args.warmup, 3)):
+            step(i, stream)
+    torch.cuda.synchronize()
+    path = qb.last_path()
+    ms, clk = time_graphs(torch, step, NL, args.steps, args.warmup, stream, world, device,
+                          clock_index=device.index)
+    step_s = ms / args.steps / 1e3
+    rec = {"path": path, "ms_per_step": ms / args.steps, "launches_per_step": launches_per_step,
+           "roofline": {"bound": "tensor" if path == "gemm_tc" else "hbm", "kernel": "whole block step",
+                        "achieved": None, "peak": None, "unit": None, "frac": None, "traffic": None,
+                        "avg_launch_us": step_s * 1e6,
+                        "note": "block steps are reported, not gated; the MoE layer carries the roofline"}}
+    Xh = torch.randn((NL, T, H), generator=torch.Generator().manual_seed(11)).pin_memory()
+    Oh = torch.empty_like(Xh).pin_memory()
+    Xd = torch.empty((T, H), device=device)
+    n_e2e = min(args.steps, 200)
+    with torch.cuda.stream(stream):
+        for i in range(3 + n_e2e):
+            if i == 3:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            j = i % NL
+            Xd.copy_(Xh[j], non_blocking=True)
+            qb.block_forward(blocks_[j], Xd, kcs[j], vcs[j], pos0, out=outs[j], ws=ws, stream=stream)
+            Oh[j].copy_(outs[j], non_blocking=True)
+            stream.synchronize()
+    dt = time.perf_counter() - t0
+    e2e = {"value": T * n_e2e * world / dt, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 4,
+           "d2h_bytes_per_step": T * H * 4, "steps": n_e2e,
+           "api": "binding.block_forward with pinned host copies on the same stream"}
+    return rec, clk, e2e
 
 
 # kernels whose DRAM bytes make up the dominant unit of each path: the decode
@@ -551,6 +707,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        # one process per GPU: N replicas need N ranks from a launcher
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch N ranks with "
+                 f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus}")
     if args.impl == "reference":
         reference_main(args, rank, world)
         return

@@ -198,9 +198,11 @@ int qmoe_moe_forward_host(const qmoe_moe_desc *d, const float *X_host, const flo
  * exits.
  *   Same arguments and result as qmoe_moe_forward with internal routing
  *   (no ids/w): X [T][H] fp32, R [T][H] fp32 or NULL, out [T][H] fp32.
- *   Returns QMOE_ERR_TOO_LARGE, enqueuing nothing, when
- *   qmoe_moe_workspace_bytes(d, T) exceeds the scratch size (at the
- *   Qwen3.5-35B-A3B layer shape that is T > 64 rows).
+ *   Returns QMOE_ERR_TOO_LARGE, enqueuing nothing and leaving ``out``
+ *   untouched, when qmoe_moe_workspace_bytes(d, T) exceeds the scratch size;
+ *   the largest row count that fits is therefore the largest T whose
+ *   workspace is at most QMOE_NOALLOC_SCRATCH_BYTES (86 rows at the
+ *   Qwen3.5-35B-A3B layer shape: H=2048, E=256, k=8, F=512, shared expert).
  *   The first call on each device looks up the scratch array's device
  *   address with that device current; make that first call before any
  *   stream capture. Every call on a device shares the one array and leaves
@@ -219,10 +221,14 @@ long long qmoe_launch_count(void);
 
 /*
  * Stage timing. After qmoe_profile_start(stage), every launch of that stage
- * by this thread (outside stream capture) is bracketed with a pair of CUDA
- * events on its stream, up to 4096 launches; qmoe_profile_stop waits for them
- * and returns the summed kernel time in milliseconds and the launch count.
- * stage 0 turns profiling off. Do not profile while a stream is capturing.
+ * by this thread is bracketed with a pair of CUDA events on its stream, up to
+ * 4096 launches; qmoe_profile_stop waits for them and returns the summed
+ * kernel time in milliseconds and the launch count, and turns profiling off.
+ * stage 0 turns profiling off. While the stream is capturing a graph the
+ * events are recorded as event-record nodes of that graph
+ * (cudaEventRecordExternal): after each replay of the graph,
+ * qmoe_profile_read returns the summed times of that replay's bracketed
+ * launches without turning profiling off (call qmoe_profile_stop once done).
  */
 typedef enum {
   QMOE_STAGE_ROUTER = 1,  /* router logits                          */
@@ -234,6 +240,7 @@ typedef enum {
 } qmoe_stage;
 int qmoe_profile_start(int stage);
 int qmoe_profile_stop(double *total_ms, int *launches);
+int qmoe_profile_read(double *total_ms, int *launches);
 
 /*
  * One transformer block around the MoE layer ([CKE-Zip] "What PR #382 Now

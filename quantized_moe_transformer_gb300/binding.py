@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
         L.qmoe_launch_count.argtypes = []
         L.qmoe_profile_start.argtypes = [_c_int]
         L.qmoe_profile_stop.argtypes = [P(ctypes.c_double), P(_c_int)]
+        L.qmoe_profile_read.argtypes = [P(ctypes.c_double), P(_c_int)]
         L.qmoe_moe_forward_noalloc.argtypes = [P(MoeDesc), _vp, _vp, _vp, _c_int, _vp]
         L.qmoe_last_cuda_error.argtypes = []
         L.qmoe_get_decode_max_rows.argtypes = []
@@ -88,7 +89,7 @@ def exported_symbols() -> list[str]:
             "qmoe_set_gemm_threshold", "qmoe_last_path", "qmoe_moe_route_workspace_bytes",
             "qmoe_moe_route", "qmoe_moe_workspace_bytes", "qmoe_moe_workspace_layout",
             "qmoe_moe_forward", "qmoe_moe_forward_host_workspace_bytes", "qmoe_moe_forward_host",
-            "qmoe_launch_count", "qmoe_profile_start", "qmoe_profile_stop",
+            "qmoe_launch_count", "qmoe_profile_start", "qmoe_profile_stop", "qmoe_profile_read",
             "qmoe_moe_forward_noalloc", "qmoe_get_decode_max_rows", "qmoe_set_decode_max_rows",
             "qmoe_last_cuda_error", "qmoe_rmsnorm", "qmoe_attn_workspace_bytes", "qmoe_attn_forward", "qmoe_block_workspace_bytes",
             "qmoe_block_forward"]
@@ -241,6 +242,15 @@ def launch_count() -> int:
 
 def profile_start(stage: str):
     _check(lib().qmoe_profile_start(STAGES[stage]))
+
+
+def profile_read():
+    """(summed kernel milliseconds, launches) of the profiled launches as the
+    last replay of a graph captured with profiling on left them."""
+    ms = ctypes.c_double()
+    n = _c_int()
+    _check(lib().qmoe_profile_read(ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value
 
 
 def profile_stop():

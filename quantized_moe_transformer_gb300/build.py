@@ -1,15 +1,20 @@
 """Builds libqmoe.so in-tree from csrc/*.cu with nvcc for sm_103a.
 
 Each translation unit is compiled in parallel, then linked as one shared
-library next to this file. A rebuild happens only when a source or header is
-newer than the library.
+library next to this file. A stamp file beside the library records the
+machine it was built on and a hash of every source, header and flag; the
+library is rebuilt whenever the stamp does not match this machine and these
+sources, so a library built elsewhere (another CPU architecture, other
+sources) is never loaded.
 """
 
 from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 
@@ -17,6 +22,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libqmoe.so")
+STAMP = OUT + ".stamp"
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -40,11 +46,22 @@ def _deps():
         glob.glob(os.path.join(ROOT, "include", "*.h"))
 
 
+def stamp() -> str:
+    """This machine and a hash of every input of the build."""
+    h = hashlib.sha256()
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    for p in sorted(_deps()):
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return f"{platform.machine()} {h.hexdigest()}"
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(OUT):
+    if not (os.path.exists(OUT) and os.path.exists(STAMP)):
         return False
-    t = os.path.getmtime(OUT)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    with open(STAMP) as f:
+        return f.read().strip() == stamp()
 
 
 def _compile(src: str, extra: list[str]) -> str:
@@ -72,6 +89,8 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, OUT)
+    with open(STAMP, "w") as f:
+        f.write(stamp() + "\n")
     return OUT
 
 

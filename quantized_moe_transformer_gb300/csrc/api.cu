@@ -34,6 +34,17 @@ struct StageProfile {
 };
 thread_local StageProfile g_prof;
 
+// Records ``ev`` on ``st``; while ``st`` is capturing a graph the record becomes
+// an event-record node of the graph (cudaEventRecordExternal), so that the
+// event's time is that of the node in each replay.
+void record_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, st);
+}
+
 // Runs ``launch`` (a kernel launch on ``st``), counting it and, when its stage
 // is being profiled, bracketing it with a pair of events.
 template <typename F>
@@ -46,13 +57,13 @@ cudaError_t staged(int stage, int n_kernels, cudaStream_t st, F&& launch) {
         return cudaErrorMemoryAllocation;
       g_prof.created = g_prof.n + 1;
     }
-    cudaEventRecord(g_prof.start[g_prof.n], st);
+    record_event(g_prof.start[g_prof.n], st);
   }
   cudaError_t e = launch();
   g_launches.fetch_add(n_kernels);
   if (e != cudaSuccess) g_last_cuda_error = (int)e;
   if (prof) {
-    cudaEventRecord(g_prof.stop[g_prof.n], st);
+    record_event(g_prof.stop[g_prof.n], st);
     ++g_prof.n;
   }
   return e;
@@ -688,6 +699,21 @@ int qmoe_profile_start(int stage) {
   if (stage < 0 || stage > QMOE_STAGE_DECODE) return QMOE_ERR_ARG;
   g_prof.stage = stage;
   g_prof.n = 0;
+  return QMOE_OK;
+}
+
+int qmoe_profile_read(double* total_ms, int* launches) {
+  if (!total_ms || !launches) return QMOE_ERR_NULL;
+  double tot = 0.0;
+  for (int i = 0; i < g_prof.n; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.stop[i]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.start[i], g_prof.stop[i]) != cudaSuccess)
+      return QMOE_ERR_CUDA;
+    tot += ms;
+  }
+  *total_ms = tot;
+  *launches = g_prof.n;
   return QMOE_OK;
 }
 

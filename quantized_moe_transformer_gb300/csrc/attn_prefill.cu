@@ -248,12 +248,8 @@ __global__ void __launch_bounds__(FA_THREADS) attn_prefill_mma_kernel(const floa
 cudaError_t launch_attention_prefill(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
                                      int T, int pos0, int nh, int nkv, cudaStream_t st) {
   const int smem = 2 * 2 * FA_TILE_BYTES;  // two stages of K and V
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(attn_prefill_mma_kernel), smem);
+  if (e != cudaSuccess) return e;
   attn_prefill_mma_kernel<<<dim3((T + FA_BQ - 1) / FA_BQ, nh), FA_THREADS, smem, st>>>(q, kc, vc, o, T, pos0, nh,
                                                                                        nkv);
   return cudaGetLastError();

@@ -5,6 +5,14 @@
 
 namespace qmoe {
 
+// device_cache.cu: per-device launch bookkeeping. ensure_kernel_smem raises
+// ``fn``'s dynamic shared-memory limit to at least ``smem`` bytes on the
+// current device (and sets the preferred carveout when ``carveout`` >= 0),
+// once per (device, kernel, size); device_sm_count is the current device's SM
+// count.
+cudaError_t ensure_kernel_smem(const void* fn, size_t smem, int carveout = -1);
+int device_sm_count();
+
 // router.cu
 int router_splits(int T, int H, int E);
 // ``wr3``: scratch of router_tc_ws_bytes(T, H, E) bytes, used (with ``status``)

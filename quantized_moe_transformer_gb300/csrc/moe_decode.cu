@@ -26,8 +26,6 @@
 //                 out = R + y_shared + sum_s w_s y_s in slot order.
 // Every CTA reaches the same routing decision from the same partials; every
 // wait on a copy is bounded and records QMOE_ERR_TIMEOUT on expiry.
-#include <mutex>
-
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -504,36 +502,9 @@ bool decode_path_supported(int T, int H, int E, int k, int F, int gate_qt, int d
   return true;
 }
 
-// Per-kernel launch attributes, set once per kernel (and again whenever a
-// launch needs more dynamic shared memory than before). All decode kernels
-// share one signature, so the bookkeeping is keyed by the kernel's address.
-static cudaError_t prepare_kernel(const void* fn, size_t smem) {
-  static std::mutex mu;
-  static const void* fns[32];
-  static size_t smem_set[32];
-  static int n = 0;
-  std::lock_guard<std::mutex> lock(mu);
-  int i = 0;
-  while (i < n && fns[i] != fn) ++i;
-  if (i == n) {
-    if (n == 32) return cudaErrorInvalidValue;
-    // the three kernels run concurrently: ask for the largest shared-memory
-    // carveout so that CTAs of different kernels can share an SM
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    fns[n] = fn;
-    smem_set[n] = 0;
-    ++n;
-  }
-  // static shared memory counts against the same limit, so the dynamic
-  // maximum is raised for every launch size not seen before
-  if (smem > smem_set[i]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    smem_set[i] = smem;
-  }
-  return cudaSuccess;
-}
+// The three kernels run concurrently: each asks for the largest shared-memory
+// carveout so that CTAs of different kernels can share an SM.
+static cudaError_t prepare_kernel(const void* fn, size_t smem) { return ensure_kernel_smem(fn, smem, 100); }
 
 template <typename K>
 static cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t st, const DecodeArgs& a) {

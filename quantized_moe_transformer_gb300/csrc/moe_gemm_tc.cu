@@ -673,17 +673,6 @@ cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, int rows, int K, co
 }
 
 // ---------------------------------------------------------------------------
-int tc_num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    n = v > 0 ? v : 1;
-  }
-  return n;
-}
-
 int tc_max_chunks(int T, int k, int E, int has_shared) {
   const int P = T * k;
   return (P + (has_shared ? T : 0)) / TC_N_MIN + E + 1;
@@ -758,14 +747,10 @@ static bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_
 
 template <bool GATEUP, int QT, int NMAX>
 static cudaError_t tc_launch_n(const TcArgs& a, const TcMaps& maps, int max_items, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(moe_tc_kernel<GATEUP, QT, NMAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<QT, NMAX>::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  int grid = tc_num_sms();
+  cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(moe_tc_kernel<GATEUP, QT, NMAX>),
+                                     TcCfg<QT, NMAX>::SMEM);
+  if (e != cudaSuccess) return e;
+  int grid = device_sm_count();
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
   moe_tc_kernel<GATEUP, QT, NMAX><<<grid, TC_THREADS, TcCfg<QT, NMAX>::SMEM, st>>>(a, maps);

@@ -300,7 +300,19 @@ __device__ __forceinline__ void warp_topk_row(const float* part, int nsplit, int
         be = oe;
       }
     }
-    if (be >= E) be = 0;  // only if every remaining logit is NaN: keep the id in range
+    if (be >= E) {
+      // every remaining logit is NaN or -inf: take the lowest index not yet
+      // taken (ties go to the lower index), so that a row never repeats an id
+      int lo = 0x7fffffff;
+#pragma unroll
+      for (int j = EPL - 1; j >= 0; --j) {
+        const int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u)) lo = e;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      be = lo;
+    }
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
     sel_l[r] = bv;
     sel_e[r] = be;
@@ -663,12 +675,8 @@ cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_s
   const size_t staged_smem = base_smem + sizeof(int32_t) * (size_t)nc * E;
   const int staged = staged_smem <= 160 * 1024 ? 1 : 0;
   const size_t smem = staged ? staged_smem : base_smem;
-  static size_t smem_set = 48 * 1024;
-  if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(perm_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    if (e != cudaSuccess) return e;
-    smem_set = 160 * 1024;
-  }
+  cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(perm_scan_kernel), smem);
+  if (e != cudaSuccess) return e;
   perm_scan_kernel<<<1, 1024, smem, st>>>(chunk_cnt, nc, T, E, k, has_shared, staged, offsets, perm, active,
                                           n_active);
   perm_scatter_kernel<<<nc, 32, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, perm);

@@ -317,12 +317,8 @@ cudaError_t launch_router_tc(const float* X, const float* Wr, float* part, int T
   if (e != cudaSuccess) return e;
   CUtensorMap m;
   if (!encode_wr3(&m, w3, (uint64_t)3 * E, (uint64_t)H)) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  e = ensure_kernel_smem(reinterpret_cast<const void*>(router_tc_kernel), RT_SMEM);
+  if (e != cudaSuccess) return e;
   const dim3 grid(E / RT_BN, (T + RT_BM - 1) / RT_BM, nsplit);
   router_tc_kernel<<<grid, RT_THREADS, RT_SMEM, st>>>(X, part, T, H, E, H / nsplit, status, m);
   return cudaGetLastError();

@@ -5,8 +5,9 @@ on the fp32-accumulate GEMV path, <= 1e-2 * max |ref| on the bf16 tensor-core
 path. Expert ids must equal the oracle's exactly, as a set, on every row whose
 oracle gap between the k-th and (k+1)-th logit is at least 1e-5; the slot
 order must match too where every adjacent gap among the top k+1 is at least
-1e-5. Rows under the gap are excused from the id and value comparison, and their
-GPU ids must still be a valid top-k of the oracle's logits to within 1e-5.
+1e-5. Rows under the gap are excused from the id and value comparison (at most one
+in a hundred of the checked rows, or one), and their GPU ids must still be a
+valid top-k of the oracle's logits to within 1e-5.
 """
 
 import numpy as np
@@ -32,6 +33,9 @@ def check_routes(ids_gpu: np.ndarray, ids_ref: np.ndarray, gap: np.ndarray,
             kth = -np.sort(-logits[t])[k - 1]
             assert len(set(ids_gpu[t].tolist())) == k
             assert np.all(logits[t, ids_gpu[t]] >= kth - GAP)
+    # the excuse is for rare accidental near-ties, not a loophole: at most one
+    # row in a hundred (or one row) may take it
+    assert int((~ok).sum()) <= max(1, T // 100), f"{int((~ok).sum())} of {T} rows excused"
     return ok
 
 

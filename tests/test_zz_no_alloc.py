@@ -54,3 +54,31 @@ def test_noalloc_rejects_oversize(layer):
     assert r == -10
     assert b"scratch" in qb.lib().qmoe_status_str(r)
     assert torch.count_nonzero(out).item() == 0
+
+
+def _largest_fitting_rows(layer):
+    T = 1
+    while layer.workspace_bytes(T + 1) <= (8 << 20):
+        T += 1
+    return T
+
+
+def test_noalloc_row_limit_boundary(layer):
+    """The largest row count whose workspace fits the 8 MiB scratch runs and
+    matches the workspace entry point; one row more is refused with
+    QMOE_ERR_TOO_LARGE and leaves ``out`` untouched."""
+    T = _largest_fitting_rows(layer)
+    assert T == 86  # at this layer shape, as the header states
+    X = torch.from_numpy(inputs.hidden(7, T, 2048)).cuda()
+    ref = qb.moe_forward(layer, X)
+    got = qb.moe_forward_noalloc(layer, X)
+    torch.cuda.synchronize()
+    assert qb.query_status() == 0
+    assert_close(got.cpu().numpy(), ref.cpu().numpy(), TOL_GEMV)
+    X1 = torch.from_numpy(inputs.hidden(8, T + 1, 2048)).cuda()
+    out = torch.full_like(X1, 3.0)
+    r = qb.lib().qmoe_moe_forward_noalloc(ctypes.byref(layer.desc), ctypes.c_void_p(X1.data_ptr()), None,
+                                          ctypes.c_void_p(out.data_ptr()), T + 1, None)
+    torch.cuda.synchronize()
+    assert r == -10
+    assert bool(torch.all(out == 3.0))
