@@ -77,7 +77,7 @@ typedef enum {
   QMOE_PATH_NONE = 0,
   QMOE_PATH_GEMV = 1,     /* grouped dequant-fused GEMV kernels        */
   QMOE_PATH_GEMM_TC = 2,  /* grouped dequant + bf16 tcgen05 GEMM       */
-  QMOE_PATH_DECODE = 3    /* T <= 4: three kernels chained with PDL    */
+  QMOE_PATH_DECODE = 3    /* T <= 4: router + persistent expert kernel */
 } qmoe_path;
 
 /*
@@ -152,10 +152,12 @@ void qmoe_set_gemm_threshold(int rows);
 int qmoe_last_path(void);
 
 /* Rows up to this count (at most 4, the built-in value) take the decode path
- * when the layer's routes are computed internally: router, gate/up and down
- * kernels chained with programmatic dependent launch, each CTA taking the
- * top-k itself and the down kernel forming the slot-order combine. 0 turns it
- * off; -1 restores the built-in value. */
+ * when the layer's routes are computed internally and the shape allows it
+ * (H 1024 or 2048, F 256 or 512, E a multiple of 8): a router kernel and one
+ * persistent expert kernel (one CTA per SM, cooperative launch) chained with
+ * programmatic dependent launch, every CTA taking the top-k itself; the
+ * expert kernel's CTAs form the slot-order combine. 0 turns it off; -1
+ * restores the built-in value. */
 int qmoe_get_decode_max_rows(void);
 void qmoe_set_decode_max_rows(int rows);
 
@@ -215,6 +217,26 @@ int qmoe_moe_forward_host(const qmoe_moe_desc *d, const float *X_host, const flo
 int qmoe_moe_forward_noalloc(const qmoe_moe_desc *d, const float *X, const float *R,
                              float *out, int T, qmoe_stream_t stream);
 
+/*
+ * Test-only fault injection (the pages have no counterpart: this exists so
+ * that the library's bounded device waits can be exercised without faulting
+ * a GPU). While a site is set, every qmoe_moe_forward that reaches that site
+ * withholds one copy or arrival, so that one wait can never complete; the
+ * waiting CTA gives up after ``wait_us`` microseconds (0: the normal limit of
+ * 2 s), records QMOE_ERR_TIMEOUT in the status word and returns with nothing
+ * of its own in flight. The call's ``out`` is then incomplete. Sites:
+ *   QMOE_FAULT_NONE        off (the default);
+ *   QMOE_FAULT_DECODE_COPY decode path: the first CTA never copies the down
+ *                          weights of its last down unit;
+ *   QMOE_FAULT_TC_ARRIVE   tensor-core path, gate/up kernel: the first CTA's
+ *                          producers never mark the last stage of their last
+ *                          work item stored.
+ * Returns QMOE_ERR_ARG for an unknown site or a negative wait. Not for use
+ * outside tests; set QMOE_FAULT_NONE afterwards.
+ */
+enum { QMOE_FAULT_NONE = 0, QMOE_FAULT_DECODE_COPY = 1, QMOE_FAULT_TC_ARRIVE = 2 };
+int qmoe_test_inject(int site, int wait_us);
+
 /* Number of kernels this library has enqueued since it was loaded (a CUDA
  * graph replay of captured launches does not add to it). */
 long long qmoe_launch_count(void);
@@ -236,7 +258,7 @@ typedef enum {
   QMOE_STAGE_GATEUP = 3,  /* grouped gate/up + SwiGLU               */
   QMOE_STAGE_DOWN = 4,    /* grouped down projection                */
   QMOE_STAGE_COMBINE = 5, /* slot-order combine + shared + residual */
-  QMOE_STAGE_DECODE = 6   /* the decode path's three chained kernels, as one unit */
+  QMOE_STAGE_DECODE = 6   /* the decode path's two chained kernels, as one unit */
 } qmoe_stage;
 int qmoe_profile_start(int stage);
 int qmoe_profile_stop(double *total_ms, int *launches);

@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.qmoe_get_decode_max_rows.argtypes = []
         L.qmoe_set_decode_max_rows.argtypes = [_c_int]
         L.qmoe_set_decode_max_rows.restype = None
+        L.qmoe_test_inject.argtypes = [_c_int, _c_int]
         _lib = L
     return _lib
 
@@ -92,7 +93,7 @@ def exported_symbols() -> list[str]:
             "qmoe_launch_count", "qmoe_profile_start", "qmoe_profile_stop", "qmoe_profile_read",
             "qmoe_moe_forward_noalloc", "qmoe_get_decode_max_rows", "qmoe_set_decode_max_rows",
             "qmoe_last_cuda_error", "qmoe_rmsnorm", "qmoe_attn_workspace_bytes", "qmoe_attn_forward", "qmoe_block_workspace_bytes",
-            "qmoe_block_forward"]
+            "qmoe_block_forward", "qmoe_test_inject"]
 
 
 def _check(status: int):
@@ -184,6 +185,15 @@ def moe_forward(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = None,
     _check(lib().qmoe_moe_forward(ctypes.byref(layer.desc), _ptr(X), _ptr(R), _ptr(ids), _ptr(w),
                                   _ptr(out), T, _ptr(ws), ws.numel(), _stream(stream)))
     return out
+
+
+FAULT_SITES = {"none": 0, "decode_copy": 1, "tc_arrive": 2}
+
+
+def test_inject(site: str, wait_us: int = 0):
+    """Test-only: make the next forwards withhold one copy or arrival at
+    ``site`` so that one bounded device wait runs out after ``wait_us``."""
+    _check(lib().qmoe_test_inject(FAULT_SITES[site], int(wait_us)))
 
 
 def query_status(stream=None) -> int:

@@ -22,6 +22,15 @@ std::atomic<int> g_decode_max_rows{kDefaultDecodeRows};
 thread_local int g_last_path = QMOE_PATH_NONE;
 thread_local int g_last_cuda_error = 0;
 std::atomic<long long> g_launches{0};
+// test-only fault injection (qmoe_test_inject) and the bound on device waits
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+std::atomic<int> g_fault_site{0};
+std::atomic<int> g_fault_wait_us{0};
+
+unsigned long long wait_limit_ns() {
+  const int us = g_fault_wait_us.load();
+  return (g_fault_site.load() != 0 && us > 0) ? 1000ull * (unsigned long long)us : kWaitLimitNs;
+}
 
 // Opt-in per-stage timing: events recorded around every launch of one stage.
 constexpr int kProfCap = 4096;
@@ -98,7 +107,7 @@ inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace carve-up (every piece 256-byte aligned).
 struct MoeWs {
-  size_t part, wr3, ids, w, route, offsets, perm, inv, active, n_active, chunk, chunks, n_chunks, xb, h, y, total;
+  size_t part, wr3, ids, w, sync, offsets, perm, inv, active, n_active, chunk, chunks, n_chunks, xb, h, y, total;
   int nsplit;
 };
 
@@ -112,7 +121,7 @@ MoeWs moe_ws_layout(int T, int H, int E, int k, int F) {
   L.wr3 = o;      o += up256(router_tc_ws_bytes(T, H, E));  // tensor-core router's Wr parts
   L.ids = o;      o += up256(sizeof(int32_t) * P);
   L.w = o;        o += up256(sizeof(float) * P);
-  L.route = o;    o += up256(sizeof(int32_t) * (P + 1));
+  L.sync = o;     o += up256(sizeof(int32_t) * (size_t)decode_sync_ints(H));  // decode path counters
   L.offsets = o;  o += up256(sizeof(int32_t) * (E + 2));
   L.perm = o;     o += up256(sizeof(int32_t) * rows);
   L.inv = o;      o += up256(sizeof(int32_t) * rows);
@@ -529,10 +538,12 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     D.ybuf = y;
     D.ids = ws_ids;
     D.w = ws_w;
-    D.route = reinterpret_cast<int32_t*>(base + L.route);
+    D.sync = reinterpret_cast<int*>(base + L.sync);
     D.status = status;
-    // router, routing, gate/up, down+combine
-    e = staged(QMOE_STAGE_DECODE, 4, st, [&] { return launch_decode(D, st); });
+    D.wait_ns = wait_limit_ns();
+    D.fault = g_fault_site.load() == QMOE_FAULT_DECODE_COPY ? 1 : 0;
+    // router, experts
+    e = staged(QMOE_STAGE_DECODE, 2, st, [&] { return launch_decode(D, st); });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
     g_last_path = QMOE_PATH_DECODE;
     return QMOE_OK;
@@ -609,7 +620,10 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     p.xb = xb;
     p.tok_rows = (int)(P + (has_shared ? T : 0));
     p.hout = h16;
+    p.wait_ns = wait_limit_ns();
+    p.fault = g_fault_site.load() == QMOE_FAULT_TC_ARRIVE ? 1 : 0;
     e = staged(QMOE_STAGE_GATEUP, 1, st, [&] { return launch_gateup_tc(p, st); });
+    p.fault = 0;
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
     p.W = static_cast<const uint8_t*>(d->Wd);
     p.W2 = nullptr;
@@ -694,6 +708,13 @@ int qmoe_moe_forward_host(const qmoe_moe_desc* d, const float* X_host, const flo
 }
 
 long long qmoe_launch_count(void) { return g_launches.load(); }
+
+int qmoe_test_inject(int site, int wait_us) {
+  if (site < 0 || site > QMOE_FAULT_TC_ARRIVE || wait_us < 0) return QMOE_ERR_ARG;
+  g_fault_wait_us.store(wait_us);
+  g_fault_site.store(site);
+  return QMOE_OK;
+}
 
 int qmoe_profile_start(int stage) {
   if (stage < 0 || stage > QMOE_STAGE_DECODE) return QMOE_ERR_ARG;

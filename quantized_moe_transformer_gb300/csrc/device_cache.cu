@@ -46,13 +46,11 @@ cudaError_t ensure_kernel_smem(const void* fn, size_t smem, int carveout) {
     if (e != cudaSuccess) return e;
     a.carveout = carveout;
   }
-  // static shared memory counts against the same limit, so every size above
-  // the default 48 KB is set explicitly
+  // the default limit is 48 KB minus the kernel's static shared memory, so
+  // every dynamic size a launch asks for is set explicitly the first time
   if (smem > a.smem) {
-    if (smem > 48 * 1024) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-    }
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     a.smem = smem;
   }
   return cudaSuccess;

@@ -74,6 +74,8 @@ struct GroupedTcArgs {
   int nmax;         // chunk cap the chunk list was built with (64 or 128)
   int T, k, E, H, F;
   int* status;
+  unsigned long long wait_ns;  // bound on a device wait (0: the default 2 s)
+  int fault;                   // test-only fault site of the gate/up kernel (0 = none)
 };
 int tc_max_chunks(int T, int k, int E, int has_shared);
 int tc_chunk_cap(int T, int k, int E);
@@ -101,7 +103,8 @@ cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaS
 cudaError_t launch_attention_prefill(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
                                      int T, int pos0, int nh, int nkv, cudaStream_t st);
 
-// moe_decode.cu: three PDL-chained kernels for T <= 4.
+// moe_decode.cu: the decode path for T <= 4 (router kernel + one persistent
+// expert kernel, programmatic dependent launch).
 struct DecodeLaunch {
   const float* X;
   const float* R;
@@ -114,9 +117,12 @@ struct DecodeLaunch {
   float* ybuf;
   int32_t* ids;
   float* w;
-  int32_t* route;  // 1 + T*k int32
+  int* sync;                   // decode_sync_ints(H) ints, cleared by the router kernel
   int* status;
+  unsigned long long wait_ns;  // a bounded wait gives up after this long
+  int fault;                   // test-only fault site (0 = none)
 };
+int decode_sync_ints(int H);
 bool decode_path_supported(int T, int H, int E, int k, int F, int gate_qt, int down_qt);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st);
 

@@ -1,41 +1,63 @@
-// Decode path (T <= 4 rows): three kernels chained with programmatic dependent
-// launch, no host round trip and no separate permutation or combine kernel.
+// Decode path (T <= 4 rows): a router kernel and one persistent expert
+// kernel, chained with programmatic dependent launch.
 //
-// "Distributed CPU: Zip Fusion Beyond Tensor Parallelism", "Decode vs Prefill":
-// at one row every packed weight byte is read once, so the layer is bound by
-// HBM bandwidth and the question is how little time the HBM pipe sits idle.
-// "CKE Zip: From Splitting Tokens To Splitting Qwen3.5 Weights", "A Separate
-// Decode Result Shows Why Axis Choice Matters": with one row the independent
-// work is the eight selected routes, merged in selected-slot order.
+// "Distributed CPU: Zip Fusion Beyond Tensor Parallelism", "Decode vs Prefill:
+// Same Weights, Different Bottlenecks": at a few rows every packed weight byte
+// is read once and the layer is bound by HBM bandwidth, so the question is how
+// little time the HBM pipe sits idle. "CKE Zip: From Splitting Tokens To
+// Splitting Qwen3.5 Weights", "A Separate Decode Result Shows Why Axis Choice
+// Matters": with one row the independent work is the selected routes, merged
+// in selected-slot order.
 //
-//   K1 router     one CTA per (8 experts, quarter of H): its threads load
-//                 their Wr rows' 32 bytes for those experts before waiting on
-//                 the previous grid, then reduce x . Wr over the quarter in a
-//                 fixed order and write 4 partial logits per (row, expert);
-//                 128 CTAs share the 2 MB read.
-//   K1b route     one CTA: sums the partials in a fixed order, takes the top-k
-//                 by rank, the weights and the ascending list of distinct
-//                 selected experts, once for all later CTAs.
-//   K2 gate/up    one CTA per (expert slot, 32 intermediate rows). The shared
-//                 expert's CTAs start their weight copies before the routing
-//                 is known; the others read the routing record and stream
-//                 their expert's rows. Output h per (row, slot) pair.
-//   K3 down       one CTA per 8 output rows. It reads the routing record,
-//                 streams its 8 rows of every selected expert's down matrix
-//                 while K2 is still running, then waits for h, and forms
-//                 out = R + y_shared + sum_s w_s y_s in slot order.
-// Every CTA reaches the same routing decision from the same partials; every
-// wait on a copy is bounded and records QMOE_ERR_TIMEOUT on expiry.
+//   K1 router   one CTA per (8 experts, quarter of H): its threads load their
+//               Wr rows' 32 bytes for those experts before waiting on the
+//               previous grid, then reduce x . Wr over the quarter in a fixed
+//               order and write 4 partial logits per (row, expert). CTA 0 also
+//               clears the expert kernel's counters.
+//   K2 experts  one CTA per SM (cooperative launch, so every CTA is resident),
+//               16 warps. Work is cut into equal shares of all SMs:
+//                 - gate/up units: (expert slot, intermediate row f), a gate
+//                   row and an up row each. The shared expert's units are
+//                   known before routing, so each CTA starts their copies
+//                   before it waits for the router; then every CTA takes the
+//                   top-k itself from the router's partials (the same fixed-
+//                   order arithmetic everywhere, so every CTA reaches the same
+//                   decision) and copies its share of the routed experts' rows
+//                   through a ring of bulk copies (cp.async.bulk + mbarrier);
+//                 - down units: (expert slot, block of 32 output rows), whose
+//                   rows are copied through a second ring as soon as the
+//                   routing is known, while the gate/up units still compute.
+//               A gate/up unit writes h = silu(x.g) * (x.u) per (row, slot)
+//               pair; when a CTA has finished its gate/up units it adds their
+//               count to a per-slot counter. A down unit waits for its slot's
+//               counter to reach F (all of h), computes y for its 32 rows and
+//               every pair of its slot, and takes a ticket of its row block;
+//               the CTA that takes the last ticket of a block forms
+//               out = R + y_shared + sum_s w_s y_s for those rows, in slot
+//               order (no atomics on the data; the result does not depend on
+//               which CTA combines).
+// Every wait (copies, counters) gives up after a bounded time, records
+// QMOE_ERR_TIMEOUT and leaves the CTA with no copy in flight.
+#include <atomic>
+
 #include "kernels.cuh"
 #include "tc.cuh"
 
 namespace qmoe {
 
-constexpr int DEC_THREADS = 256;
+constexpr int RT_THREADS = 256;
 constexpr int RT_EPC = 8;  // router: experts per CTA
 constexpr int RT_HQ = 4;   // router: parts of H (CTAs per expert group)
-constexpr int DEC_FROWS = 32;   // intermediate rows per gate/up CTA
-constexpr int DEC_HROWS = 8;    // output rows per down CTA
+
+constexpr int DX_THREADS = 512;
+constexpr int DX_WARPS = DX_THREADS / 32;
+constexpr int DX_UPS = 8;    // gate/up units per ring stage: one row per warp
+constexpr int DX_NSTG = 4;   // gate/up ring stages
+constexpr int DX_DR = 32;    // output rows per down unit: two per warp
+constexpr int DX_NSTD = 4;   // down ring stages
+constexpr int DX_MAXT = 4;
+constexpr int DX_MAXK = 16;
+constexpr int DX_MAXSLOT = DX_MAXT * DX_MAXK + 1;
 
 struct DecodeArgs {
   const float* X;
@@ -49,124 +71,165 @@ struct DecodeArgs {
   float* ybuf;     // [T*k + T][H]
   int32_t* ids;    // [T][k]
   float* w;        // [T][k]
-  int32_t* route;  // record: [0] n_distinct, [1..] distinct experts (T*k entries)
+  int* sync;       // [DX_MAXSLOT] h counters per slot, then [H / DX_DR] combine tickets
   int* status;
+  unsigned long long wait_ns;  // a wait gives up after this many nanoseconds
+  int fault;                   // test-only: 1 = CTA 0 withholds the copy of its last down unit
 };
 
-// ---------------------------------------------------------------------------
-// routing shared by K2 and K3: logits from the partials (fixed order), top-k
-// per row (lower index on ties), distinct selected experts in ascending order.
-// ---------------------------------------------------------------------------
-struct RouteSmem {
-  int32_t ids[4 * 16];
-  float w[4 * 16];
-  int32_t distinct[4 * 16];
-  int32_t n_distinct;
-};
+// ---------------------------------------------------------------- waits
 
-// ---------------------------------------------------------------------------
-// K1b: routing, once, in one CTA: logits from the 4 partials (fixed order),
-// top-k by rank, weights, the ascending list of distinct selected experts.
-// The record (ids and w to the workspace, distinct list to ``route``) is read
-// by every CTA of the next two kernels.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(DEC_THREADS) decode_route_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  float* logits = reinterpret_cast<float*>(smem);                       // [T][E]
-  int32_t* mark = reinterpret_cast<int32_t*>(logits + (size_t)a.T * a.E);  // [E]
-  __shared__ float sel_l[4 * 16];
-  __shared__ int32_t sel_e[4 * 16];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int T = a.T, E = a.E, k = a.k;
-  tc::grid_dep_wait();  // the router's partials are complete
-  tc::grid_dep_launch();
-  for (int i = tid; i < T * E; i += DEC_THREADS) {
-    float v[RT_HQ];
-#pragma unroll
-    for (int q = 0; q < RT_HQ; ++q) v[q] = __ldcg(a.logits + (size_t)q * T * E + i);
-    float sum = 0.f;
-#pragma unroll
-    for (int q = 0; q < RT_HQ; ++q) sum += v[q];
-    logits[i] = (sum == sum) ? sum : -INFINITY;  // NaN sorts last
-  }
-  for (int e = tid; e < E; e += DEC_THREADS) mark[e] = 0;
-  __syncthreads();
-  // top-k by rank: the thread of expert e counts the experts that come before
-  // it (larger logit first, lower index on ties), stopping once the count
-  // reaches k; a count below k is e's slot
-  for (int t = 0; t < T; ++t) {
-    const float* L = logits + t * E;
-    for (int e = tid; e < E; e += DEC_THREADS) {
-      const float v = L[e];
-      int cnt = 0;
-      for (int j0 = 0; j0 < E && cnt < k; j0 += 4) {
-        const float4 q = *reinterpret_cast<const float4*>(L + j0);
-        cnt += (q.x > v || (q.x == v && j0 < e)) + (q.y > v || (q.y == v && j0 + 1 < e)) +
-               (q.z > v || (q.z == v && j0 + 2 < e)) + (q.w > v || (q.w == v && j0 + 3 < e));
-      }
-      if (cnt < k) {
-        sel_e[t * k + cnt] = e;
-        sel_l[t * k + cnt] = v;
-      }
-    }
-  }
-  __syncthreads();
-  if (tid < T * k) {
-    const int t = tid / k;
-    const float l0 = sel_l[t * k];
-    float den = 0.f;
-    for (int r = 0; r < k; ++r) den += expf(sel_l[t * k + r] - l0);
-    a.ids[tid] = sel_e[tid];
-    a.w[tid] = expf(sel_l[tid] - l0) / den;
-    mark[sel_e[tid]] = 1;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int run = 0;
-    for (int b = 0; b < E; b += 32) {
-      const int e = b + lane;
-      const int m = (e < E) ? mark[e] : 0;
-      const unsigned bal = __ballot_sync(0xffffffffu, m);
-      if (m) a.route[1 + run + __popc(bal & ((1u << lane) - 1u))] = e;
-      run += __popc(bal);
-    }
-    if (lane == 0) a.route[0] = run;
+__device__ __forceinline__ uint64_t gtime() { return tc::global_ns(); }
+
+// Waits for the phase of ``parity`` of ``bar``; false after ``limit`` ns.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, uint64_t limit) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = gtime();
+  for (uint32_t i = 1;; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0 && gtime() - t0 > limit) return false;
   }
 }
 
-// Reads the routing record into shared memory (called after the PDL wait that
-// makes the routing grid's writes visible).
-__device__ void load_route(const DecodeArgs& a, RouteSmem& rs) {
-  const int tid = threadIdx.x;
-  const int P = a.T * a.k;
-  for (int p = tid; p < P; p += DEC_THREADS) {
-    rs.ids[p] = __ldcg(a.ids + p);
-    rs.w[p] = __ldcg(a.w + p);
+// Waits until *p >= target (acquire); false after ``limit`` ns.
+__device__ __forceinline__ bool wait_count(const int* p, int target, uint64_t limit) {
+  const uint64_t t0 = gtime();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (gtime() - t0 > limit) return false;
+    __nanosleep(32);
   }
-  if (tid == 0) rs.n_distinct = __ldcg(a.route);
-  __syncthreads();
-  for (int i = tid; i < rs.n_distinct; i += DEC_THREADS) rs.distinct[i] = __ldcg(a.route + 1 + i);
-  __syncthreads();
 }
 
-__device__ __forceinline__ bool wait_copies(uint64_t* bar, int* status) {
-  for (uint32_t i = 0; i < tc::kMaxPolls; ++i)
-    if (tc::mbar_try_wait(bar, 0)) return true;
-  record_status(status, QMOE_ERR_TIMEOUT);
-  return false;
+// ---------------------------------------------------------------- arithmetic
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
+__device__ __forceinline__ float sum2(uint64_t v) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+  return __uint_as_float(lo) + __uint_as_float(hi);
+}
+
+// S = sum over the 8 NW weights of ``w`` of (0.5 + q_i/256) * x_i. Word n
+// holds weights 8n..8n+7 (byte b: weight 8n+2b in the low nibble, 8n+2b+1 in
+// the high one); for Q5_K bit i of ``hb`` is weight i's fifth bit. Each quant
+// is placed by one byte permute into the mantissa of a float whose exponent
+// makes it 0.5 + q/256 exactly (no int->float conversion), and the pairs of
+// weights (8n+2b, 8n+2b+1) meet their activation pairs x2[4n+b] in one
+// two-lane fp32 FMA (each lane rounds as fmaf does).
+template <int QT, int NW>
+__device__ __forceinline__ float dot_words(const uint32_t* w, uint32_t hb, const uint64_t* x2) {
+  uint64_t acc = 0;  // (0.0f, 0.0f)
+#pragma unroll
+  for (int n = 0; n < NW; ++n) {
+    uint32_t ev = w[n] & 0x0F0F0F0Fu;
+    uint32_t od = (w[n] >> 4) & 0x0F0F0F0Fu;
+    if (QT == QMOE_Q5K) {
+      ev |= spread4(hb >> (8 * n), 0);
+      od |= spread4(hb >> (8 * n), 1);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t sel = 0x7044u | ((uint32_t)b << 8);
+      const uint64_t q2 = pack2(__byte_perm(ev, 0x3F000000u, sel), __byte_perm(od, 0x3F000000u, sel));
+      acc = ffma2(q2, x2[4 * n + b], acc);
+    }
+  }
+  return sum2(acc);
+}
+
+__device__ __forceinline__ KHeader header_of(const uint4 hv) {
+  KHeader hd;
+  const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
+  hd.d = dd.x;
+  hd.dmin = dd.y;
+  hd.f0 = hv.y;
+  hd.f1 = hv.z;
+  hd.f2 = hv.w;
+  return hd;
+}
+
+// x . row for one packed row of H = 1024 SL weights in shared memory: lane l
+// takes sub-blocks l + 32 j, whose activations it holds in ``x2`` (pairs) and
+// their sums in ``xs``; the warp adds the lanes in a fixed butterfly order.
+template <int SL, int QT>
+__device__ __forceinline__ float gate_row_dot(const uint8_t* row, const uint64_t (&x2)[SL][16], const float (&xs)[SL],
+                                              int lane) {
+  constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < SL; ++j) {
+    const int c = lane + 32 * j;
+    const uint8_t* blk = row + (size_t)(c >> 3) * BYTES;
+    const int sj = c & 7;
+    const KHeader hd = header_of(*reinterpret_cast<const uint4*>(blk));
+    const uint4 qv = *reinterpret_cast<const uint4*>(blk + quant_offset(QT, sj));
+    const uint32_t hb = QT == QMOE_Q5K ? *reinterpret_cast<const uint32_t*>(blk + 16 + 4 * sj) : 0u;
+    const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+    acc += sub_contrib(dot_words<QT, 4>(w, hb, x2[j]), xs[j], sub_scale(hd, sj));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  return acc;
+}
+
+// h . row for one packed down row of F = 32 FSUB weights: LPS = 32 / FSUB
+// lanes per sub-block, each taking 32 / LPS consecutive weights of it.
+template <int FSUB, int QT>
+__device__ __forceinline__ float down_row_dot(const uint8_t* row, const float* h, int lane) {
+  constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
+  constexpr int LPS = 32 / FSUB;   // 2 (F = 512) or 4 (F = 256)
+  constexpr int WPL = 32 / LPS;    // weights per lane: 16 or 8
+  constexpr int NW = WPL / 8;      // quant words per lane
+  const int c = lane / LPS, p = lane % LPS;
+  const uint8_t* blk = row + (size_t)(c >> 3) * BYTES;
+  const int sj = c & 7;
+  const KHeader hd = header_of(*reinterpret_cast<const uint4*>(blk));
+  uint32_t w[NW];
+  const uint32_t* qp = reinterpret_cast<const uint32_t*>(blk + quant_offset(QT, sj) + p * (WPL / 2));
+#pragma unroll
+  for (int n = 0; n < NW; ++n) w[n] = qp[n];
+  const uint32_t hb = QT == QMOE_Q5K ? (*reinterpret_cast<const uint32_t*>(blk + 16 + 4 * sj) >> (p * WPL)) : 0u;
+  const uint64_t* h2 = reinterpret_cast<const uint64_t*>(h + c * 32 + p * WPL);
+  uint64_t x2[WPL / 2];
+  float hs = 0.f;
+#pragma unroll
+  for (int i = 0; i < WPL / 2; ++i) {
+    x2[i] = h2[i];
+    hs += sum2(x2[i]);
+  }
+  float acc = sub_contrib(dot_words<QT, NW>(w, hb, x2), hs, sub_scale(hd, sj));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  return acc;
 }
 
 // ---------------------------------------------------------------------------
 // K1: router partial logits. CTA (g, q) owns experts 8g..8g+7 and rows
 // [q H/4, (q+1) H/4); thread i loads rows i + 256j of that quarter (32 bytes
 // each) before the dependency wait, multiplies them with x after it, and the
-// CTA reduces over its 8 warps in a fixed order.
+// CTA reduces over its 8 warps in a fixed order. CTA 0 clears the expert
+// kernel's counters (after the wait: the previous expert kernel, which used
+// them, has completed).
 // ---------------------------------------------------------------------------
 template <int RPT>  // Wr rows per thread = H / (256 * RT_HQ)
-__global__ void __launch_bounds__(DEC_THREADS) decode_router_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(RT_THREADS) decode_router_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   float* xs = reinterpret_cast<float*>(smem);  // [T][H]
-  __shared__ float red[8][4][RT_EPC];
+  __shared__ float red[8][DX_MAXT][RT_EPC];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H, E = a.E, T = a.T;
   const int e0 = (blockIdx.x / RT_HQ) * RT_EPC, hq = blockIdx.x % RT_HQ;
@@ -180,7 +243,9 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_router_kernel(DecodeArgs a
   }
   tc::grid_dep_wait();    // X may come from the previous grid
   tc::grid_dep_launch();
-  for (int i = tid; i < T * H / 4; i += DEC_THREADS)
+  if (blockIdx.x == 0)
+    for (int i = tid; i < DX_MAXSLOT + H / DX_DR; i += RT_THREADS) a.sync[i] = 0;
+  for (int i = tid; i < T * H / 4; i += RT_THREADS)
     reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(a.X) + i);
   __syncthreads();
   for (int t = 0; t < T; ++t) {
@@ -217,259 +282,347 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_router_kernel(DecodeArgs a
 }
 
 // ---------------------------------------------------------------------------
-// K2: gate/up + SwiGLU for one (expert slot, 32 intermediate rows). The rows
-// arrive in 4 stages of 8 gate + 8 up rows, each on its own mbarrier, so the
-// warps compute a stage while the next ones stream in. Warp w owns gate row
-// 8s+w and up row 8s+w of stage s and produces h for that row itself.
+// K2: the experts. See the top of the file.
 // ---------------------------------------------------------------------------
-constexpr int DEC_STAGES = 4;
+struct DxShared {
+  uint64_t bar_sh;               // the shared expert's gate/up rows
+  uint64_t bar_g[DX_NSTG];       // gate/up ring
+  uint64_t bar_d[DX_NSTD];       // down ring
+  float sel_l[DX_MAXT * DX_MAXK];
+  int32_t sel_e[DX_MAXT * DX_MAXK];
+  float wts[DX_MAXT * DX_MAXK];
+  int32_t slot_e[DX_MAXSLOT];           // expert of each slot (E = shared)
+  int32_t pair_of[DX_MAXSLOT][DX_MAXT]; // pair index of (slot, row), -1 if the row does not use the slot
+  float gu[2][DX_UPS][DX_MAXT];         // gate / up dot products of a stage
+  float ys[DX_MAXT][DX_DR];             // y of a down unit
+  int32_t n_slots;
+  int32_t wflag;  // a counter wait succeeded
+  int32_t cflag;  // this CTA combines the current row block
+};
 
-template <int NSUB, int QT>
-__device__ __forceinline__ float row_dot_warp(const uint8_t* row, const float (&xv)[NSUB / 32 > 0 ? NSUB / 32 : 1][32],
-                                              const float (&xs)[NSUB / 32 > 0 ? NSUB / 32 : 1], int lane) {
-  constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
-  constexpr int SL = NSUB / 32;
-  float acc = 0.f;
-#pragma unroll
-  for (int j = 0; j < SL; ++j) {
-    const int c = lane + 32 * j;
-    const uint8_t* blk = row + (size_t)(c >> 3) * BYTES;
-    const int sj = c & 7;
-    const uint4 hv = *reinterpret_cast<const uint4*>(blk);
-    KHeader hd;
-    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
-    hd.d = dd.x;
-    hd.dmin = dd.y;
-    hd.f0 = hv.y;
-    hd.f1 = hv.z;
-    hd.f2 = hv.w;
-    const uint4 qv = *reinterpret_cast<const uint4*>(blk + quant_offset(QT, sj));
-    const uint32_t hb = QT == QMOE_Q5K ? *reinterpret_cast<const uint32_t*>(blk + 16 + 4 * sj) : 0u;
-    acc += sub_contrib(dot_sub_prmt<QT>(qv, hb, xv[j]), xs[j], sub_scale(hd, sj));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  return acc;
-}
+// Bytes of one gate/up unit (a gate row and an up row) and of one down row.
+__host__ __device__ constexpr int dx_unit_bytes(int H, int qt) { return 2 * (H / QK) * (qt == QMOE_Q5K ? 176 : 144); }
+__host__ __device__ constexpr int dx_drow_bytes(int F, int qt) { return (F / QK) * (qt == QMOE_Q5K ? 176 : 144); }
 
-template <int NSUB, int QT>
-__global__ void __launch_bounds__(DEC_THREADS) decode_gateup_kernel(DecodeArgs a) {
-  static_assert(NSUB >= 32, "decode gate/up needs H >= 1024");
+template <int SL, int FSUB, int GQ, int DQ>
+__global__ void __launch_bounds__(DX_THREADS, 1) decode_experts_kernel(DecodeArgs a) {
+  constexpr int H = 1024 * SL;
+  constexpr int F = 32 * FSUB;
+  constexpr int NBLK = H / DX_DR;
+  constexpr int RB = (H / QK) * (GQ == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES);   // one gate or up row
+  constexpr int DRB = (F / QK) * (DQ == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES);  // one down row
+  constexpr int STG = 2 * DX_UPS * RB;   // gate/up stage: UPS gate rows, then UPS up rows
+  constexpr int DSTG = DX_DR * DRB;      // down stage
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar[DEC_STAGES];
-  __shared__ RouteSmem rs;
-  __shared__ int32_t pairs[4];
-  __shared__ int32_t n_pairs;
-  constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
-  constexpr int H = NSUB * SUBK;
-  constexpr int SL = NSUB / 32;
-  constexpr int RPS = DEC_FROWS / DEC_STAGES;  // gate rows (and up rows) per stage: 8
+  __shared__ DxShared S;
+  const int T = a.T, k = a.k, E = a.E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int F = a.F, T = a.T, k = a.k, E = a.E;
-  const int FCH = F / DEC_FROWS;
-  const int slot = blockIdx.x / FCH, fc = blockIdx.x % FCH;
-  constexpr size_t row_bytes = (size_t)(H / QK) * BYTES;
-  constexpr uint32_t stage_rows_bytes = (uint32_t)(RPS * row_bytes);
-  uint8_t* wgs = smem;                                   // 32 gate rows
-  uint8_t* wus = smem + DEC_FROWS * row_bytes;           // 32 up rows
-  const bool is_shared = a.has_shared && slot == 0;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const uint64_t lim = a.wait_ns;
+  uint8_t* sh_rows = smem;                                   // shared expert units [STG]
+  uint8_t* ring_g = sh_rows + STG;                           // [DX_NSTG][STG]
+  uint8_t* ring_d = ring_g + DX_NSTG * STG;                  // [DX_NSTD][DSTG]
+  float* xsm = reinterpret_cast<float*>(ring_d + DX_NSTD * DSTG);  // [T][H]
+  float* hsm = xsm + T * H;                                  // [T][F]
+
+  // shared expert units of this CTA: rows [fs0, fs1)
+  const int fs0 = a.has_shared ? (int)((long long)cta * F / G) : 0;
+  const int fs1 = a.has_shared ? (int)((long long)(cta + 1) * F / G) : 0;
   if (tid == 0) {
-    for (int i = 0; i < DEC_STAGES; ++i) tc::mbar_init(&bar[i], 1);
+    tc::mbar_init(&S.bar_sh, 1);
+    for (int i = 0; i < DX_NSTG; ++i) tc::mbar_init(&S.bar_g[i], 1);
+    for (int i = 0; i < DX_NSTD; ++i) tc::mbar_init(&S.bar_d[i], 1);
     tc::fence_barrier_init();
+    if (fs1 > fs0) {
+      // the shared expert's weights do not depend on the routing: their copies
+      // start before the wait for the router
+      const uint32_t n = (uint32_t)((fs1 - fs0) * RB);
+      tc::mbar_expect_tx(&S.bar_sh, 2 * n);
+      tc::bulk_g2s(sh_rows, a.Sg + (size_t)fs0 * RB, n, &S.bar_sh);
+      tc::bulk_g2s(sh_rows + DX_UPS * RB, a.Su + (size_t)fs0 * RB, n, &S.bar_sh);
+    }
+  }
+  tc::grid_dep_wait();  // the router's partials, cleared counters and X are visible
+  __syncthreads();
+
+  // ---------------------------------------------------------------- routing
+  // logits from the 4 partials in a fixed order (NaN ranks below -inf's
+  // index order: it is mapped to -inf), then the top-k by rank: the thread of
+  // (row t, expert e) counts the experts ordered before e (larger logit, or
+  // equal logit and lower index) and stops at k; a count below k is e's slot.
+  float* lg = hsm;  // [T][E] logits, in the h staging area (not yet in use)
+  for (int i = tid; i < T * E; i += DX_THREADS) {
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < RT_HQ; ++q) v += __ldcg(a.logits + (size_t)q * T * E + i);
+    lg[i] = (v == v) ? v : -INFINITY;
+  }
+  for (int i = tid; i < T * H / 4; i += DX_THREADS)
+    reinterpret_cast<float4*>(xsm)[i] = __ldcg(reinterpret_cast<const float4*>(a.X) + i);
+  __syncthreads();
+  for (int i = tid; i < T * E; i += DX_THREADS) {
+    const int t = i / E, e = i % E;
+    const float* L = lg + t * E;
+    const float v = L[e];
+    int cnt = 0;
+    for (int j0 = 0; j0 < E && cnt < k; j0 += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(L + j0);
+      cnt += (q.x > v || (q.x == v && j0 < e)) + (q.y > v || (q.y == v && j0 + 1 < e)) +
+             (q.z > v || (q.z == v && j0 + 2 < e)) + (q.w > v || (q.w == v && j0 + 3 < e));
+    }
+    if (cnt < k) {
+      S.sel_e[t * k + cnt] = e;
+      S.sel_l[t * k + cnt] = v;
+    }
   }
   __syncthreads();
-  // warp 0 issues the 8 copies (4 stages x gate/up) from 8 lanes, after lanes
-  // 0..3 have set each stage's expected byte count
-  auto issue = [&](const uint8_t* gsrc, const uint8_t* usrc) {
-    if (lane < DEC_STAGES) tc::mbar_expect_tx(&bar[lane], 2 * stage_rows_bytes);
-    __syncwarp();
-    if (lane < 2 * DEC_STAGES) {
-      const int st = lane >> 1;
-      const uint8_t* src = (lane & 1) ? usrc : gsrc;
-      uint8_t* dst = (lane & 1) ? wus : wgs;
-      tc::bulk_g2s(dst + st * stage_rows_bytes, src + st * stage_rows_bytes, stage_rows_bytes, &bar[st]);
+  if (tid < T * k) {
+    const int t = tid / k;
+    const float l0 = S.sel_l[t * k];
+    float den = 0.f;
+    for (int r = 0; r < k; ++r) den += expf(S.sel_l[t * k + r] - l0);
+    S.wts[tid] = expf(S.sel_l[tid] - l0) / den;
+    if (cta == 0) {
+      a.ids[tid] = S.sel_e[tid];
+      a.w[tid] = S.wts[tid];
+    }
+  }
+  // slots: the shared expert first, then the distinct selected experts in
+  // ascending order (warp 0 compacts a mark per expert)
+  int* mark = reinterpret_cast<int*>(lg + T * E);  // [E], after the logits
+  for (int e = tid; e < E; e += DX_THREADS) mark[e] = 0;
+  __syncthreads();
+  if (tid < T * k) mark[S.sel_e[tid]] = 1;
+  __syncthreads();
+  if (warp == 0) {
+    int run = a.has_shared;
+    if (a.has_shared && lane == 0) S.slot_e[0] = E;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      const int m = (e < E) ? mark[e] : 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, m);
+      if (m) S.slot_e[run + __popc(bal & ((1u << lane) - 1u))] = e;
+      run += __popc(bal);
+    }
+    if (lane == 0) S.n_slots = run;
+  }
+  __syncthreads();
+  const int ns = S.n_slots;
+  for (int i = tid; i < ns * DX_MAXT; i += DX_THREADS) {
+    const int u = i / DX_MAXT, t = i % DX_MAXT;
+    int p = -1;
+    if (t < T) {
+      const int e = S.slot_e[u];
+      if (e == E) {
+        p = T * k + t;
+      } else {
+        for (int s = 0; s < k; ++s)
+          if (S.sel_e[t * k + s] == e) p = t * k + s;
+      }
+    }
+    S.pair_of[u][t] = p;
+  }
+
+  // this CTA's routed gate/up units [r0, r1) of U*F (slot has_shared + r / F,
+  // row r % F) and down units [d0, d1) of ns * NBLK (slot d / NBLK, block d % NBLK)
+  const int U = ns - a.has_shared;
+  const int NR = U * F, ND = ns * NBLK;
+  const int r0 = (int)((long long)cta * NR / G), r1 = (int)((long long)(cta + 1) * NR / G);
+  const int d0 = (int)((long long)cta * ND / G), d1 = (int)((long long)(cta + 1) * ND / G);
+  const int n_gs = (r1 - r0 + DX_UPS - 1) / DX_UPS;  // routed gate/up stages
+  const int n_du = d1 - d0;
+
+  auto issue_gate_stage = [&](int s) {
+    const int slot = s % DX_NSTG;
+    const int u0 = r0 + s * DX_UPS, u1 = min(r1, u0 + DX_UPS);
+    uint8_t* dst = ring_g + (size_t)slot * STG;
+    tc::mbar_expect_tx(&S.bar_g[slot], (uint32_t)(2 * (u1 - u0) * RB));
+    for (int u = u0; u < u1;) {
+      const int sl = a.has_shared + u / F, f = u % F;
+      const int n = min(u1 - u, F - f);  // rows of this slot in the stage
+      const int e = S.slot_e[sl];
+      const size_t src = ((size_t)e * F + f) * RB;
+      tc::bulk_g2s(dst + (size_t)(u - u0) * RB, a.Wg + src, (uint32_t)(n * RB), &S.bar_g[slot]);
+      tc::bulk_g2s(dst + (size_t)(DX_UPS + u - u0) * RB, a.Wu + src, (uint32_t)(n * RB), &S.bar_g[slot]);
+      u += n;
     }
   };
-  const size_t chunk_off = (size_t)fc * DEC_FROWS * row_bytes;
-  if (is_shared && warp == 0) issue(a.Sg + chunk_off, a.Su + chunk_off);
-  tc::grid_dep_wait();     // the routing record (and X) are complete
-  tc::grid_dep_launch();
-  load_route(a, rs);
-  int e = a.E;  // shared
-  if (!is_shared) {
-    const int ri = slot - a.has_shared;
-    if (ri >= rs.n_distinct) return;  // this CTA issued no copies
-    e = rs.distinct[ri];
-    if (warp == 0) {
-      const size_t eoff = (size_t)e * F * row_bytes + chunk_off;
-      issue(a.Wg + eoff, a.Wu + eoff);
-    }
-  }
-  if (tid == 0) {
-    int n = 0;
-    for (int t = 0; t < T; ++t) {
-      if (is_shared) {
-        pairs[n++] = T * k + t;
-      } else {
-        for (int s2 = 0; s2 < k; ++s2)
-          if (rs.ids[t * k + s2] == e) pairs[n++] = t * k + s2;
-      }
-    }
-    n_pairs = n;
-  }
+  auto issue_down_unit = [&](int i) {
+    const int slot = i % DX_NSTD;
+    const int d = d0 + i, sl = d / NBLK, b = d % NBLK;
+    const int e = S.slot_e[sl];
+    const uint8_t* src = (e == E ? a.Sd : a.Wd + (size_t)e * H * DRB) + (size_t)b * DX_DR * DRB;
+    tc::mbar_expect_tx(&S.bar_d[slot], (uint32_t)DSTG);
+    // test-only fault: the last down unit of CTA 0 is never copied, so its
+    // wait runs out (nothing else of this CTA is in flight by then)
+    if (!(a.fault == 1 && cta == 0 && i == n_du - 1))
+      tc::bulk_g2s(ring_d + (size_t)slot * DSTG, src, (uint32_t)DSTG, &S.bar_d[slot]);
+  };
   __syncthreads();
-  const int np = n_pairs;
-  // one row (pair) at a time: lane l holds the activations of sub-blocks
-  // l + 32j; the stages are waited in order (a completed stage stays complete)
-  for (int pi = 0; pi < np; ++pi) {
-    const int pair = pairs[pi];
-    const int t = pair < T * k ? pair / k : pair - T * k;
-    float xv[SL][32];
-    float xs[SL];
+  // ring bookkeeping: stages / units issued (thread 0) and consumed (all)
+  int g_iss = 0, d_iss = 0, g_cons = 0, d_cons = 0;
+  bool sh_cons = !(fs1 > fs0);
+  if (tid == 0) {
+    for (; g_iss < min(n_gs, DX_NSTG); ++g_iss) issue_gate_stage(g_iss);
+    for (; d_iss < min(n_du, DX_NSTD); ++d_iss) issue_down_unit(d_iss);
+  }
+  // the next layer's router may start loading its weights now
+  tc::grid_dep_launch();
+
+  // ---------------------------------------------------------------- gate/up
+  // activations of row ``xt`` for the lane's sub-blocks, as fp32 pairs
+  uint64_t x2[SL][16];
+  float xsum[SL];
+  int xt = -1;
+  auto load_x = [&](int t) {
 #pragma unroll
     for (int j = 0; j < SL; ++j) {
-      const float4* x4 = reinterpret_cast<const float4*>(a.X + (size_t)t * H + (lane + 32 * j) * SUBK);
-      float sum = 0.f;
+      const uint64_t* src = reinterpret_cast<const uint64_t*>(xsm + (size_t)t * H + (lane + 32 * j) * SUBK);
+      float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 v = __ldg(x4 + i);
-        xv[j][4 * i] = v.x;
-        xv[j][4 * i + 1] = v.y;
-        xv[j][4 * i + 2] = v.z;
-        xv[j][4 * i + 3] = v.w;
-        sum += (v.x + v.y) + (v.z + v.w);
+      for (int i = 0; i < 16; ++i) {
+        x2[j][i] = src[i];
+        s += sum2(x2[j][i]);
       }
-      xs[j] = sum;
+      xsum[j] = s;
     }
-    for (int st = 0; st < DEC_STAGES; ++st) {
-      if (!wait_copies(&bar[st], a.status)) return;
-      const int r = st * RPS + warp;  // row within the 32-row chunk
-      const float g = row_dot_warp<NSUB, QT>(wgs + (size_t)r * row_bytes, xv, xs, lane);
-      const float u = row_dot_warp<NSUB, QT>(wus + (size_t)r * row_bytes, xv, xs, lane);
-      if (lane == 0) a.hbuf[(size_t)pair * F + fc * DEC_FROWS + r] = silu_mul(g, u);
+    xt = t;
+  };
+  bool ok = true;
+  // stage -1 is the shared expert's units (rows fs0..fs1), stages 0.. the routed ones
+  for (int s = (fs1 > fs0) ? -1 : 0; s < n_gs && ok; ++s) {
+    const uint8_t* base;
+    int nu, slot_first, f_first;
+    if (s < 0) {
+      ok = __syncthreads_and(wait_bar(&S.bar_sh, 0, lim));
+      sh_cons = ok;
+      base = sh_rows;
+      nu = fs1 - fs0;
+      slot_first = 0;
+      f_first = fs0;
+    } else {
+      ok = __syncthreads_and(wait_bar(&S.bar_g[s % DX_NSTG], (s / DX_NSTG) & 1, lim));
+      if (ok) g_cons = s + 1;
+      base = ring_g + (size_t)(s % DX_NSTG) * STG;
+      const int u0 = r0 + s * DX_UPS;
+      nu = min(r1 - u0, DX_UPS);
+      slot_first = a.has_shared + u0 / F;
+      f_first = u0 % F;
     }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// K3: down projection of 8 output rows for every selected expert and the
-// shared expert, then the slot-order combine with the residual. Warp w owns
-// output row r0 + w; lanes split a row's sub-blocks (G lanes per pair, 32/G
-// pairs per pass).
-// ---------------------------------------------------------------------------
-template <int NSUBD, int QT>
-__global__ void __launch_bounds__(DEC_THREADS) decode_down_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ RouteSmem rs;
-  __shared__ int32_t slot_of[4 * 16 + 4];
-  __shared__ float ys[(4 * 16 + 4) * DEC_HROWS];
-  constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
-  constexpr int F = NSUBD * SUBK;
-  constexpr int G = NSUBD < 32 ? NSUBD : 32;  // lanes per (pair, row)
-  constexpr int PPP = 32 / G;                 // pairs per pass
-  constexpr int SL = NSUBD / G;               // sub-blocks per lane
-  constexpr size_t row_bytes = (size_t)(F / QK) * BYTES;
-  constexpr uint32_t blk_bytes = (uint32_t)(DEC_HROWS * row_bytes);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int H = a.H, T = a.T, k = a.k, E = a.E;
-  const int r0 = blockIdx.x * DEC_HROWS;
-  const int maxx = T * k + 1;  // experts incl. shared
-  const int P = T * k + (a.has_shared ? T : 0);
-  // h rows are staged with each 32-float sub-block padded to 36 floats, so
-  // that the 8 lanes of a quarter-warp reading 8 different sub-blocks of a row
-  // hit 8 different bank groups
-  constexpr int HSTRIDE = NSUBD * 36;
-  uint8_t* wsm = smem;                                                       // [maxx][8 rows]
-  float* hs = reinterpret_cast<float*>(smem + (size_t)maxx * blk_bytes);    // [P][NSUBD][36]
-  if (tid == 0) {
-    tc::mbar_init(&bar, 1);
-    tc::fence_barrier_init();
-  }
-  __syncthreads();
-  // the routing grid completed before the gate/up grid let this one launch
-  load_route(a, rs);
-  const int nd = rs.n_distinct;
-  if (warp == 0) {
-    // one copy per lane: 8 rows of every selected expert's down matrix, and
-    // of the shared expert's
-    const int nx = nd + (a.has_shared ? 1 : 0);
-    if (lane == 0) tc::mbar_expect_tx(&bar, nx * blk_bytes);
-    __syncwarp();
-    for (int i = lane; i < nx; i += 32) {
-      const uint8_t* src = i < nd ? a.Wd + ((size_t)rs.distinct[i] * H + r0) * row_bytes : a.Sd + (size_t)r0 * row_bytes;
-      tc::bulk_g2s(wsm + (size_t)i * blk_bytes, src, blk_bytes, &bar);
-    }
-  }
-  for (int p = tid; p < P; p += DEC_THREADS) {
-    int sl = nd;  // shared
-    if (p < T * k) {
-      const int e = rs.ids[p];
-      for (int i = 0; i < nd; ++i)
-        if (rs.distinct[i] == e) sl = i;
-    }
-    slot_of[p] = sl;
-  }
-  tc::grid_dep_wait();     // h from the gate/up grid is complete
-  tc::grid_dep_launch();
-  for (int i = tid; i < P * F / 4; i += DEC_THREADS) {
-    const int p = i / (F / 4), rem = i % (F / 4);
-    reinterpret_cast<float4*>(hs + (size_t)p * HSTRIDE + (rem >> 3) * 36)[rem & 7] =
-        __ldcg(reinterpret_cast<const float4*>(a.hbuf) + i);
-  }
-  __syncthreads();
-  if (!wait_copies(&bar, a.status)) return;
-
-  const int row = warp;  // 8 warps, 8 rows
-  const int sub_lane = lane % G, pair_lane = lane / G;
-  for (int p0 = 0; p0 < P; p0 += PPP) {
-    const int p = p0 + pair_lane;
-    float acc = 0.f;
-    if (p < P) {
-      const uint8_t* rowp = wsm + (size_t)slot_of[p] * blk_bytes + (size_t)row * row_bytes;
-#pragma unroll
-      for (int j = 0; j < SL; ++j) {
-        const int c = sub_lane + G * j;
-        const uint8_t* blk = rowp + (size_t)(c >> 3) * BYTES;
-        const int sj = c & 7;
-        const uint4 hv = *reinterpret_cast<const uint4*>(blk);
-        KHeader hd;
-        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
-        hd.d = dd.x;
-        hd.dmin = dd.y;
-        hd.f0 = hv.y;
-        hd.f1 = hv.z;
-        hd.f2 = hv.w;
-        const uint4 qv = *reinterpret_cast<const uint4*>(blk + quant_offset(QT, sj));
-        const uint32_t hb = QT == QMOE_Q5K ? *reinterpret_cast<const uint32_t*>(blk + 16 + 4 * sj) : 0u;
-        const float4* x4 = reinterpret_cast<const float4*>(hs + (size_t)p * HSTRIDE + c * 36);
-        float xv[32], xsum = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v = x4[i];
-          xv[4 * i] = v.x;
-          xv[4 * i + 1] = v.y;
-          xv[4 * i + 2] = v.z;
-          xv[4 * i + 3] = v.w;
-          xsum += (v.x + v.y) + (v.z + v.w);
-        }
-        acc += sub_contrib(dot_sub_prmt<QT>(qv, hb, xv), xsum, sub_scale(hd, sj));
+    if (!ok) break;
+    // warp w: unit w % UPS, matrix w / UPS (0 gate, 1 up)
+    const int j = warp % DX_UPS, mat = warp / DX_UPS;
+    if (j < nu) {
+      // a stage holds at most two slots (UPS <= F)
+      const int f = f_first + j;
+      const int sl = f < F ? slot_first : slot_first + 1;
+      const uint8_t* row = base + (size_t)(mat * DX_UPS + j) * RB;
+      for (int t = 0; t < T; ++t) {
+        if (S.pair_of[sl][t] < 0) continue;
+        if (t != xt) load_x(t);
+        const float v = gate_row_dot<SL, GQ>(row, x2, xsum, lane);
+        if (lane == 0) S.gu[mat][j][t] = v;
       }
     }
-#pragma unroll
-    for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (sub_lane == 0 && p < P) {
-      ys[p * DEC_HROWS + row] = acc;
-      a.ybuf[(size_t)p * H + r0 + row] = acc;
+    __syncthreads();
+    if (tid < DX_UPS * T) {
+      const int jj = tid / T, t = tid % T;
+      if (jj < nu) {
+        const int f = f_first + jj;
+        const int sl = f < F ? slot_first : slot_first + 1;
+        const int p = S.pair_of[sl][t];
+        if (p >= 0) a.hbuf[(size_t)p * F + (f < F ? f : f - F)] = silu_mul(S.gu[0][jj][t], S.gu[1][jj][t]);
+      }
+    }
+    if (tid == 0 && s >= 0 && s + DX_NSTG < n_gs) {
+      // every read of this ring stage is done (barrier above)
+      tc::fence_proxy_async_smem();
+      issue_gate_stage(g_iss++);
+    }
+    __syncthreads();
+  }
+  // publish this CTA's h rows per slot
+  __threadfence();
+  __syncthreads();
+  if (ok && tid == 0) {
+    if (fs1 > fs0) atomicAdd(&a.sync[0], fs1 - fs0);
+    for (int u = r0; u < r1;) {
+      const int sl = a.has_shared + u / F, n = min(r1 - u, F - u % F);
+      atomicAdd(&a.sync[sl], n);
+      u += n;
     }
   }
-  __syncthreads();
-  for (int tr = tid; tr < T * DEC_HROWS; tr += DEC_THREADS) {
-    const int t = tr / DEC_HROWS, r = tr % DEC_HROWS;
-    float acc = a.R ? a.R[(size_t)t * H + r0 + r] : 0.f;
-    if (a.has_shared) acc += ys[(T * k + t) * DEC_HROWS + r];
-    for (int s2 = 0; s2 < k; ++s2) acc = fmaf(rs.w[t * k + s2], ys[(t * k + s2) * DEC_HROWS + r], acc);
-    a.out[(size_t)t * H + r0 + r] = acc;
+
+  // ---------------------------------------------------------------- down
+  int cur = -1;
+  for (int i = 0; i < n_du && ok; ++i) {
+    const int d = d0 + i, sl = d / NBLK, b = d % NBLK;
+    if (sl != cur) {
+      // all of h for this slot: every CTA's gate/up units of it are counted
+      if (tid == 0) S.wflag = wait_count(&a.sync[sl], F, lim) ? 1 : 0;
+      __syncthreads();
+      if (!S.wflag) {
+        ok = false;
+        break;
+      }
+      for (int q = tid; q < T * F / 4; q += DX_THREADS) {
+        const int t = q / (F / 4), c = q % (F / 4);
+        const int p = S.pair_of[sl][t];
+        if (p >= 0)
+          reinterpret_cast<float4*>(hsm + (size_t)t * F)[c] = __ldcg(reinterpret_cast<const float4*>(a.hbuf + (size_t)p * F) + c);
+      }
+      cur = sl;
+    }
+    ok = __syncthreads_and(wait_bar(&S.bar_d[i % DX_NSTD], (i / DX_NSTD) & 1, lim));
+    if (!ok) break;
+    d_cons = i + 1;
+    const uint8_t* base = ring_d + (size_t)(i % DX_NSTD) * DSTG;
+#pragma unroll
+    for (int rr = 0; rr < DX_DR / DX_WARPS; ++rr) {
+      const int r = warp * (DX_DR / DX_WARPS) + rr;
+      for (int t = 0; t < T; ++t) {
+        if (S.pair_of[sl][t] < 0) continue;
+        const float v = down_row_dot<FSUB, DQ>(base + (size_t)r * DRB, hsm + (size_t)t * F, lane);
+        if (lane == 0) S.ys[t][r] = v;
+      }
+    }
+    __syncthreads();
+    if (tid < T * DX_DR) {
+      const int t = tid / DX_DR, r = tid % DX_DR;
+      const int p = S.pair_of[sl][t];
+      if (p >= 0) {
+        a.ybuf[(size_t)p * H + b * DX_DR + r] = S.ys[t][r];
+        __threadfence();
+      }
+    }
+    if (tid == 0 && i + DX_NSTD < n_du) {
+      tc::fence_proxy_async_smem();
+      issue_down_unit(d_iss++);
+    }
+    __syncthreads();
+    // one ticket per (slot, block); the CTA with the last one of the block combines
+    if (tid == 0) {
+      const int old = atomicAdd(&a.sync[DX_MAXSLOT + b], 1);
+      S.cflag = (old == ns - 1) ? 1 : 0;
+      if (S.cflag) __threadfence();
+    }
+    __syncthreads();
+    if (S.cflag && tid < T * DX_DR) {
+      const int t = tid / DX_DR, r = b * DX_DR + tid % DX_DR;
+      float acc = a.R ? a.R[(size_t)t * H + r] : 0.f;
+      if (a.has_shared) acc += __ldcg(a.ybuf + (size_t)(T * k + t) * H + r);
+      for (int s2 = 0; s2 < k; ++s2) acc = fmaf(S.wts[t * k + s2], __ldcg(a.ybuf + (size_t)(t * k + s2) * H + r), acc);
+      a.out[(size_t)t * H + r] = acc;
+    }
+  }
+  if (!ok && tid == 0) {
+    record_status(a.status, QMOE_ERR_TIMEOUT);
+    // leave with nothing in flight: wait (bounded) for every copy this CTA
+    // issued and did not consume (a copy that was never issued just runs
+    // out again)
+    if (!sh_cons) wait_bar(&S.bar_sh, 0, lim);
+    for (int s = g_cons; s < g_iss; ++s) wait_bar(&S.bar_g[s % DX_NSTG], (s / DX_NSTG) & 1, lim);
+    for (int i = d_cons; i < d_iss; ++i) wait_bar(&S.bar_d[i % DX_NSTD], (i / DX_NSTD) & 1, lim);
   }
 }
 
@@ -478,41 +631,37 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_down_kernel(DecodeArgs a) 
 // ---------------------------------------------------------------------------
 static size_t router_smem(int T, int H) { return sizeof(float) * (size_t)T * H; }
 
-static size_t gateup_smem(int T, int H, int E, int qt) {
-  const size_t row_bytes = (size_t)(H / QK) * qtype_bytes(qt);
-  return 2 * DEC_FROWS * row_bytes;
+static size_t experts_smem(int T, int H, int E, int F, int gq, int dq) {
+  const size_t stg = (size_t)DX_UPS * dx_unit_bytes(H, gq);
+  const size_t dstg = (size_t)DX_DR * dx_drow_bytes(F, dq);
+  const size_t xs = sizeof(float) * (size_t)T * H;
+  // the h staging area also holds the routing's logits and expert marks
+  size_t hs = sizeof(float) * (size_t)T * F;
+  const size_t route = sizeof(float) * (size_t)T * E + sizeof(int) * (size_t)E;
+  if (route > hs) hs = route;
+  return stg + DX_NSTG * stg + DX_NSTD * dstg + xs + hs;
 }
 
-static size_t route_smem(int T, int E) { return sizeof(float) * (size_t)T * E + sizeof(int32_t) * E; }
-
-static size_t down_smem(int T, int E, int F, int k, int qt) {
-  const size_t row_bytes = (size_t)(F / QK) * qtype_bytes(qt);
-  const int P = T * k + T;
-  return (size_t)(T * k + 1) * DEC_HROWS * row_bytes + sizeof(float) * (size_t)P * (F / SUBK) * 36;
-}
+int decode_sync_ints(int H) { return DX_MAXSLOT + H / DX_DR; }
 
 bool decode_path_supported(int T, int H, int E, int k, int F, int gate_qt, int down_qt) {
-  if (T < 1 || T > 4 || k > 8) return false;
-  if (H != 1024 && H != 2048 && H != 4096) return false;
-  if (F != 256 && F != 512 && F != 1024 && F != 2048) return false;
+  if (T < 1 || T > DX_MAXT || k > DX_MAXK) return false;
+  if (H != 1024 && H != 2048) return false;
+  if (F != 256 && F != 512) return false;
   if (E % RT_EPC != 0) return false;
-  if (router_smem(T, H) > 200 * 1024) return false;
-  if (gateup_smem(T, H, E, gate_qt) > 200 * 1024) return false;
-  if (down_smem(T, E, F, k, down_qt) > 200 * 1024) return false;
+  const int G = device_sm_count();
+  if ((F + G - 1) / G > DX_UPS) return false;  // the shared expert's units of a CTA fit one stage
+  if (experts_smem(T, H, E, F, gate_qt, down_qt) > 200 * 1024) return false;
   return true;
 }
 
-// The three kernels run concurrently: each asks for the largest shared-memory
-// carveout so that CTAs of different kernels can share an SM.
-static cudaError_t prepare_kernel(const void* fn, size_t smem) { return ensure_kernel_smem(fn, smem, 100); }
-
 template <typename K>
-static cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t st, const DecodeArgs& a) {
-  cudaError_t pe = prepare_kernel(reinterpret_cast<const void*>(kernel), smem);
-  if (pe != cudaSuccess) return pe;
+static cudaError_t launch_router(K kernel, int grid, size_t smem, cudaStream_t st, const DecodeArgs& a) {
+  cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(kernel), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(DEC_THREADS);
+  cfg.blockDim = dim3(RT_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -523,16 +672,50 @@ static cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t st, 
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-template <int NSUB>
-static cudaError_t launch_gateup_t(int qt, int grid, size_t smem, cudaStream_t st, const DecodeArgs& a) {
-  return qt == QMOE_Q5K ? launch_pdl(decode_gateup_kernel<NSUB, QMOE_Q5K>, grid, smem, st, a)
-                        : launch_pdl(decode_gateup_kernel<NSUB, QMOE_Q4K>, grid, smem, st, a);
+// Cooperative launch (every CTA resident at once: the down units wait on
+// counters other CTAs advance), one CTA per SM, programmatically dependent
+// on the router.
+template <typename K>
+static cudaError_t launch_experts(K kernel, size_t smem, cudaStream_t st, const DecodeArgs& a) {
+  cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(kernel), smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_sm_count());
+  cfg.blockDim = dim3(DX_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  // if the runtime refuses the programmatic dependency on a cooperative
+  // launch, the kernel is launched cooperatively without it (and remembered)
+  static std::atomic<int> coop_pdl{0};  // 0 untried, 1 accepted, -1 refused
+  const int mode = coop_pdl.load();
+  cfg.numAttrs = mode >= 0 ? 2 : 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, a);
+  if (mode == 0) {
+    if (e == cudaSuccess) {
+      coop_pdl.store(1);
+    } else {
+      (void)cudaGetLastError();
+      coop_pdl.store(-1);
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, kernel, a);
+    }
+  }
+  return e;
 }
 
-template <int NSUBD>
-static cudaError_t launch_down_t(int qt, int grid, size_t smem, cudaStream_t st, const DecodeArgs& a) {
-  return qt == QMOE_Q5K ? launch_pdl(decode_down_kernel<NSUBD, QMOE_Q5K>, grid, smem, st, a)
-                        : launch_pdl(decode_down_kernel<NSUBD, QMOE_Q4K>, grid, smem, st, a);
+template <int SL, int FSUB>
+static cudaError_t launch_experts_q(int gq, int dq, size_t smem, cudaStream_t st, const DecodeArgs& a) {
+  if (gq == QMOE_Q4K)
+    return dq == QMOE_Q5K ? launch_experts(decode_experts_kernel<SL, FSUB, QMOE_Q4K, QMOE_Q5K>, smem, st, a)
+                          : launch_experts(decode_experts_kernel<SL, FSUB, QMOE_Q4K, QMOE_Q4K>, smem, st, a);
+  return dq == QMOE_Q5K ? launch_experts(decode_experts_kernel<SL, FSUB, QMOE_Q5K, QMOE_Q5K>, smem, st, a)
+                        : launch_experts(decode_experts_kernel<SL, FSUB, QMOE_Q5K, QMOE_Q4K>, smem, st, a);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
@@ -540,38 +723,21 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.X = L.X; a.R = L.R; a.out = L.out; a.Wr = L.Wr;
   a.Wg = L.Wg; a.Wu = L.Wu; a.Wd = L.Wd; a.Sg = L.Sg; a.Su = L.Su; a.Sd = L.Sd;
   a.T = L.T; a.H = L.H; a.E = L.E; a.k = L.k; a.F = L.F; a.has_shared = L.Sg != nullptr;
-  a.logits = L.part; a.hbuf = L.hbuf; a.ybuf = L.ybuf; a.ids = L.ids; a.w = L.w; a.route = L.route;
-  a.status = L.status;
+  a.logits = L.part; a.hbuf = L.hbuf; a.ybuf = L.ybuf; a.ids = L.ids; a.w = L.w;
+  a.sync = L.sync; a.status = L.status;
+  a.wait_ns = L.wait_ns;
+  a.fault = L.fault;
   const int g1 = (L.E / RT_EPC) * RT_HQ;
   const size_t s1 = router_smem(L.T, L.H);
-  cudaError_t e;
-  switch (L.H) {
-    case 1024: e = launch_pdl(decode_router_kernel<1>, g1, s1, st, a); break;
-    case 2048: e = launch_pdl(decode_router_kernel<2>, g1, s1, st, a); break;
-    case 4096: e = launch_pdl(decode_router_kernel<4>, g1, s1, st, a); break;
-    default: return cudaErrorInvalidValue;
-  }
+  cudaError_t e = L.H == 1024 ? launch_router(decode_router_kernel<1>, g1, s1, st, a)
+                              : launch_router(decode_router_kernel<2>, g1, s1, st, a);
   if (e != cudaSuccess) return e;
-  if ((e = launch_pdl(decode_route_kernel, 1, route_smem(L.T, L.E), st, a)) != cudaSuccess) return e;
-  const int slots = a.has_shared + (L.T * L.k < L.E ? L.T * L.k : L.E);
-  const int g2 = slots * (L.F / DEC_FROWS);
-  const size_t s2 = gateup_smem(L.T, L.H, L.E, L.gate_qt);
-  switch (L.H) {
-    case 1024: e = launch_gateup_t<32>(L.gate_qt, g2, s2, st, a); break;
-    case 2048: e = launch_gateup_t<64>(L.gate_qt, g2, s2, st, a); break;
-    case 4096: e = launch_gateup_t<128>(L.gate_qt, g2, s2, st, a); break;
-    default: return cudaErrorInvalidValue;
-  }
-  if (e != cudaSuccess) return e;
-  const size_t s3 = down_smem(L.T, L.E, L.F, L.k, L.down_qt);
-  const int g3 = L.H / DEC_HROWS;
-  switch (L.F) {
-    case 256: return launch_down_t<8>(L.down_qt, g3, s3, st, a);
-    case 512: return launch_down_t<16>(L.down_qt, g3, s3, st, a);
-    case 1024: return launch_down_t<32>(L.down_qt, g3, s3, st, a);
-    case 2048: return launch_down_t<64>(L.down_qt, g3, s3, st, a);
-    default: return cudaErrorInvalidValue;
-  }
+  const size_t s2 = experts_smem(L.T, L.H, L.E, L.F, L.gate_qt, L.down_qt);
+  if (L.H == 1024)
+    return L.F == 256 ? launch_experts_q<1, 8>(L.gate_qt, L.down_qt, s2, st, a)
+                      : launch_experts_q<1, 16>(L.gate_qt, L.down_qt, s2, st, a);
+  return L.F == 256 ? launch_experts_q<2, 8>(L.gate_qt, L.down_qt, s2, st, a)
+                    : launch_experts_q<2, 16>(L.gate_qt, L.down_qt, s2, st, a);
 }
 
 }  // namespace qmoe

@@ -111,6 +111,8 @@ struct TcArgs {
   float* yout_f32;              // down output in fp32 instead, when not null
   int T, k, E, H, F;
   int* status;
+  unsigned long long wait_ns;   // a bounded wait gives up after this long
+  int fault;                    // test-only: 1 = CTA 0's producer warp 4 withholds its last full arrival
 };
 
 // Tensor maps of the packed weights as 2-D byte arrays [rows][row bytes]:
@@ -223,6 +225,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t lim = g.wait_ns;
   const int NB = GATEUP ? g.F / 128 : g.H / 256;      // weight blocks per chunk
   const int KT = GATEUP ? g.H / TC_BK : g.F / TC_BK;  // k-tiles
   const int KB = KT / 2;                              // super-blocks along K
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     int it = 0;
     for (int wi = blockIdx.x; wi < total; wi += gridDim.x, ++it) {
       // warp-uniform outcome: the TMEM loads below are warp-collective
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(acc_full, it & 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(acc_full, it & 1, abort_flag, lim))) break;
       tc::tc_fence_after();
       const Chunk ch = chunk_at(g.chunks, wi / NB);
       const int blk = wi % NB;
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       uint4 hdr = make_uint4(0, 0, 0, 0), hq0 = hdr, hq1 = hdr;
       // loads the super-block header (and Q5_K high bits) of ring slot u % RS
       auto open_sb = [&](int u) -> bool {
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag))) return false;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag, lim))) return false;
         const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
         hdr = rp[0];
         if (QT == QMOE_Q5K) {
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       for (int hh = 0; hh < 2; ++hh) {
         const int stage = kg % S;
         // warp-uniform outcome: the TMEM stores below are warp-collective
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], ((kg / S) & 1) ^ 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], ((kg / S) & 1) ^ 1, abort_flag, lim))) {
           ok = false;
           break;
         }
@@ -399,7 +402,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&full[stage]);
+        // test-only fault: the first CTA's first producer warp never marks the
+        // last k-tile of its last item stored, so the MMA warps' wait on it
+        // runs out (every copy of the CTA has landed by then)
+        const bool withhold = GATEUP && g.fault == 1 && blockIdx.x == 0 && pw == 0 && u == NU - 1 && hh == 1;
+        if (lane == 0 && !withhold) tc::mbar_arrive(&full[stage]);
         ++kg;
         // then dequantise the next k-tile while the MMAs run
         if (hh == 0) {
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       };
       for (int u = 0; u < NU; ++u) {
         const int slot = u % RS;
-        if (!tc::mbar_wait(&raw_empty[slot], ((u / RS) & 1) ^ 1, abort_flag)) break;
+        if (!tc::mbar_wait(&raw_empty[slot], ((u / RS) & 1) ^ 1, abort_flag, lim)) break;
         const int j = u / KB, sb = u % KB;
         int e, y0;
         block_of(j, e, y0);
@@ -474,7 +481,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         const int pos0 = g.offsets[ch.e] + ch.c0;
         for (int kt = 0; kt < KT; ++kt, ++kg) {
           const int stage = kg % TS;
-          if (!tc::mbar_wait(&tok_empty[stage], ((kg / TS) & 1) ^ 1, abort_flag)) {
+          if (!tc::mbar_wait(&tok_empty[stage], ((kg / TS) & 1) ^ 1, abort_flag, lim)) {
             ok = false;
             break;
           }
@@ -505,12 +512,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x, ++it) {
         const Chunk ch = chunk_at(g.chunks, wi / NB);
         const uint32_t idesc = tc::idesc_bf16_f32(128, (ch.n + 15) & ~15);
-        if (!tc::mbar_wait(acc_empty, (it & 1) ^ 1, abort_flag)) break;
+        if (!tc::mbar_wait(acc_empty, (it & 1) ^ 1, abort_flag, lim)) break;
         tc::tc_fence_after();
         int stage = kg % S, ts = kg % TS;
         for (int kt = 0; kt < KT; ++kt, ++kg) {
-          if (!tc::mbar_wait_spin(&tok_full[ts], (kg / TS) & 1, abort_flag) ||
-              !tc::mbar_wait_spin(&full[stage], (kg / S) & 1, abort_flag)) {
+          if (!tc::mbar_wait_spin(&tok_full[ts], (kg / TS) & 1, abort_flag, lim) ||
+              !tc::mbar_wait_spin(&full[stage], (kg / S) & 1, abort_flag, lim)) {
             ok = false;
             break;
           }
@@ -532,7 +539,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       // drain: every MMA this thread issued has completed before TMEM is freed
       tc::mma_commit(&drain[which]);
       volatile int never = 0;
-      tc::mbar_wait(&drain[which], 0, &never);
+      tc::mbar_wait(&drain[which], 0, &never, lim);
     }
     __syncwarp();
   }
@@ -769,6 +776,8 @@ static TcArgs tc_args(const GroupedTcArgs& p) {
   a.offsets = p.offsets; a.perm = p.perm; a.chunks = p.chunks; a.n_chunks = p.n_chunks;
   a.xb = p.xb; a.hin = p.hin; a.hout = p.hout; a.yout = p.yout; a.yout_f32 = p.yout_f32;
   a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
+  a.wait_ns = p.wait_ns ? p.wait_ns : tc::kWaitLimitNs;
+  a.fault = p.fault;
   return a;
 }
 

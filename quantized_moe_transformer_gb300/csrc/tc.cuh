@@ -54,25 +54,41 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of ``parity`` to complete, giving up after a bounded
-// number of polls or when another warp of the CTA has set ``*abort``.
-// Returns false on give-up (the caller then records the error and leaves).
-constexpr uint32_t kMaxPolls = 1u << 25;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+// The GPU's global nanosecond timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase of ``parity`` to complete, giving up after ``limit_ns``
+// nanoseconds (then it also sets ``*abort``) or when another warp of the CTA
+// has set ``*abort``. Returns false on give-up (the caller then records the
+// error and leaves).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u && *abort) return false;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > limit_ns) {
+        *abort = 1;
+        return false;
+      }
+    }
   }
-  *abort = 1;
-  return false;
 }
 
 // Like mbar_wait, for a thread that usually finds the phase complete: polls
 // without suspending first.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns = kWaitLimitNs) {
   for (int i = 0; i < 64; ++i)
     if (mbar_test_wait(bar, parity)) return true;
-  return mbar_wait(bar, parity, abort);
+  return mbar_wait(bar, parity, abort, limit_ns);
 }
 
 __device__ __forceinline__ void fence_barrier_init() {

@@ -140,15 +140,19 @@ def test_nan_rows_take_lowest_indices():
 def extreme_layer(kind):
     """Layer whose super-blocks hold extreme header fields: d = dmin = 65504
     ("large") or 2^-14 ("small") with every s_j = m_j = 63 and every Q5_K high
-    bit set (quants random); or ("max") d = dmin = 2^-10, s = m = 63 and every
-    quant at its maximum (q = 15, 31)."""
+    bit set (quants random); or ("max") every quant at its maximum (q = 15,
+    31), s = m = 63, d = 2^-10 and dmin = (q_max - 1) d, so that every weight
+    is 63 d, a value bf16 holds exactly (a constant weight that bf16 rounded
+    would put the same rounding error on every product, which no tolerance
+    built on independent roundings covers)."""
     arr = inputs.moe_layer(5, H, E, F, shared=True)
     d = {"large": 65504.0, "small": 2.0**-14, "max": 2.0**-10}[kind]
-    hdr = np.frombuffer(kq.encode_header(d, d, [63] * 8, [63] * 8), dtype=np.uint8)
     for name in ("Wg", "Wu", "Sg", "Su", "Wd", "Sd"):
         a = arr[name]
-        a[..., 0:16] = hdr
-        if a.shape[-1] == 176:
+        q5 = a.shape[-1] == 176
+        dmin = d if kind != "max" else (30.0 if q5 else 14.0) * d
+        a[..., 0:16] = np.frombuffer(kq.encode_header(d, dmin, [63] * 8, [63] * 8), dtype=np.uint8)
+        if q5:
             a[..., 16:48] = 0xFF
         if kind == "max":
             a[..., -128:] = 0xFF
@@ -212,7 +216,7 @@ def test_every_row_same_eight_experts(oracle):
     each for eight experts (32 token chunks each), 248 experts idle."""
     arr = inputs.moe_layer(7, H, E, F, shared=True)
     bias = np.full(E, -50.0, np.float32)
-    bias[40:48] = 50.0 + np.arange(8, dtype=np.float32)
+    bias[40:48] = 50.0 + 10.0 * np.arange(8, dtype=np.float32)  # spaced far beyond the logit noise
     arr["Wr"][0] = bias
     lay = qb.MoeLayer.from_arrays(arr, K)
     T = 4096
