@@ -110,6 +110,26 @@ __device__ __forceinline__ float dot_sub_prmt(const uint4 qv, uint32_t hb, const
   return acc0 + acc1;
 }
 
+// Two-lane fp32 arithmetic on register pairs (lo, hi): fma.rn.f32x2 rounds
+// each lane exactly as fmaf does.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+
 // Contribution of one sub-block: d*s_j * sum q x - dmin*m_j * sum x, from the
 // byte-permute sum S of dot_sub_prmt and xs = sum x.
 __device__ __forceinline__ float sub_contrib(float S, float xs, float2 sc) {

@@ -144,11 +144,16 @@ __device__ __forceinline__ Chunk chunk_at(const int2* chunks, int i) {
 // inverse of kPerm8), as an index into the row.
 __device__ __forceinline__ int kperm_slot(int f) { return (f & ~7) | ((f & 3) << 1) | ((f >> 2) & 1); }
 
-// Dequantises sub-block j (32 weights) into 16 bf16x2 words in kPerm8 order,
-// in bf16x2 arithmetic: q is exact (the quant bits under the exponent of
-// 128.0, minus 128), then w = q * (d*s_j) - dmin*m_j in one bf16x2 FMA with the
-// two scales rounded to bf16. ``hdr`` is the super-block's first 16 bytes,
-// ``qv`` the sub-block's 16 quant bytes, ``hb`` (Q5_K) its 32 high bits.
+// Dequantises sub-block j (32 weights) into 16 bf16x2 words in kPerm8 order:
+// each weight d*s_j*q - dmin*m_j is formed in fp32 and rounded once to bf16
+// (nearest even). The quant enters as f = 0.5 + q/256, placed by one byte
+// permute into the mantissa of a float whose exponent makes it exact, and
+// w = f * (256 d s_j) - (128 d s_j + dmin m_j) is one fp32 FMA (two weights per
+// two-lane FMA): 256 d s_j is exact, and the fp32 rounding of the constant
+// term is about 2^-24 of 128 d s_j, far below the bf16 step of the weight.
+// ``hdr`` is the super-block's first 16 bytes, ``qv`` the sub-block's 16
+// quant bytes, ``hb`` (Q5_K) its 32 high bits. Word 4n+i of the output holds
+// weights 8n+i (low half) and 8n+i+4 (high half).
 template <int QT>
 __device__ __forceinline__ void dequant_sub(const uint4 hdr, const uint4 qv, uint32_t hb, int j, uint32_t* o) {
   KHeader h;
@@ -158,26 +163,28 @@ __device__ __forceinline__ void dequant_sub(const uint4 hdr, const uint4 qv, uin
   h.f0 = hdr.y;
   h.f1 = hdr.z;
   h.f2 = hdr.w;
-  const __nv_bfloat162 m128 = __float2bfloat162_rn(-128.f);
   const float2 sc = sub_scale(h, j);
-  const __nv_bfloat162 ds2 = __float2bfloat162_rn(sc.x);
-  const __nv_bfloat162 ndm2 = __float2bfloat162_rn(-sc.y);
+  const uint32_t av = __float_as_uint(256.f * sc.x);
+  const uint32_t cv = __float_as_uint(-fmaf(128.f, sc.x, sc.y));
+  const uint64_t a2 = pack2(av, av), c2 = pack2(cv, cv);
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
   for (int n = 0; n < 4; ++n) {
-    // Q5_K: the high bits of weights 8n .. 8n+7 copied to bits 4-11 and
-    // 16-23, so that (u >> i) holds that of weight 8n+i at bit 4 and that of
-    // weight 8n+i+4 at bit 20 (the 16s of the two bf16 mantissas below)
-    const uint32_t u = QT == QMOE_Q5K ? ((hb >> (8 * n)) & 0xFFu) * 0x10010u : 0u;
+    // ev: quants of weights 8n, 8n+2, 8n+4, 8n+6 in bytes 0..3; od: 8n+1, ...
+    uint32_t ev = w[n] & 0x0F0F0F0Fu;
+    uint32_t od = (w[n] >> 4) & 0x0F0F0F0Fu;
+    if (QT == QMOE_Q5K) {
+      ev |= spread4(hb >> (8 * n), 0);
+      od |= spread4(hb >> (8 * n), 1);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      // quants of weights 8n+i and 8n+i+4 as bf16 128+q in the two halves
-      uint32_t x = ((w[n] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-      if (QT == QMOE_Q5K) x |= (u >> i) & 0x00100010u;
-      __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
-      v = __hadd2(v, m128);             // q, exact
-      v = __hfma2(v, ds2, ndm2);        // q*d*s - dmin*m, one rounding
-      o[4 * n + i] = *reinterpret_cast<uint32_t*>(&v);
+      const uint32_t src = (i & 1) ? od : ev;
+      const uint32_t blo = (uint32_t)(i >> 1), bhi = blo + 2;  // weights 8n+i, 8n+i+4
+      const uint64_t f2 = pack2(__byte_perm(src, 0x3F000000u, 0x7044u | (blo << 8)),
+                                __byte_perm(src, 0x3F000000u, 0x7044u | (bhi << 8)));
+      const float2 wv = unpack2(ffma2(f2, a2, c2));
+      o[4 * n + i] = tc::pack_bf16x2(wv.x, wv.y);
     }
   }
 }
