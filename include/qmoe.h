@@ -40,6 +40,22 @@
  *     bit i%8 of byte 16 + i/8; [48,176) low nibbles as in Q4_K.
  *   Weight i (sub-block j = i/32): w_i = d*s_j*q_i - dmin*m_j, q_i the 4-bit
  *   quant (Q4_K) or quant + 16*high bit (Q5_K).
+ *   Q6_K, 210 bytes ("CKE Zip: From Splitting Tokens To Splitting Qwen3.5
+ *     Weights", opening paragraphs: a Q4_K_M model file keeps some tensors in
+ *     Q6_K; the layout is the library's own): [0,2) d fp16; [2,18) sixteen
+ *     signed 8-bit scales s_0..s_15, one per 16 weights; [18,82) 2-bit high
+ *     parts, weight i in bits 2(i%4)..2(i%4)+1 of byte 18 + i/4; [82,210) low
+ *     nibbles as in Q4_K. w_i = d*s_{i/16}*(q_i - 32), q_i = nibble + 16*high.
+ *   MXFP4, 136 bytes ("Distributed CPU: Zip Fusion Beyond Tensor
+ *     Parallelism", "Decode vs Prefill: Same Weights, Different
+ *     Bottlenecks": an MXFP4-class format; element and scale types of the OCP
+ *     microscaling format, the 256-weight grouping the library's own): [0,8)
+ *     E8M0 scales e_0..e_7, one per 32 weights (2^(e-127), 255 = NaN);
+ *     [8,136) FP4 E2M1 codes (sign, 2 exponent bits, 1 mantissa bit), byte b
+ *     = weight 2b (low nibble), 2b+1 (high). w_i = 2^(e_{i/32}-127)*E2M1(code).
+ *   Q6_K and MXFP4 are taken by the grouped GEMV path at every row count
+ *   (qmoe_last_path() reports it); the decode and tensor-core paths take
+ *   Q4_K and Q5_K.
  *   Matrices are stored one output feature per row, super-blocks running
  *   along the input (reduction) axis: a [rows][cols] matrix with cols % 256
  *   == 0 is rows * (cols/256) consecutive super-blocks.
@@ -70,7 +86,7 @@ typedef enum {
   QMOE_ERR_TOO_LARGE = -10   /* the problem needs more than the library's fixed scratch */
 } qmoe_status;
 
-typedef enum { QMOE_Q4K = 0, QMOE_Q5K = 1 } qmoe_qtype;
+typedef enum { QMOE_Q4K = 0, QMOE_Q5K = 1, QMOE_Q6K = 2, QMOE_MXFP4 = 3 } qmoe_qtype;
 
 /* Execution path the last successful qmoe_moe_forward took on this thread. */
 typedef enum {

@@ -16,8 +16,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmoe.so")
 
-Q4K, Q5K = 0, 1
-QTYPE = {"q4k": Q4K, "q5k": Q5K}
+Q4K, Q5K, Q6K, MXFP4 = 0, 1, 2, 3
+QTYPE = {"q4k": Q4K, "q5k": Q5K, "q6k": Q6K, "mxfp4": MXFP4}
 PATH_NAMES = {0: "none", 1: "gemv", 2: "gemm_tc", 3: "decode"}
 
 _c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p

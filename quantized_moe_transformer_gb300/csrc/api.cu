@@ -145,8 +145,7 @@ int check_desc(const qmoe_moe_desc* d) {
   if (!d) return QMOE_ERR_NULL;
   if (!supported_width(d->H) || !supported_width(d->F)) return QMOE_ERR_ARG;
   if (d->E < 1 || d->E > 1024 || d->k < 1 || d->k > 16 || d->k > d->E) return QMOE_ERR_ARG;
-  if ((d->gate_type != QMOE_Q4K && d->gate_type != QMOE_Q5K) ||
-      (d->down_type != QMOE_Q4K && d->down_type != QMOE_Q5K))
+  if (d->gate_type < QMOE_Q4K || d->gate_type > QMOE_MXFP4 || d->down_type < QMOE_Q4K || d->down_type > QMOE_MXFP4)
     return QMOE_ERR_ARG;
   if (!d->Wr || !d->Wg || !d->Wu || !d->Wd) return QMOE_ERR_NULL;
   const bool any_shared = d->Sg || d->Su || d->Sd;
@@ -513,7 +512,10 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
   const int P = T * k;
 
   cudaError_t e = cudaSuccess;
-  if (ids == nullptr && T <= g_decode_max_rows.load() &&
+  // the decode and tensor-core paths take the k-quant formats; Q6_K and MXFP4
+  // layers take the grouped GEMV path at every row count
+  const bool kquant = d->gate_type <= QMOE_Q5K && d->down_type <= QMOE_Q5K;
+  if (kquant && ids == nullptr && T <= g_decode_max_rows.load() &&
       decode_path_supported(T, H, E, k, F, d->gate_type, d->down_type)) {
     DecodeLaunch D{};
     D.X = X;
@@ -586,7 +588,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
   if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
   const float* w_use = ids ? w : ws_w;
 
-  if (T > g_gemm_threshold.load()) {
+  if (kquant && T > g_gemm_threshold.load()) {
     // grouped dequant + bf16 tcgen05 GEMM path: h and y are bf16
     int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
     int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);

@@ -15,7 +15,14 @@ constexpr int SUBK = 32;         // weights per sub-block
 constexpr int Q4K_BYTES = 144;
 constexpr int Q5K_BYTES = 176;
 
-__host__ __device__ inline int qtype_bytes(int qt) { return qt == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES; }
+constexpr int Q6K_BYTES = 210;
+constexpr int MXFP4_BYTES = 136;
+
+// Bytes of one 256-weight super-block of format ``qt``.
+__host__ __device__ constexpr int qtype_size(int qt) {
+  return qt == QMOE_Q5K ? Q5K_BYTES : qt == QMOE_Q6K ? Q6K_BYTES : qt == QMOE_MXFP4 ? MXFP4_BYTES : Q4K_BYTES;
+}
+__host__ __device__ inline int qtype_bytes(int qt) { return qtype_size(qt); }
 
 // One super-block header: d, dmin and the sixteen 6-bit fields. The header is
 // the first 16 bytes of both formats, loaded as one 16-byte vector.
