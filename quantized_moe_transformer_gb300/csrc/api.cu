@@ -214,6 +214,24 @@ int check_block(const qmoe_block_desc* b) {
 // the bf16 copy of x) once for every projection of the same x.
 bool dense_uses_tc(int T) { return T > g_gemm_threshold.load(); }
 
+// dense_prep of RMSNorm(x; gamma) on the tensor-core path: the norm is written
+// straight into the bf16 token operand (no fp32 normed copy).
+cudaError_t dense_prep_norm(const float* x, const float* gamma, float eps, int T, int K, char* base,
+                            const AttnWs& L, cudaStream_t st) {
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
+  int32_t* active = reinterpret_cast<int32_t*>(base + L.active);
+  int32_t* n_active = reinterpret_cast<int32_t*>(base + L.n_active);
+  cudaError_t e = launch_dense_route(offsets, perm, active, n_active, T, st);
+  if (e != cudaSuccess) return e;
+  int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
+  int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
+  __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
+  if ((e = launch_build_chunks(offsets, 1, 128, chunks, n_chunks, st)) != cudaSuccess) return e;
+  g_launches.fetch_add(3);
+  return launch_rmsnorm_bf16(x, gamma, eps, xb, T, K, st);
+}
+
 cudaError_t dense_prep(const float* x, int T, int K, char* base, const AttnWs& L, cudaStream_t st) {
   int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
   int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
@@ -298,9 +316,15 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
   const int H = b->H, nh = b->n_heads, nkv = b->n_kv, hd = b->head_dim;
   __nv_bfloat16* kcb = reinterpret_cast<__nv_bfloat16*>(kc);
   __nv_bfloat16* vcb = reinterpret_cast<__nv_bfloat16*>(vc);
-  cudaError_t e = launch_rmsnorm(X, b->g1, b->eps, rr, T, H, st);
-  g_launches.fetch_add(1);
-  if (e == cudaSuccess) e = dense_prep(rr, T, H, base, L, st);
+  cudaError_t e;
+  if (dense_uses_tc(T)) {
+    // RMSNorm fused into the bf16 token operand of the Q, K, V projections
+    e = dense_prep_norm(X, b->g1, b->eps, T, H, base, L, st);
+  } else {
+    e = launch_rmsnorm(X, b->g1, b->eps, rr, T, H, st);
+    g_launches.fetch_add(1);
+    if (e == cudaSuccess) e = dense_prep(rr, T, H, base, L, st);
+  }
   if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wq, QMOE_Q4K, nh * hd, q, base, L, status, st);
   if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wk, QMOE_Q4K, nkv * hd, k, base, L, status, st);
   if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wv, QMOE_Q4K, nkv * hd, v, base, L, status, st);
@@ -551,6 +575,13 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     return QMOE_OK;
   }
   const bool small = P <= 2048;
+  // on the tensor-core path at large T the permutation scan also builds the
+  // token-chunk list
+  const bool use_tc = kquant && T > g_gemm_threshold.load();
+  const bool chunks_in_scan = use_tc && !small;
+  int2* tc_chunks = reinterpret_cast<int2*>(base + L.chunks);
+  int32_t* tc_n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
+  const int tc_cap = tc_chunk_cap(T, k, E);
   if (ids == nullptr) {
     e = staged(QMOE_STAGE_ROUTER, router_launches(T, H, E), st, [&] {
       return launch_router_logits(X, d->Wr, part, T, H, E, L.nsplit, base + L.wr3, status, st);
@@ -569,7 +600,8 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
           cudaError_t e2 = launch_topk(part, L.nsplit, T, E, k, ws_ids, ws_w, st);
           if (e2 != cudaSuccess) return e2;
           return launch_perm_large(ws_ids, T, E, k, has_shared, chunk, offsets, perm, active,
-                                   n_active, status, st);
+                                   n_active, status, st, tc_cap, chunks_in_scan ? tc_chunks : nullptr,
+                                   tc_n_chunks);
         });
       }
     }
@@ -582,22 +614,25 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     else
       e = staged(QMOE_STAGE_ROUTE, 3, st, [&] {
         return launch_perm_large(ids, T, E, k, has_shared, chunk, offsets, perm, active,
-                                 n_active, status, st);
+                                 n_active, status, st, tc_cap, chunks_in_scan ? tc_chunks : nullptr,
+                                 tc_n_chunks);
       });
   }
   if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
   const float* w_use = ids ? w : ws_w;
 
-  if (kquant && T > g_gemm_threshold.load()) {
+  if (use_tc) {
     // grouped dequant + bf16 tcgen05 GEMM path: h and y are bf16
-    int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
-    int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
+    int2* chunks = tc_chunks;
+    int32_t* n_chunks = tc_n_chunks;
     __nv_bfloat16* h16 = reinterpret_cast<__nv_bfloat16*>(hbuf);
     __nv_bfloat16* y16 = reinterpret_cast<__nv_bfloat16*>(y);
     __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
-    e = staged(QMOE_STAGE_ROUTE, 2, st, [&] {
-      cudaError_t e2 = launch_build_chunks(offsets, E, tc_chunk_cap(T, k, E), chunks, n_chunks, st);
-      if (e2 != cudaSuccess) return e2;
+    e = staged(QMOE_STAGE_ROUTE, chunks_in_scan ? 1 : 2, st, [&] {
+      if (!chunks_in_scan) {
+        cudaError_t e2 = launch_build_chunks(offsets, E, tc_cap, chunks, n_chunks, st);
+        if (e2 != cudaSuccess) return e2;
+      }
       return launch_to_bf16(X, xb, (int)(P + (has_shared ? T : 0)), H, perm, T, k, inv, st);
     });
     if (e != cudaSuccess) return QMOE_ERR_LAUNCH;
@@ -607,7 +642,7 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     p.chunks = chunks;
     p.n_chunks = n_chunks;
     p.max_chunks = tc_max_chunks(T, k, E, has_shared);
-    p.nmax = tc_chunk_cap(T, k, E);
+    p.nmax = tc_cap;
     p.T = T;
     p.k = k;
     p.E = E;

@@ -34,6 +34,48 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
   for (int i = tid; i < H; i += 256) y[(size_t)t * H + i] = xr[i] * inv * gamma[i];
 }
 
+// RMSNorm fused into the bf16 token operand of a tensor-core projection:
+// y = bf16(x / sqrt(mean(x^2) + eps) * gamma), one CTA per row, written in the
+// operand's K order (inside every group of 8 values, K offsets 0 4 1 5 2 6 3 7)
+// as the bf16 conversion of the projection input would write it. The values
+// are the same as RMSNorm then conversion: the fp32 expression is the same.
+__global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restrict__ x,
+                                                           const float* __restrict__ gamma, float eps,
+                                                           __nv_bfloat16* __restrict__ y, int H) {
+  __shared__ float red[8];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const float* xr = x + (size_t)t * H;
+  float s = 0.f;
+  for (int i = tid; i < H; i += 256) s = fmaf(xr[i], xr[i], s);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if ((tid & 31) == 0) red[tid >> 5] = s;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / (float)H + eps);
+  for (int g = tid; g < H / 8; g += 256) {
+    const float4 a = reinterpret_cast<const float4*>(xr)[2 * g];
+    const float4 b = reinterpret_cast<const float4*>(xr)[2 * g + 1];
+    const float4 ga = reinterpret_cast<const float4*>(gamma)[2 * g];
+    const float4 gb = reinterpret_cast<const float4*>(gamma)[2 * g + 1];
+    __nv_bfloat162 o[4];
+    o[0] = __floats2bfloat162_rn(a.x * inv * ga.x, b.x * inv * gb.x);
+    o[1] = __floats2bfloat162_rn(a.y * inv * ga.y, b.y * inv * gb.y);
+    o[2] = __floats2bfloat162_rn(a.z * inv * ga.z, b.z * inv * gb.z);
+    o[3] = __floats2bfloat162_rn(a.w * inv * ga.w, b.w * inv * gb.w);
+    reinterpret_cast<uint4*>(y + (size_t)t * H)[g] = *reinterpret_cast<const uint4*>(o);
+  }
+}
+
+cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, float eps, __nv_bfloat16* y, int T, int H,
+                                cudaStream_t st) {
+  if (H % 8 != 0) return cudaErrorInvalidValue;
+  rmsnorm_bf16_kernel<<<T, 256, 0, st>>>(x, gamma, eps, y, H);
+  return cudaGetLastError();
+}
+
 // Routing of a dense projection seen as one expert (index 0) holding all rows.
 __global__ void dense_route_kernel(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T; i += gridDim.x * blockDim.x) perm[i] = i;

@@ -34,9 +34,12 @@ cudaError_t launch_route_small(const float* part, int nsplit, const int32_t* ids
                                int32_t* perm, int32_t* active, int32_t* n_active, int* status,
                                cudaStream_t st);
 int perm_chunks(int P);
+// with ``chunks`` set, also the tensor-core path's token-chunk list (cap 64
+// or 128 rows), as launch_build_chunks would build it
 cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_shared,
                               int32_t* chunk_cnt, int32_t* offsets, int32_t* perm,
-                              int32_t* active, int32_t* n_active, int* status, cudaStream_t st);
+                              int32_t* active, int32_t* n_active, int* status, cudaStream_t st,
+                              int cap = 0, int2* chunks = nullptr, int32_t* n_tok_chunks = nullptr);
 
 // moe_gemv.cu: grouped dequant-fused GEMV kernels and the combine.
 struct GroupedArgs {
@@ -90,6 +93,9 @@ cudaError_t launch_combine_bf16(const __nv_bfloat16* y, const int32_t* inv, cons
 
 // block.cu: the attention + MoE block's other kernels.
 cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, float* y, int T, int H, cudaStream_t st);
+// RMSNorm straight into the bf16 token operand of a tensor-core projection.
+cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, float eps, __nv_bfloat16* y, int T, int H,
+                                cudaStream_t st);
 cudaError_t launch_dense_route(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T,
                                cudaStream_t st);
 cudaError_t launch_rope_cache(float* q, const float* k, const float* v, __nv_bfloat16* kc, __nv_bfloat16* vc, int T,

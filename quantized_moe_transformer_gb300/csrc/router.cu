@@ -452,13 +452,19 @@ __global__ void perm_count_kernel(const int32_t* __restrict__ ids, int P, int E,
   for (int i = threadIdx.x; i < E; i += blockDim.x) chunk_cnt[(size_t)c * E + i] = cnt[i];
 }
 
+// Also builds the tensor-core path's token-chunk list when ``chunks`` is set:
+// every expert with rows (the shared expert last) cut into ceil(rows / cap)
+// chunks of near-equal size (first row below 2^24, packed with the row count).
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_cnt,
                                                          int n_chunks, int T, int E, int k,
                                                          int has_shared, int staged,
                                                          int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ perm,
                                                          int32_t* __restrict__ active,
-                                                         int32_t* __restrict__ n_active) {
+                                                         int32_t* __restrict__ n_active, int cap,
+                                                         int2* __restrict__ chunks,
+                                                         int32_t* __restrict__ n_tok_chunks) {
+  __shared__ int32_t cstart[1025 + 32];
   extern __shared__ int32_t tot[];  // [E+1], then (staged) [n_chunks][E] counts
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int32_t* cs = tot + ((E + 1 + 3) & ~3);
@@ -496,41 +502,56 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   if (tid == 0) tot[E] = has_shared ? T : 0;
   __syncthreads();
   if (warp == 0) {
-    int run = 0, arun = 0;
+    // offsets, active list and (with a chunk list) each expert's first chunk
+    int run = 0, arun = 0, crun = 0;
     for (int base = 0; base <= E; base += 32) {
       int e = base + lane;
       int c = (e <= E) ? tot[e] : 0;
       int a = c > 0;
-      int incl = c, aincl = a;
+      int nc = chunks ? (c + cap - 1) / cap : 0;
+      int incl = c, aincl = a, cincl = nc;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         int o = __shfl_up_sync(0xffffffffu, incl, off);
         int oa = __shfl_up_sync(0xffffffffu, aincl, off);
+        int oc = __shfl_up_sync(0xffffffffu, cincl, off);
         if (lane >= off) {
           incl += o;
           aincl += oa;
+          cincl += oc;
         }
       }
       if (e <= E) {
         offsets[e] = run + incl - c;
+        cstart[e] = crun + cincl - nc;
         if (a) active[arun + aincl - 1] = e;
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
       arun += __shfl_sync(0xffffffffu, aincl, 31);
+      crun += __shfl_sync(0xffffffffu, cincl, 31);
     }
     if (lane == 0) {
       offsets[E + 1] = run;
       n_active[0] = arun;
+      if (chunks) n_tok_chunks[0] = crun;
     }
   }
   __syncthreads();
   if (staged) {
-    for (int i = tid; i < n_chunks * E; i += blockDim.x) chunk_cnt[i] = cs[i] + offsets[i % E];
-  } else {
-    for (int e = tid; e < E; e += blockDim.x) {
-      const int base = offsets[e];
-#pragma unroll 8
-      for (int c = 0; c < n_chunks; ++c) chunk_cnt[(size_t)c * E + e] += base;
+    // the scatter adds each expert's offset itself
+    for (int i = tid; i < n_chunks * E; i += blockDim.x) chunk_cnt[i] = cs[i];
+  }
+  if (chunks) {
+    for (int e = tid; e <= E; e += blockDim.x) {
+      const int Me = tot[e];
+      if (Me <= 0) continue;
+      const int nc = (Me + cap - 1) / cap;
+      for (int i = 0; i < nc; ++i) {
+        // rows [i Me / nc, (i + 1) Me / nc)
+        const int c0 = (int)((long long)i * Me / nc);
+        const int c1 = (int)((long long)(i + 1) * Me / nc);
+        chunks[cstart[e] + i] = make_int2(e, c0 | ((c1 - c0 - 1) << 24));
+      }
     }
   }
   const int P = T * k;
@@ -540,10 +561,11 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
 
 __global__ void perm_scatter_kernel(const int32_t* __restrict__ ids, int P, int E,
                                     const int32_t* __restrict__ chunk_base,
+                                    const int32_t* __restrict__ offsets,
                                     int32_t* __restrict__ perm) {
   extern __shared__ int32_t cur[];
   const int c = blockIdx.x, lane = threadIdx.x;
-  for (int i = lane; i < E; i += 32) cur[i] = chunk_base[(size_t)c * E + i];
+  for (int i = lane; i < E; i += 32) cur[i] = chunk_base[(size_t)c * E + i] + offsets[i];
   __syncwarp();
   int p0 = c * PERM_CHUNK, p1 = min(P, p0 + PERM_CHUNK);
   // the chunk's expert ids, all loads in flight at once
@@ -667,7 +689,9 @@ int perm_chunks(int P) { return (P + PERM_CHUNK - 1) / PERM_CHUNK; }
 
 cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_shared,
                               int32_t* chunk_cnt, int32_t* offsets, int32_t* perm,
-                              int32_t* active, int32_t* n_active, int* status, cudaStream_t st) {
+                              int32_t* active, int32_t* n_active, int* status, cudaStream_t st, int cap,
+                              int2* chunks, int32_t* n_tok_chunks) {
+  if (E > 1024 || (chunks != nullptr && cap != 64 && cap != 128)) return cudaErrorInvalidValue;
   const int P = T * k, nc = perm_chunks(P);
   perm_count_kernel<<<nc, 256, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, status);
   // the scan stages every chunk count in shared memory when they fit
@@ -678,8 +702,8 @@ cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_s
   cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(perm_scan_kernel), smem);
   if (e != cudaSuccess) return e;
   perm_scan_kernel<<<1, 1024, smem, st>>>(chunk_cnt, nc, T, E, k, has_shared, staged, offsets, perm, active,
-                                          n_active);
-  perm_scatter_kernel<<<nc, 32, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, perm);
+                                          n_active, cap, chunks, n_tok_chunks);
+  perm_scatter_kernel<<<nc, 32, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, offsets, perm);
   return cudaGetLastError();
 }
 
