@@ -656,8 +656,7 @@ def measure_block(torch, qb, layers, T, pos0, args, stream, world, device, rank,
 # kernels whose DRAM bytes make up the dominant unit of each path: the decode
 # path's chained kernels per step, the grouped gate/up kernel otherwise
 TRAFFIC_KERNELS = {
-    "decode": ("decode_router_kernel", ("decode_router_kernel", "decode_route_kernel", "decode_gateup_kernel",
-                                        "decode_down_kernel")),
+    "decode": ("decode_router_kernel", ("decode_router_kernel", "decode_experts_kernel")),
     "gemm_tc": ("moe_tc_kernel<1,", ("moe_tc_kernel<1,",)),
     "gemv": ("gateup_gemv_kernel", ("gateup_gemv_kernel",)),
 }

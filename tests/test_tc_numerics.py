@@ -1,15 +1,16 @@
 """The error budget of the tensor-core path's number format, on the CPU.
 
-The tensor-core path multiplies bf16 operands: its weights are dequantised in
-bf16x2 arithmetic (q exact; d*s_j and dmin*m_j computed in fp32, rounded to
-bf16; w = q*ds - dm in one bf16 FMA, one rounding), the token rows are rounded
-to bf16, and h is rounded to bf16 between the two projections; products are
+The tensor-core path multiplies bf16 operands: each weight is formed in fp32
+as f * (256 d s_j) - (128 d s_j + dmin m_j) with f = 0.5 + q/256 (exact),
+one fp32 FMA, and rounded once to bf16; the token rows are rounded to bf16,
+and h is rounded to bf16 between the two projections; products are
 accumulated in fp32. This module models those roundings in numpy (float64
-arithmetic with explicit bf16 rounding, torch's round-to-nearest-even) and
-checks the reading's two claims: the per-weight error of the bf16 dequant is
-about twice that of rounding the exact weight, and a layer computed this way
-stays well inside the 1e-2 * max|ref| tolerance of that path. It models the
-format, not the kernels, and no GPU test uses it as a reference.
+arithmetic with explicit fp32 and bf16 rounding, torch's round-to-nearest-even)
+and checks the reading's two claims: the per-weight error of the dequant is
+that of rounding the exact weight to bf16 (the fp32 stage adds next to
+nothing), and a layer computed this way stays well inside the 1e-2 * max|ref|
+tolerance of that path. It models the format, not the kernels, and no GPU
+test uses it as a reference.
 """
 
 import numpy as np
@@ -39,16 +40,24 @@ def fields(blocks: np.ndarray):
     return d, dmin, vals[..., :8], vals[..., 8:], q
 
 
+def f32(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
 def bf16_dequant(blocks: np.ndarray) -> np.ndarray:
-    """The tensor-core path's weights: bf16(q * bf16(d*s_j) - bf16(dmin*m_j))."""
+    """The tensor-core path's weights: bf16(fp32 FMA of f = 0.5 + q/256 with
+    256 d s_j and the fp32 constant -(128 d s_j + dmin m_j))."""
     d, dmin, s, m, q = fields(blocks)
     j = np.arange(256) // 32
-    ds = bf16(d[..., None] * s.astype(np.float32))        # fp32 product, then bf16
-    dm = bf16(dmin[..., None] * m.astype(np.float32))
-    return bf16(q * ds[..., j] - dm[..., j])                # exact in fp64, one rounding
+    ds = f32(d[..., None].astype(np.float64) * s)           # exact: 11 x 6 bits
+    dm = f32(dmin[..., None].astype(np.float64) * m)
+    a = 256.0 * ds                                           # exact
+    c = -f32(128.0 * ds + dm)                                # fp32 FMA: one rounding
+    f = 0.5 + q / 256.0                                      # exact
+    return bf16(f32(f * a[..., j] + c[..., j]))              # product exact in fp64; fp32 FMA, then bf16
 
 
-def test_bf16_dequant_error_is_about_twice_plain_rounding():
+def test_bf16_dequant_error_is_that_of_plain_rounding():
     rng = inputs.generator(9, "Wg")
     for qt in ("q4k", "q5k"):
         blocks = inputs.packed_blocks(rng, (8192,), qt)
@@ -57,8 +66,9 @@ def test_bf16_dequant_error_is_about_twice_plain_rounding():
         rel_tc = np.abs(bf16_dequant(blocks) - exact)[mask] / np.abs(exact)[mask]
         rel_rn = np.abs(bf16(exact) - exact)[mask] / np.abs(exact)[mask]
         assert rel_rn.mean() < 0.0016
-        assert rel_tc.mean() < 0.0035
-        assert 1.0 < rel_tc.mean() / rel_rn.mean() < 2.5, qt
+        assert rel_tc.mean() / rel_rn.mean() < 1.05, qt
+        # the fp32 stage moves a weight across a bf16 rounding boundary rarely
+        assert np.mean(bf16_dequant(blocks) != bf16(exact)) < 0.01, qt
 
 
 def test_layer_in_the_tensor_core_format_is_inside_its_tolerance():
@@ -90,4 +100,4 @@ def test_layer_in_the_tensor_core_format_is_inside_its_tolerance():
             e = ids[t, s]
             out[t] += w[t, s] * ffn(layer["Wg"][e], layer["Wu"][e], layer["Wd"][e], np.array([t]))[0]
     ratio = np.max(np.abs(out - ref)) / np.max(np.abs(ref))
-    assert ratio < 6e-3, ratio  # 4.0e-3 at these seeds; the GPU measured 2.7e-3 on a 16-row case
+    assert ratio < 5e-3, ratio  # 3.0e-3 at these seeds
