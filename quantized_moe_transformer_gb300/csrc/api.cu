@@ -333,7 +333,7 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
     g_launches.fetch_add(1);
   }
   if (e == cudaSuccess) {
-    e = launch_attention(q, kcb, vcb, part, o, T, pos0, nh, nkv, hd, L.chunked, st);
+    e = launch_attention(q, kcb, vcb, part, o, T, pos0, nh, nkv, hd, L.chunked, status, wait_limit_ns(), st);
     g_launches.fetch_add(L.chunked ? 2 : 1);
   }
   float* proj_out = R ? rr : out;  // rr is free once Q, K, V exist

@@ -7,251 +7,405 @@
 // Attention at Long Context": the softmax over key blocks is carried by its
 // running maximum, normaliser and weighted output, which is how this kernel
 // walks the keys.
-//
-// CTA = (64 query rows, one head), 4 warps of 16 rows. Per 64-key tile:
-//   S = Q K^T    bf16 mma.sync m16n8k16, fp32 accumulate; Q (scaled by
-//                log2(e)/sqrt(hd)) lives in registers as A fragments, K
-//                comes from shared memory by ldmatrix;
-//   softmax      online in exp2 form: row max over the tile, O and the
-//                normaliser rescaled by exp2(m_old - m_new);
-//   O += P V     P (bf16) goes from the S accumulator registers straight
-//                into A fragments; V by ldmatrix.trans.
-// K and V tiles (bf16, from the caches) are double-buffered with cp.async
-// into 16-byte-chunk XOR-swizzled rows, so ldmatrix reads no bank twice.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kernels.cuh"
+#include "tc.cuh"
 
 namespace qmoe {
 
-constexpr int FA_BQ = 64, FA_BK = 64, FA_HD = 128;
-constexpr int FA_THREADS = 128;
-constexpr int FA_TILE_BYTES = FA_BK * FA_HD * 2;  // 16 KB per K or V tile
+// CTA = (128 query rows, one head); key blocks of 128.
+//   S_j = Q K_j^T   Q scaled by log2(e)/sqrt(hd) and split into two bf16
+//                   parts (hi = bf16(q), lo = bf16(q - hi)), two MMAs per K
+//                   step, so that S carries about 16 bits of q (with scores
+//                   of a few thousand, which random weights give, the 2^-9
+//                   step of a bf16 q alone would move the softmax argument by
+//                   several units); K is exact (the cache is bf16); Q and K_j
+//                   in shared memory
+//                   (128-byte swizzled, K-major), fp32 S in TMEM, two S
+//                   buffers so that S_{j+1} is computed while the softmax
+//                   reads S_j;
+//   softmax         warps 0-3, one query row per thread (its TMEM lane):
+//                   row max over the block (causal mask on diagonal blocks),
+//                   p = exp2(s - m) written back to TMEM as bf16 P_j (two
+//                   buffers), the normaliser l summed in fp32;
+//   O += P_j V_j    P_j from TMEM as the A operand, V_j from shared memory as
+//                   an MN-major B operand (its rows are keys, head dims
+//                   contiguous), fp32 O in TMEM.
+// The running max m is a reference, not the exact maximum: O and l are
+// rescaled by exp2(m_old - m_new) only when a row's maximum exceeds m by more
+// than 2^8 (so p <= 256), which leaves out(t) = O / l unchanged in exact
+// arithmetic; the rescale waits for the previous P V to complete.
+// Warp 4 copies K_j and V_j (2-D boxes of 64 head dims x 128 keys of one KV
+// head, by a 3-D tensor map [position][kv head][head dim]) into a two-stage
+// ring; warp 5 allocates TMEM and issues the MMAs (S_0, then S_{j+1} before
+// P_j V_j). Every wait is bounded: on time-out the CTA records
+// QMOE_ERR_TIMEOUT, drains its MMAs, frees its TMEM and returns.
+constexpr int AT_BQ = 128, AT_BK = 128, AT_HD = 128;
+constexpr int AT_THREADS = 192;
+constexpr int AT_LOAD_WARP = 4, AT_MMA_WARP = 5;
+constexpr int AT_HALF = 128 * 128;               // 128 rows x 64 bf16 (one K half of a tile)
+constexpr int AT_Q_BYTES = 4 * AT_HALF;          // 64 KB: hi part (two K halves), then lo part
+constexpr int AT_KV_BYTES = 4 * AT_HALF;         // K_j then V_j: 64 KB a stage
+constexpr int AT_STAGES = 2;
+constexpr int AT_SMEM = 1024 + AT_Q_BYTES + AT_STAGES * AT_KV_BYTES + 256;
+constexpr uint32_t AT_S_COL = 0;                 // S buffer b at 128 b
+constexpr uint32_t AT_O_COL = 256;
+constexpr uint32_t AT_P_COL = 384;               // P buffer b at 384 + 64 b
+constexpr float AT_RESCALE_LOG2 = 8.f;
 
-__device__ __forceinline__ uint32_t fa_smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Byte offset of 16-byte chunk c (0..15) of row r in a 256-byte-row tile.
-__device__ __forceinline__ uint32_t fa_swz(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
-
-__device__ __forceinline__ void fa_cp_async16(uint32_t dst, const void* src, bool valid) {
-  const uint32_t n = valid ? 16u : 0u;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ void fa_ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void fa_ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// D += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate.
-__device__ __forceinline__ void fa_mma(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                       uint32_t b1) {
+__device__ __forceinline__ void at_tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                               uint32_t bar) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
-__device__ __forceinline__ uint32_t fa_pack(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+// 32 lanes x 32 consecutive 32-bit TMEM columns at ``ta``, then the wait.
+__device__ __forceinline__ void at_tmem_ld32(uint32_t ta, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(ta)
+      : "memory");
 }
 
-// q [T][nh][128] fp32 (rotated), kc/vc [ctx][nkv][128] bf16, o [T][nh][128]
-// fp32; query t sits at position pos0 + t and sees keys 0 .. pos0 + t.
-__global__ void __launch_bounds__(FA_THREADS) attn_prefill_mma_kernel(const float* __restrict__ q,
-                                                                      const __nv_bfloat16* __restrict__ kc,
-                                                                      const __nv_bfloat16* __restrict__ vc,
-                                                                      float* __restrict__ o, int T, int pos0, int nh,
-                                                                      int nkv) {
-  extern __shared__ __align__(128) uint8_t fa_smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g8 = lane >> 2, t4 = lane & 3;
-  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;  // heavy (late) tiles first
+// Descriptor of an MN-major operand with 128-byte swizzle: rows of 128 bytes
+// (64 values along N) for consecutive K, 8-row atoms of 1024 bytes; the
+// leading byte offset steps to the next 64 values along N, the stride byte
+// offset to the next 8 rows along K.
+__device__ __forceinline__ uint64_t at_mn_sw128_desc(uint32_t smem_addr, uint32_t lbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// q [T][nh][128] fp32 (rotated), the caches through the tensor maps
+// (positions [0, pos0 + T)), o [T][nh][128] fp32; query t sits at position
+// pos0 + t and sees keys 0 .. pos0 + t.
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    attn_prefill_tc_kernel(const float* __restrict__ q, float* __restrict__ o, int T, int pos0, int nh, int nkv,
+                           int* status, unsigned long long wait_ns, const __grid_constant__ CUtensorMap kmap,
+                           const __grid_constant__ CUtensorMap vmap) {
+  extern __shared__ uint8_t at_smem_raw[];
+  const uint32_t s0 = tc::smem_u32(at_smem_raw);
+  uint8_t* smem = at_smem_raw + (((s0 + 1023u) & ~1023u) - s0);
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + AT_Q_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + AT_STAGES * AT_KV_BYTES);
+  uint64_t* kv_full = bars;       // [2] K_j and V_j landed
+  uint64_t* kv_empty = bars + 2;  // [2] P_j V_j done (the stage may be refilled)
+  uint64_t* s_full = bars + 4;    // [2] S_j computed
+  uint64_t* s_free = bars + 6;    // [2] S buffer read by the softmax
+  uint64_t* p_full = bars + 8;    // [2] P_j stored
+  uint64_t* p_free = bars + 10;   // [2] P_j V_j done (P buffer reusable, O current)
+  uint64_t* q_ready = bars + 12;
+  uint64_t* o_final = bars + 13;
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;  // late (long) query tiles first
   const int h = blockIdx.y, kvh = h / (nh / nkv);
-  const int t0 = qt * FA_BQ;
-  const int qrow0 = t0 + 16 * warp;  // this warp's first query row
-  const uint32_t sbase = fa_smem_u32(fa_smem);
-  // stage s: K at s * 2 * TILE, V at s * 2 * TILE + TILE
-  auto k_tile = [&](int s) { return sbase + (uint32_t)(s * 2 * FA_TILE_BYTES); };
-  auto v_tile = [&](int s) { return sbase + (uint32_t)(s * 2 * FA_TILE_BYTES + FA_TILE_BYTES); };
+  const int q0 = qt * AT_BQ;
+  const int last_row = min(T - 1, q0 + AT_BQ - 1);
+  const int nb = (pos0 + last_row + 1 + AT_BK - 1) / AT_BK;  // key blocks
+  const uint64_t lim = wait_ns;
 
-  const int last_row = min(T - 1, t0 + FA_BQ - 1);
-  const int kend = pos0 + last_row + 1;  // keys [0, kend)
-  const int ntiles = (kend + FA_BK - 1) / FA_BK;
-
-  // K and V tile loads: 64 rows x 16 chunks each, 16 chunks per thread
-  auto load_tile = [&](int kt, int s) {
-    const int k0 = kt * FA_BK;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = tid + FA_THREADS * i;  // 0..1023
-      const int r = idx >> 4, c = idx & 15;
-      const int key = k0 + r;
-      const bool valid = key < kend;
-      const size_t off = ((size_t)(valid ? key : 0) * nkv + kvh) * FA_HD + 8 * c;
-      fa_cp_async16(k_tile(s) + fa_swz(r, c), kc + off, valid);
-      fa_cp_async16(v_tile(s) + fa_swz(r, c), vc + off, valid);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&kv_full[i], 1);
+      tc::mbar_init(&kv_empty[i], 1);
+      tc::mbar_init(&s_full[i], 1);
+      tc::mbar_init(&s_free[i], 4);
+      tc::mbar_init(&p_full[i], 4);
+      tc::mbar_init(&p_free[i], 1);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
-  load_tile(0, 0);
-
-  // Q fragments (rows qrow0 + g8, + 8), scaled so that exp2 gives e^(s/sqrt(hd))
-  const float qscale = 1.4426950408889634f * rsqrtf((float)FA_HD);
-  uint32_t qa[8][4];
-  {
-    const int ra = qrow0 + g8, rb = ra + 8;
-    const float* qa_row = q + ((size_t)(ra < T ? ra : 0) * nh + h) * FA_HD;
-    const float* qb_row = q + ((size_t)(rb < T ? rb : 0) * nh + h) * FA_HD;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int c = 16 * ks + 2 * t4;
-      const float2 x0 = ra < T ? *reinterpret_cast<const float2*>(qa_row + c) : make_float2(0.f, 0.f);
-      const float2 x1 = rb < T ? *reinterpret_cast<const float2*>(qb_row + c) : make_float2(0.f, 0.f);
-      const float2 x2 = ra < T ? *reinterpret_cast<const float2*>(qa_row + c + 8) : make_float2(0.f, 0.f);
-      const float2 x3 = rb < T ? *reinterpret_cast<const float2*>(qb_row + c + 8) : make_float2(0.f, 0.f);
-      qa[ks][0] = fa_pack(x0.x * qscale, x0.y * qscale);
-      qa[ks][1] = fa_pack(x1.x * qscale, x1.y * qscale);
-      qa[ks][2] = fa_pack(x2.x * qscale, x2.y * qscale);
-      qa[ks][3] = fa_pack(x3.x * qscale, x3.y * qscale);
-    }
+    tc::mbar_init(q_ready, 4);
+    tc::mbar_init(o_final, 1);
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
   }
+  if (warp == AT_MMA_WARP) tc::tmem_alloc(tmem_slot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  float oacc[16][4];
+  if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int r = 32 * warp + lane, t = q0 + r;
+    const int pr = pos0 + t;  // this row's position
+    // Q row -> bf16, scaled, into the swizzled K-major tile
+    {
+      const float qscale = 1.4426950408889634f * rsqrtf((float)AT_HD);
+      const float* qr = q + ((size_t)(t < T ? t : 0) * nh + h) * AT_HD;
+#pragma unroll 4
+      for (int c = 0; c < 16; ++c) {
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (t < T) {
+          const float4 a = *reinterpret_cast<const float4*>(qr + 8 * c);
+          const float4 b = *reinterpret_cast<const float4*>(qr + 8 * c + 4);
+          x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+          x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        }
+        uint32_t hi[4], lo[4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) oacc[j][c] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY;  // running max of rows g8, g8 + 8
-  float l_a = 0.f, l_b = 0.f;              // this thread's share of the normalisers
-  const int pa = pos0 + qrow0 + g8, pb = pa + 8;  // query positions
-
-  for (int kt = 0; kt < ntiles; ++kt) {
-    const int s = kt & 1;
-    if (kt + 1 < ntiles) {
-      load_tile(kt + 1, s ^ 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = x[2 * i] * qscale, x1 = x[2 * i + 1] * qscale;
+          hi[i] = tc::pack_bf16x2(x0, x1);
+          lo[i] = tc::pack_bf16x2(x0 - __uint_as_float(hi[i] << 16), x1 - __uint_as_float(hi[i] & 0xFFFF0000u));
+        }
+        const uint32_t off = (uint32_t)(c >> 3) * AT_HALF + tc::sw128_offset(r, c & 7);
+        *reinterpret_cast<uint4*>(sQ + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sQ + 2 * AT_HALF + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(q_ready);
     }
-    __syncthreads();
-    const int k0 = kt * FA_BK;
-    // ---- S = Q K^T: 16 rows x 64 keys per warp
-    float sacc[8][4];
+    const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nb && ok; ++j) {
+      const int b = j & 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag, lim))) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      const uint32_t ts = tq + AT_S_COL + 128u * b;
+      const int k0 = j * AT_BK;
+      const bool diag = k0 + AT_BK - 1 > pos0 + q0;
+      uint32_t v[32];
+      // pass 1: the block's row maximum
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        at_tmem_ld32(ts + 32 * c, v);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+        for (int i = 0; i < 32; ++i) {
+          const float sv = (diag && k0 + 32 * c + i > pr) ? -INFINITY : __uint_as_float(v[i]);
+          mx = fmaxf(mx, sv);
+        }
+      }
+      if (j == 0) {
+        m = mx;
+      } else {
+        const bool need = mx > m + AT_RESCALE_LOG2;
+        if (__any_sync(0xffffffffu, need)) {
+          // O must hold P_{j-1} V_{j-1} before it is rescaled
+          if (!__all_sync(0xffffffffu, tc::mbar_wait(&p_free[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, lim))) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const float alpha = need ? exp2f(m - mx) : 1.f;
+          if (need) m = mx;
+          l *= alpha;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            at_tmem_ld32(tq + AT_O_COL + 32 * c, v);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) sacc[j][c] = 0.f;
-    const uint32_t kb = k_tile(s);
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tc::tmem_st16(tq + AT_O_COL + 32 * c, v);
+            tc::tmem_st16(tq + AT_O_COL + 32 * c + 16, v + 16);
+          }
+          tc::tmem_wait_st();
+        }
+      }
+      // P buffer b is reusable once P_{j-2} V_{j-2} is done
+      if (j >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(&p_free[b], ((j - 2) >> 1) & 1, abort_flag, lim))) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      // pass 2: p = exp2(s - m) as bf16 P, and the normaliser
+      const float mref = m == -INFINITY ? 0.f : m;
+      const uint32_t tp = tq + AT_P_COL + 64u * b;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        at_tmem_ld32(ts + 32 * c, v);
+        uint32_t pw[16];
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {  // key n-tiles 2jp, 2jp+1
-        const int m = lane >> 3, rr = lane & 7;
-        const int key = 8 * (2 * jp + (m >> 1)) + rr;
-        const int chunk = 2 * ks + (m & 1);
-        uint32_t b0, b1, b2, b3;
-        fa_ldsm_x4(kb + fa_swz(key, chunk), b0, b1, b2, b3);
-        fa_mma(sacc[2 * jp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        fa_mma(sacc[2 * jp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        for (int i = 0; i < 16; ++i) {
+          const int key = k0 + 32 * c + 2 * i;
+          float p0 = exp2f(__uint_as_float(v[2 * i]) - mref);
+          float p1 = exp2f(__uint_as_float(v[2 * i + 1]) - mref);
+          if (diag && key > pr) p0 = 0.f;
+          if (diag && key + 1 > pr) p1 = 0.f;
+          const uint32_t w = tc::pack_bf16x2(p0, p1);
+          // the normaliser sums the values P V uses
+          l += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+          pw[i] = w;
+        }
+        tc::tmem_st16(tp + 16 * c, pw);
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&s_free[b]);
+        tc::mbar_arrive(&p_full[b]);
       }
     }
-    // ---- causal mask and online softmax (rows g8 and g8 + 8)
-    const bool diag = k0 + FA_BK - 1 > pos0 + qrow0;  // some key of the tile is past some row's position
-    float mx_a = m_a, mx_b = m_b;
+    // out = O / l
+    if (ok && __all_sync(0xffffffffu, tc::mbar_wait(o_final, 0, abort_flag, lim))) {
+      tc::tc_fence_after();
+      const float il = 1.f / l;
+      float* orow = o + ((size_t)(t < T ? t : 0) * nh + h) * AT_HD;
+      uint32_t v[32];
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        at_tmem_ld32(tq + AT_O_COL + 32 * c, v);
+        if (t < T) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int key = k0 + 8 * j + 2 * t4;
-      if (diag) {
-        if (key > pa) sacc[j][0] = -INFINITY;
-        if (key + 1 > pa) sacc[j][1] = -INFINITY;
-        if (key > pb) sacc[j][2] = -INFINITY;
-        if (key + 1 > pb) sacc[j][3] = -INFINITY;
-      }
-      mx_a = fmaxf(mx_a, fmaxf(sacc[j][0], sacc[j][1]));
-      mx_b = fmaxf(mx_b, fmaxf(sacc[j][2], sacc[j][3]));
-    }
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-    // rows past T see only masked or zero keys; keep their max finite
-    const float ref_a = mx_a == -INFINITY ? 0.f : mx_a;
-    const float ref_b = mx_b == -INFINITY ? 0.f : mx_b;
-    const float al_a = exp2f(m_a - ref_a), al_b = exp2f(m_b - ref_b);  // 0 on the first tile
-    m_a = mx_a;
-    m_b = mx_b;
-    l_a *= al_a;
-    l_b *= al_b;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      oacc[j][0] *= al_a;
-      oacc[j][1] *= al_a;
-      oacc[j][2] *= al_b;
-      oacc[j][3] *= al_b;
-    }
-    // P = exp2(S - m), as bf16 A fragments of P V (keys 16 ks .. 16 ks + 15)
-    uint32_t pfrag[4][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float p0 = exp2f(sacc[j][0] - ref_a), p1 = exp2f(sacc[j][1] - ref_a);
-      const float p2 = exp2f(sacc[j][2] - ref_b), p3 = exp2f(sacc[j][3] - ref_b);
-      l_a += p0 + p1;
-      l_b += p2 + p3;
-      const int ks = j >> 1, hi = j & 1;
-      pfrag[ks][2 * hi + 0] = fa_pack(p0, p1);  // row g8
-      pfrag[ks][2 * hi + 1] = fa_pack(p2, p3);  // row g8 + 8
-    }
-    // ---- O += P V: 16 rows x 128 head dims per warp
-    const uint32_t vb = v_tile(s);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-      for (int jp = 0; jp < 8; ++jp) {  // head-dim n-tiles 2jp, 2jp+1
-        const int m = lane >> 3, rr = lane & 7;
-        const int key = 16 * ks + 8 * (m & 1) + rr;
-        const int chunk = 2 * jp + (m >> 1);
-        uint32_t b0, b1, b2, b3;
-        fa_ldsm_x4_t(vb + fa_swz(key, chunk), b0, b1, b2, b3);
-        fa_mma(oacc[2 * jp], pfrag[ks][0], pfrag[ks][1], pfrag[ks][2], pfrag[ks][3], b0, b1);
-        fa_mma(oacc[2 * jp + 1], pfrag[ks][0], pfrag[ks][1], pfrag[ks][2], pfrag[ks][3], b2, b3);
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(orow + 32 * c + 4 * i) =
+                make_float4(__uint_as_float(v[4 * i]) * il, __uint_as_float(v[4 * i + 1]) * il,
+                            __uint_as_float(v[4 * i + 2]) * il, __uint_as_float(v[4 * i + 3]) * il);
+        }
       }
     }
-    __syncthreads();  // the stage is refilled next
-  }
-  // normalisers: the 4 threads of a row hold parts of it
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  const int ra = qrow0 + g8, rb = ra + 8;
-  const float ia = 1.f / l_a, ib = 1.f / l_b;
+  } else if (warp == AT_LOAD_WARP) {
+    // ------------------------------------------------------------ K, V copies
+    if (lane == 0) {
+      for (int j = 0; j < nb; ++j) {
+        const int st = j & 1;
+        if (!tc::mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, lim)) break;
+        const uint32_t dst = tc::smem_u32(sKV + st * AT_KV_BYTES);
+        const uint32_t bar = tc::smem_u32(&kv_full[st]);
+        tc::mbar_expect_tx(&kv_full[st], AT_KV_BYTES);
+        at_tma_load_3d(dst, &kmap, 0, kvh, j * AT_BK, bar);
+        at_tma_load_3d(dst + AT_HALF, &kmap, 64, kvh, j * AT_BK, bar);
+        at_tma_load_3d(dst + 2 * AT_HALF, &vmap, 0, kvh, j * AT_BK, bar);
+        at_tma_load_3d(dst + 3 * AT_HALF, &vmap, 64, kvh, j * AT_BK, bar);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = tc::idesc_bf16_f32(AT_BQ, AT_BK);
+      const uint32_t idesc_o = tc::idesc_bf16_f32(AT_BQ, AT_HD) | (1u << 16);  // B (V) MN-major
+      const uint64_t qd = tc::sw128_desc(tc::smem_u32(sQ));                  // hi part
+      const uint64_t qld = tc::sw128_desc(tc::smem_u32(sQ + 2 * AT_HALF));   // lo part
+      bool ok = tc::mbar_wait(q_ready, 0, abort_flag, lim);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!tc::mbar_wait_spin(&kv_full[st], (j >> 1) & 1, abort_flag, lim)) return false;
+        if (j >= 2 && !tc::mbar_wait_spin(&s_free[st], ((j - 2) >> 1) & 1, abort_flag, lim)) return false;
+        tc::tc_fence_after();
+        const uint64_t kd = tc::sw128_desc(tc::smem_u32(sKV + st * AT_KV_BYTES));
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int d = 8 * j + 2 * t4;
-    if (ra < T)
-      *reinterpret_cast<float2*>(o + ((size_t)ra * nh + h) * FA_HD + d) = make_float2(oacc[j][0] * ia, oacc[j][1] * ia);
-    if (rb < T)
-      *reinterpret_cast<float2*>(o + ((size_t)rb * nh + h) * FA_HD + d) = make_float2(oacc[j][2] * ib, oacc[j][3] * ib);
+        for (int kk = 0; kk < AT_HD / 16; ++kk) {
+          const uint64_t off = (uint64_t)((kk >> 2) * (AT_HALF >> 4) + 2 * (kk & 3));
+          tc::mma_bf16(tmem + AT_S_COL + 128u * st, qd + off, kd + off, idesc_s, kk != 0);
+          tc::mma_bf16(tmem + AT_S_COL + 128u * st, qld + off, kd + off, idesc_s, 1u);
+        }
+        tc::mma_commit(&s_full[st]);
+        return true;
+      };
+      if (ok) {
+        tc::tc_fence_after();
+        ok = issue_s(0);
+      }
+      for (int j = 0; j < nb && ok; ++j) {
+        if (j + 1 < nb && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        const int b = j & 1;
+        if (!tc::mbar_wait_spin(&p_full[b], (j >> 1) & 1, abort_flag, lim)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t vs = tc::smem_u32(sKV + b * AT_KV_BYTES + 2 * AT_HALF);
+#pragma unroll
+        for (int kk = 0; kk < AT_BK / 16; ++kk)
+          tc::mma_bf16_ts(tmem + AT_O_COL, tmem + AT_P_COL + 64u * b + 8u * kk, at_mn_sw128_desc(vs + 2048u * kk, AT_HALF),
+                          idesc_o, (j | kk) != 0);
+        tc::mma_commit(&p_free[b]);
+        tc::mma_commit(&kv_empty[b]);
+      }
+      if (ok) tc::mma_commit(o_final);
+      // drain: every MMA issued here has completed before TMEM is freed
+      tc::mma_commit(drain);
+      volatile int never = 0;
+      tc::mbar_wait(drain, 0, &never, lim);
+    }
+    __syncwarp();
   }
+
+  if (*abort_flag && threadIdx.x == 0) record_status(status, QMOE_ERR_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == AT_MMA_WARP) tc::tmem_dealloc(tmem, 512);
 }
 
-cudaError_t launch_attention_prefill(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
-                                     int T, int pos0, int nh, int nkv, cudaStream_t st) {
-  const int smem = 2 * 2 * FA_TILE_BYTES;  // two stages of K and V
-  cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(attn_prefill_mma_kernel), smem);
+// A cache [positions][nkv][128] bf16 as a 3-D tensor map over positions
+// [0, rows): boxes of 64 head dims x 1 KV head x 128 positions, 128-byte
+// swizzle; positions from ``rows`` on read as zero.
+static bool at_encode_cache(CUtensorMap* m, const void* base, int nkv, int rows) {
+  struct Entry {
+    const void* base;
+    int nkv, rows;
+    CUtensorMap map;
+  };
+  static Entry cache[8];
+  static int n = 0, next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (cache[i].base == base && cache[i].nkv == nkv && cache[i].rows == rows) {
+      *m = cache[i].map;
+      return true;
+    }
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)AT_HD, (cuuint64_t)nkv, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)AT_HD * 2, (cuuint64_t)nkv * AT_HD * 2};
+  const cuuint32_t box[3] = {64, 1, AT_BK};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache[next] = Entry{base, nkv, rows, *m};
+  next = (next + 1) % 8;
+  if (n < 8) ++n;
+  return true;
+}
+
+cudaError_t launch_attention_prefill_tc(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
+                                        int T, int pos0, int nh, int nkv, int* status, unsigned long long wait_ns,
+                                        cudaStream_t st) {
+  if (T < 1 || nkv < 1 || nh % nkv != 0) return cudaErrorInvalidValue;
+  CUtensorMap km, vm;
+  if (!at_encode_cache(&km, kc, nkv, pos0 + T) || !at_encode_cache(&vm, vc, nkv, pos0 + T))
+    return cudaErrorInvalidValue;
+  cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(attn_prefill_tc_kernel), AT_SMEM);
   if (e != cudaSuccess) return e;
-  attn_prefill_mma_kernel<<<dim3((T + FA_BQ - 1) / FA_BQ, nh), FA_THREADS, smem, st>>>(q, kc, vc, o, T, pos0, nh,
-                                                                                       nkv);
+  attn_prefill_tc_kernel<<<dim3((T + AT_BQ - 1) / AT_BQ, nh), AT_THREADS, AT_SMEM, st>>>(
+      q, o, T, pos0, nh, nkv, status, wait_ns ? wait_ns : tc::kWaitLimitNs, km, vm);
   return cudaGetLastError();
 }
 
