@@ -227,17 +227,44 @@ __device__ __forceinline__ void bitonic_desc(uint64_t (&v)[KMAX]) {
       if ((i & d) == 0) cas_desc(v[i], v[i + d]);
 }
 
+// Sorts KMAX keys into descending order (a bitonic sorting network: depth
+// log2(KMAX) (log2(KMAX) + 1) / 2, the compare-exchanges of a stage independent).
+template <int KMAX>
+__device__ __forceinline__ void bitonic_sort_desc(uint64_t (&v)[KMAX]) {
+#pragma unroll
+  for (int size = 2; size <= KMAX; size <<= 1)
+#pragma unroll
+    for (int d = size / 2; d > 0; d >>= 1)
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) {
+        const int j = i ^ d;
+        if (j > i) {
+          if ((i & size) == 0) cas_desc(v[i], v[j]);  // a descending run
+          else cas_desc(v[j], v[i]);                  // an ascending run
+        }
+      }
+}
+
 // The k best experts of one row of E logits (L, shared memory), in selection
-// order, into sel_e / sel_l; one warp, KMAX >= k a power of two.
+// order, into sel_e / sel_l; one warp, KMAX >= k a power of two. Each lane
+// sorts groups of KMAX of its experts and keeps the best KMAX seen.
 template <int KMAX>
 __device__ __forceinline__ void warp_topk(const float* L, int E, int k, int lane, int32_t* sel_e, float* sel_l) {
   uint64_t top[KMAX];
 #pragma unroll
   for (int i = 0; i < KMAX; ++i) top[i] = 0;  // below every key
-  for (int e = lane; e < E; e += 32) {
-    uint64_t key = sel_key(L[e], e);
+  for (int e0 = 0; e0 < E; e0 += 32 * KMAX) {
+    uint64_t g[KMAX];
 #pragma unroll
-    for (int i = 0; i < KMAX; ++i) cas_desc(top[i], key);  // insert; the smallest falls out
+    for (int i = 0; i < KMAX; ++i) {
+      const int e = e0 + lane + 32 * i;
+      g[i] = e < E ? sel_key(L[e], e) : 0;
+    }
+    bitonic_sort_desc<KMAX>(g);
+    // the best KMAX of top and g: a bitonic sequence, then sorted
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) top[i] = top[i] > g[KMAX - 1 - i] ? top[i] : g[KMAX - 1 - i];
+    bitonic_desc<KMAX>(top);
   }
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
