@@ -673,6 +673,8 @@ def record_traffic(args):
         rows = [r for r in csv.reader(f) if len(r) > 5]
     hdr = rows[0]
     ki, mi, vi, ii = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value"), hdr.index("ID")
+    ui = hdr.index("Metric Unit") if "Metric Unit" in hdr else None
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     for r in rows[1:]:
         name = r[ki].replace(" ", "")
         if not any(n.replace(" ", "") in name for n in names):
@@ -680,7 +682,7 @@ def record_traffic(args):
         if r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             continue
         d = per_launch.setdefault(r[ii], {"name": name, "bytes": 0.0})
-        d["bytes"] += float(r[vi].replace(",", ""))
+        d["bytes"] += float(r[vi].replace(",", "")) * (scale[r[ui]] if ui is not None else 1.0)
     units = sum(1 for d in per_launch.values() if first.replace(" ", "") in d["name"])
     total = sum(d["bytes"] for d in per_launch.values())
     if units == 0:

@@ -371,8 +371,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       bool ok = tc::mbar_wait(q_ready, 0, abort_flag, lim);
       for (int j = 0; j < nb && ok; ++j) {
         const int st = j & 1;
-        if (!tc::mbar_wait_spin(&k_full[st], (j >> 1) & 1, abort_flag, lim) ||
-            (j >= 2 && !tc::mbar_wait_spin(&s_free[st], ((j - 2) >> 1) & 1, abort_flag, lim))) {
+        if (!tc::mbar_wait_poll(&k_full[st], (j >> 1) & 1, abort_flag, lim) ||
+            (j >= 2 && !tc::mbar_wait_poll(&s_free[st], ((j - 2) >> 1) & 1, abort_flag, lim))) {
           ok = false;
           break;
         }
@@ -401,8 +401,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       bool ok = true;
       for (int j = 0; j < nb && ok; ++j) {
         const int b = j & 1;
-        if (!tc::mbar_wait_spin(&v_full[b], (j >> 1) & 1, abort_flag, lim) ||
-            !tc::mbar_wait_spin(&p_full[b], (j >> 1) & 1, abort_flag, lim)) {
+        // (polling waits: a suspended issuer wakes up late, and each block's
+        // P V is on the critical path)
+        if (!tc::mbar_wait_poll(&v_full[b], (j >> 1) & 1, abort_flag, lim) ||
+            !tc::mbar_wait_poll(&p_full[b], (j >> 1) & 1, abort_flag, lim)) {
           ok = false;
           break;
         }
