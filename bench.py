@@ -37,6 +37,12 @@ sys.path.insert(0, ROOT)
 
 H, E, K_TOP, F = 2048, 256, 8, 512
 EXPERT_BYTES = 2 * F * (H // 256) * 144 + H * (F // 256) * 176   # 1 900 544
+QTYPE_BYTES = {"q4k": 144, "q5k": 176, "q6k": 210, "mxfp4": 136}
+DOWN_TYPE = "q5k"  # the down projection's format (set from --down-type)
+
+
+def expert_bytes():
+    return 2 * F * (H // 256) * 144 + H * (F // 256) * QTYPE_BYTES[DOWN_TYPE]
 GATEUP_EXPERT_BYTES = 2 * F * (H // 256) * 144                    # 1 179 648
 KERNEL_SOURCES = {
     "decode": ["quantized_moe_transformer_gb300/csrc/moe_decode.cu",
@@ -68,6 +74,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     p.add_argument("--layers", type=int, default=16)
+    p.add_argument("--down-type", choices=["q5k", "q6k", "mxfp4"], default="q5k",
+                   help="format of the down projections (q6k and mxfp4 run on the grouped GEMV kernels)")
     p.add_argument("--T", type=int, default=None, help="override the workload's row count")
     p.add_argument("--routing", choices=["uniform", "zipf"], default=None)
     p.add_argument("--gemm-threshold", type=int, default=None,
@@ -88,9 +96,11 @@ def workload_config(name, T, routing, layers):
     what = ("attention (16 q heads, 2 kv heads, hd 128, bf16 cache of 4096) + routed-MoE block"
             if WORKLOADS[name].get("block") else "routed-MoE layer")
     return {"workload": f"{name}: {what}, T={T} rows, H={H}, E={E}, top-{K_TOP}, F={F}, "
-                        f"shared expert, Q4_K gate/up, Q5_K down, fp32 hidden, {routing} routing",
+                        f"shared expert, Q4_K gate/up, {DOWN_TYPE.upper().replace('K', '_K')} down, "
+                        f"fp32 hidden, {routing} routing",
             "T": T, "H": H, "E": E, "top_k": K_TOP, "F": F, "routing": routing,
-            "l2": f"{layers} distinct layer instances rotated ({layers * EXPERT_BYTES * 257 / 1e9:.1f} GB "
+            "down_type": DOWN_TYPE,
+            "l2": f"{layers} distinct layer instances rotated ({layers * expert_bytes() * 257 / 1e9:.1f} GB "
                   f"> 129 MB L2)",
             "parallelism": "replicas"}
 
@@ -223,9 +233,17 @@ def make_layer_on_device(torch, seed, routing, device, from_arrays=None):
     g.manual_seed(seed)
 
     def blocks(n, nb):
+        # the distributions of inputs.packed_blocks: Q4_K/Q5_K d, dmin in
+        # [2^-12, 2^-10]; Q6_K d in [2^-14, 2^-12]; MXFP4 exponents 119..124
         b = torch.randint(0, 256, (n, nb), dtype=torch.uint8, device=device, generator=g)
-        dd = torch.empty((n, 2), device=device).uniform_(2.0**-12, 2.0**-10, generator=g)
-        b[:, 0:4] = dd.half().view(torch.uint8).reshape(n, 4)
+        if nb in (144, 176):
+            dd = torch.empty((n, 2), device=device).uniform_(2.0**-12, 2.0**-10, generator=g)
+            b[:, 0:4] = dd.half().view(torch.uint8).reshape(n, 4)
+        elif nb == 210:
+            dd = torch.empty((n, 1), device=device).uniform_(2.0**-14, 2.0**-12, generator=g)
+            b[:, 0:2] = dd.half().view(torch.uint8).reshape(n, 2)
+        else:
+            b[:, 0:8] = torch.randint(119, 125, (n, 8), dtype=torch.uint8, device=device, generator=g)
         return b
 
     Wr = torch.randn((H, E), device=device, generator=g) * 0.02
@@ -235,11 +253,12 @@ def make_layer_on_device(torch, seed, routing, device, from_arrays=None):
     nb = H // 256
     Wg = blocks(E * F * nb, 144).reshape(E, F, nb, 144)
     Wu = blocks(E * F * nb, 144).reshape(E, F, nb, 144)
-    Wd = blocks(E * H * (F // 256), 176).reshape(E, H, F // 256, 176)
+    db = QTYPE_BYTES[DOWN_TYPE]
+    Wd = blocks(E * H * (F // 256), db).reshape(E, H, F // 256, db)
     Sg = blocks(F * nb, 144).reshape(F, nb, 144)
     Su = blocks(F * nb, 144).reshape(F, nb, 144)
-    Sd = blocks(H * (F // 256), 176).reshape(H, F // 256, 176)
-    return qb.MoeLayer(H, E, K_TOP, F, Wr.contiguous(), Wg, Wu, Wd, Sg, Su, Sd, "q4k", "q5k")
+    Sd = blocks(H * (F // 256), db).reshape(H, F // 256, db)
+    return qb.MoeLayer(H, E, K_TOP, F, Wr.contiguous(), Wg, Wu, Wd, Sg, Su, Sd, "q4k", DOWN_TYPE)
 
 
 CTX = 4096
@@ -430,7 +449,7 @@ def distinct_experts(torch, qb, layers, step, ws, ws_off, T, NL, stream):
 
 
 def layer_bytes(u_mean, T):
-    return (u_mean + 1) * EXPERT_BYTES + H * E * 4 + 2 * T * H * 4
+    return (u_mean + 1) * expert_bytes() + H * E * 4 + 2 * T * H * 4
 
 
 def layer_flops(T):
@@ -522,7 +541,7 @@ def ours_main(args, rank, world, local_rank):
 
     is_block = wl.get("block", False)
     pos0 = wl.get("pos0", 0)
-    arr0 = inputs.moe_layer(0, H, E, F, shared=True, routing=routing)
+    arr0 = inputs.moe_layer(0, H, E, F, shared=True, routing=routing, down_type=DOWN_TYPE)
     layers = [make_layer_on_device(torch, 1000 * rank + i, routing, device,
                                    arr0 if i == 0 else None) for i in range(NL)]
     stream = torch.cuda.Stream(device=device)
@@ -698,7 +717,9 @@ def record_traffic(args):
 
 
 def main():
+    global DOWN_TYPE
     args = parse()
+    DOWN_TYPE = args.down_type
     if args.record_traffic:
         record_traffic(args)
         return
