@@ -575,9 +575,13 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     return QMOE_OK;
   }
   const bool small = P <= 2048;
+  // the tensor-core kernels take Q4_K/Q5_K weights, and Q6_K down weights
+  // (whole rows by bulk copies) with F up to 512
+  const bool tc_formats = d->gate_type <= QMOE_Q5K &&
+                          (d->down_type <= QMOE_Q5K || (d->down_type == QMOE_Q6K && F <= 512));
+  const bool use_tc = tc_formats && T > g_gemm_threshold.load();
   // on the tensor-core path at large T the permutation scan also builds the
   // token-chunk list
-  const bool use_tc = kquant && T > g_gemm_threshold.load();
   const bool chunks_in_scan = use_tc && !small;
   int2* tc_chunks = reinterpret_cast<int2*>(base + L.chunks);
   int32_t* tc_n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);

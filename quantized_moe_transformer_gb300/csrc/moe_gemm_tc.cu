@@ -80,17 +80,27 @@ constexpr int TC_N_MIN = 64;                  // the smaller chunk cap (bounds t
 // the 512 TMEM columns and the A stages (128 columns each: K = 128 for both
 // matrices) the rest, so a cap of 64 rows buys 3 A stages instead of 2; it is
 // chosen when experts get few rows (T * k / E <= 32).
+// Q6_K weights (down pass only): a 210-byte super-block is only 2-byte
+// aligned, so neither a tensor-map box nor a bulk copy can take one
+// super-block column. An item's 256 rows of the down matrix are contiguous
+// and 16-byte aligned instead (256 x 210 bytes is a multiple of 16): the
+// weight loader copies all of them (both super-blocks for K <= 512) into the
+// one raw stage with four bulk copies.
+template <int QT>
+__host__ __device__ constexpr bool tc_rowcopy() { return QT == QMOE_Q6K; }
+constexpr int TC_ROWCOPY_KB = 2;  // super-blocks along K that the raw stage holds
+
 template <int QT, int NMAX>
 struct TcCfg {
-  static constexpr int BYTES = QT == QMOE_Q5K ? Q5K_BYTES : Q4K_BYTES;
+  static constexpr int BYTES = qtype_size(QT);
   static constexpr int S = (512 - 2 * NMAX) / (int)TC_A_STAGE_COLS;  // A stages in TMEM
   static constexpr uint32_t D1_COL = NMAX;                          // D0 at column 0
   static constexpr uint32_t A_COL = 2 * NMAX;                       // A stage s at A_COL + 128 s
   static constexpr int B_HALF = NMAX * 128;                         // K 64 x NMAX rows, one swizzle atom row each
   static constexpr int B_BYTES = 2 * B_HALF;                        // token tile per stage: two K halves
-  static constexpr int RS = (QT == QMOE_Q5K && NMAX == 128) ? 2 : 3;
+  static constexpr int RS = tc_rowcopy<QT>() ? 1 : ((QT == QMOE_Q5K && NMAX == 128) ? 2 : 3);
   static constexpr int TS = NMAX == 64 ? (QT == QMOE_Q5K ? 4 : 5) : 3;
-  static constexpr int RAW_STAGE = 256 * BYTES;
+  static constexpr int RAW_STAGE = tc_rowcopy<QT>() ? 256 * TC_ROWCOPY_KB * BYTES : 256 * BYTES;
   static constexpr int SMEM = TS * B_BYTES + RS * RAW_STAGE + TC_EPI_WARPS * TC_EPI_BYTES + 1024 /*align*/ +
                               512 /*barriers*/;
 };
@@ -177,6 +187,72 @@ __device__ __forceinline__ void dequant_sub(const uint4 hdr, const uint4 qv, uin
       ev |= spread4(hb >> (8 * n), 0);
       od |= spread4(hb >> (8 * n), 1);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t src = (i & 1) ? od : ev;
+      const uint32_t blo = (uint32_t)(i >> 1), bhi = blo + 2;  // weights 8n+i, 8n+i+4
+      const uint64_t f2 = pack2(__byte_perm(src, 0x3F000000u, 0x7044u | (blo << 8)),
+                                __byte_perm(src, 0x3F000000u, 0x7044u | (bhi << 8)));
+      const float2 wv = unpack2(ffma2(f2, a2, c2));
+      o[4 * n + i] = tc::pack_bf16x2(wv.x, wv.y);
+    }
+  }
+}
+
+// Q6_K: 32 weights (group g of a 210-byte super-block at ``blk``, 2-byte
+// aligned in shared memory) into 16 bf16x2 words in kPerm8 order. Weight i
+// of the super-block is d * s_{i/16} * (q_i - 32), q_i = its low nibble
+// (byte 82 + i/2, the high nibble for odd i) + 16 * its 2-bit high part
+// (byte 18 + i/4, bits 2 (i % 4)); the s are signed bytes at 2. As in
+// dequant_sub the quant enters as f = 0.5 + q/256 (a byte permute into a
+// float's mantissa; q < 64) and w = f * (256 d s) - 160 d s is one fp32 FMA
+// (both constants exact: d s has at most 19 significant bits), rounded once
+// to bf16.
+__device__ __forceinline__ uint32_t lds_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// The 16 bytes at ``p`` (2-byte aligned, shared memory) as four words.
+__device__ __forceinline__ uint4 lds16_align2(const uint8_t* p) {
+  const uint32_t off = (uint32_t)(reinterpret_cast<uintptr_t>(p) & 3u);
+  const uint8_t* a = p - off;
+  const uint32_t w0 = lds_u32(a), w1 = lds_u32(a + 4), w2 = lds_u32(a + 8), w3 = lds_u32(a + 12);
+  if (off == 0) return make_uint4(w0, w1, w2, w3);
+  const uint32_t w4 = lds_u32(a + 16);  // off == 2: the piece ends 2 bytes into this word
+  return make_uint4(__funnelshift_r(w0, w1, 16), __funnelshift_r(w1, w2, 16), __funnelshift_r(w2, w3, 16),
+                    __funnelshift_r(w3, w4, 16));
+}
+
+__device__ __forceinline__ uint2 lds8_align2(const uint8_t* p) {
+  const uint32_t off = (uint32_t)(reinterpret_cast<uintptr_t>(p) & 3u);
+  const uint8_t* a = p - off;
+  const uint32_t w0 = lds_u32(a), w1 = lds_u32(a + 4);
+  if (off == 0) return make_uint2(w0, w1);
+  const uint32_t w2 = lds_u32(a + 8);
+  return make_uint2(__funnelshift_r(w0, w1, 16), __funnelshift_r(w1, w2, 16));
+}
+
+__device__ __forceinline__ void dequant_q6k_group(const uint8_t* blk, int g, uint32_t* o) {
+  const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk)));
+  const uint32_t s2 = (uint32_t)*reinterpret_cast<const unsigned short*>(blk + 2 + 2 * g);
+  const float ds0 = d * (float)(int8_t)(s2 & 0xFFu), ds1 = d * (float)(int8_t)(s2 >> 8);
+  const uint32_t a0 = __float_as_uint(256.f * ds0), c0 = __float_as_uint(-160.f * ds0);
+  const uint32_t a1 = __float_as_uint(256.f * ds1), c1 = __float_as_uint(-160.f * ds1);
+  const uint4 qv = lds16_align2(blk + 82 + 16 * g);
+  const uint2 hv = lds8_align2(blk + 18 + 8 * g);  // 2-bit high parts of the group's 32 weights
+  const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    // the high parts of weights 8n .. 8n + 7 (2 bits each), bytes duplicated:
+    // a = [b0, b0, b1, b1] with b0 = weights 8n..8n+3, b1 = 8n+4..8n+7
+    const uint32_t hh = ((n < 2 ? hv.x : hv.y) >> (16 * (n & 1))) & 0xFFFFu;
+    const uint32_t a = __byte_perm(hh, 0u, 0x1100u);
+    // weights 8n + 2k (byte k of ev) and 8n + 2k + 1 (byte k of od): their
+    // high parts moved to bits 4-5 of byte k
+    const uint32_t ev_hi = ((a << 4) & 0x00300030u) | (a & 0x30003000u);
+    const uint32_t od_hi = ((a << 2) & 0x00300030u) | ((a >> 2) & 0x30003000u);
+    const uint32_t ev = (w[n] & 0x0F0F0F0Fu) | ev_hi;
+    const uint32_t od = ((w[n] >> 4) & 0x0F0F0F0Fu) | od_hi;
+    const uint64_t a2 = n < 2 ? pack2(a0, a0) : pack2(a1, a1);  // 16 weights per scale
+    const uint64_t c2 = n < 2 ? pack2(c0, c0) : pack2(c1, c1);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t src = (i & 1) ? od : ev;
@@ -360,12 +436,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       const int r = 32 * (pw & 3) + lane;
       const uint32_t ta0 =
           tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * (TC_BK / 2) + sp * 32);
-      const uint8_t* my_row = sRaw + (size_t)(mat * 128 + r) * BYTES;
+      // (whole rows: the item's rows, every super-block, in one stage)
+      constexpr bool ROWCOPY = tc_rowcopy<QT>();
+      const size_t row_pitch = ROWCOPY ? (size_t)KB * BYTES : (size_t)BYTES;
+      const uint8_t* my_row = sRaw + (size_t)(mat * 128 + r) * row_pitch;
       const int NU = n_mine * KB;
       uint32_t wa[16], wb[16];
       uint4 hdr = make_uint4(0, 0, 0, 0), hq0 = hdr, hq1 = hdr;
       // loads the super-block header (and Q5_K high bits) of ring slot u % RS
       auto open_sb = [&](int u) -> bool {
+        if constexpr (ROWCOPY) {
+          // the stage holds item u / KB; its first super-block waits for it
+          return u % KB != 0 ||
+                 __all_sync(0xffffffffu, tc::mbar_wait(&raw_full[0], (u / KB) & 1, abort_flag, lim));
+        }
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&raw_full[u % RS], (u / RS) & 1, abort_flag, lim))) return false;
         const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
         hdr = rp[0];
@@ -377,6 +461,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     };
     // sub-blocks 4 hh + 2 sp and + 1 of super-block u
     auto deq = [&](int u, int hh) {
+      if constexpr (ROWCOPY) {
+        const uint8_t* blk = my_row + (size_t)(u % KB) * BYTES;
+        dequant_q6k_group(blk, 4 * hh + 2 * sp, wa);
+        dequant_q6k_group(blk, 4 * hh + 2 * sp + 1, wb);
+        return;
+      }
       const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
       const int j0 = 4 * hh + 2 * sp;
       const uint4 q0 = rp[(QT == QMOE_Q5K ? 3 : 1) + j0];
@@ -420,9 +510,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
           deq(u, 1);
         } else {
           // every read of slot u is done: release it to the weight loader
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&raw_empty[u % RS]);
+          // (whole rows: after the item's last super-block)
+          if (!ROWCOPY || u % KB == KB - 1) {
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&raw_empty[ROWCOPY ? 0 : u % RS]);
+          }
           if (u + 1 < NU) {
             if (!open_sb(u + 1)) ok = false;
             else deq(u + 1, 0);
@@ -452,7 +545,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         e = ch.e;
         y0 = GATEUP ? (e < g.E ? e * g.F : 0) + blk * 128 : (e < g.E ? e * g.H : 0) + blk * 256;
       };
-      for (int u = 0; u < NU; ++u) {
+      if constexpr (tc_rowcopy<QT>()) {
+        // item j: its 256 rows (every super-block) as four bulk copies of 64
+        // rows, each 16-byte aligned (64 x 210 x KB bytes)
+        const size_t pitch = (size_t)KB * BYTES;
+        for (int j = 0; j < n_mine; ++j) {
+          if (!tc::mbar_wait(&raw_empty[0], (j & 1) ^ 1, abort_flag, lim)) break;
+          int e, y0;
+          block_of(j, e, y0);
+          const uint8_t* src = (e < g.E ? g.W : g.S) + (size_t)y0 * pitch;
+          tc::mbar_expect_tx(&raw_full[0], (uint32_t)(256 * pitch));
+          for (int q = 0; q < 4; ++q)
+            tc::bulk_g2s(sRaw + (size_t)q * 64 * pitch, src + (size_t)q * 64 * pitch, (uint32_t)(64 * pitch),
+                         &raw_full[0]);
+        }
+      }
+      for (int u = 0; u < NU && !tc_rowcopy<QT>(); ++u) {
         const int slot = u % RS;
         if (!tc::mbar_wait(&raw_empty[slot], ((u / RS) & 1) ^ 1, abort_flag, lim)) break;
         const int j = u / KB, sb = u % KB;
@@ -840,6 +948,16 @@ cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
   const uint32_t bytes = (uint32_t)qtype_bytes(p.qt);
   const uint64_t rb = (uint64_t)(p.F / QK) * bytes;
   TcMaps m;
+  if (p.qt == QMOE_Q6K) {
+    // whole rows by bulk copies (no weight tensor maps)
+    if (p.F / QK > TC_ROWCOPY_KB || !encode_tokens(&m.tok, p.hin, (uint64_t)p.tok_rows, (uint64_t)p.F))
+      return cudaErrorInvalidValue;
+    memset(&m.w, 0, sizeof(m.w));
+    memset(&m.s, 0, sizeof(m.s));
+    memset(&m.w2, 0, sizeof(m.w2));
+    memset(&m.s2, 0, sizeof(m.s2));
+    return tc_launch_t<false, QMOE_Q6K>(a, m, p.max_chunks * (p.H / 256), p.nmax, st);
+  }
   if (!encode_rows(&m.w, p.W, (uint64_t)p.E * p.H, rb, bytes, 256) ||
       !encode_rows(&m.s, p.S, (uint64_t)p.H, rb, bytes, 256) ||
       !encode_tokens(&m.tok, p.hin, (uint64_t)p.tok_rows, (uint64_t)p.F))

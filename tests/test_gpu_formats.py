@@ -6,9 +6,10 @@ paragraphs: the pages run a Q4_K_M model file, a file type that keeps some
 tensors (typically the down projections) in Q6_K. "Distributed CPU: Zip Fusion
 Beyond Tensor Parallelism", "Decode vs Prefill: Same Weights, Different
 Bottlenecks": the model class it targets carries MXFP4-class weights. Layers
-with either format on the down projection (and on gate/up) run on the grouped
-GEMV path at every row count, with fp32 accumulation, so the fp32 tolerance
-applies.
+with either format run on the grouped GEMV kernels (fp32 accumulation, the
+fp32 tolerance), except Q6_K down projections next to Q4_K gate/up above the
+tensor-core threshold: those take the tcgen05 kernels (whole weight rows by
+bulk copies, bf16 operands, the tensor-core tolerance).
 """
 
 import numpy as np
@@ -17,7 +18,7 @@ import torch
 
 from quantized_moe_transformer_gb300 import binding as qb
 from quantized_moe_transformer_gb300 import inputs
-from tests.parity import GAP, TOL_GEMV, assert_close, check_routes
+from tests.parity import GAP, TOL_GEMV, TOL_TC, assert_close, check_routes
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +47,11 @@ def layer(gate, down, seed=3):
     return _layers[key]
 
 
+def expected_path(arr, T):
+    tc = (arr["Wg"].shape[-1] == 144 and arr["Wd"].shape[-1] == 210 and T > qb.get_gemm_threshold())
+    return "gemm_tc" if tc else "gemv"
+
+
 def run(oracle, arr, lay, T, seed, rows=None):
     X = inputs.hidden(seed, T, H)
     R = inputs.residual(seed, T, H)
@@ -53,14 +59,15 @@ def run(oracle, arr, lay, T, seed, rows=None):
     out = qb.moe_forward(lay, torch.from_numpy(X).cuda(), torch.from_numpy(R).cuda(), ws=ws)
     torch.cuda.synchronize()
     assert qb.query_status() == 0
-    assert qb.last_path() == "gemv"
+    path = expected_path(arr, T)
+    assert qb.last_path() == path
     if rows is None:
         rows = np.arange(T)
     L = lay.workspace_layout(T)
     ids = ws[L.ids:L.ids + 4 * T * K].view(torch.int32).reshape(T, K).cpu().numpy()
     ref, parts = oracle.moe_forward_rows(X, arr, K, rows, R)
     ok = check_routes(ids[rows], parts["ids"], parts["gap"], parts["logits"])
-    assert_close(out.cpu().numpy()[rows], ref, TOL_GEMV, rows=ok)
+    assert_close(out.cpu().numpy()[rows], ref, TOL_TC if path == "gemm_tc" else TOL_GEMV, rows=ok)
 
 
 @pytest.mark.parametrize("down", ["q6k", "mxfp4"])
@@ -88,14 +95,30 @@ def test_tiny_layer_all_rows(oracle):
         X = inputs.hidden(6, 33, 256)
         out = qb.moe_forward(lay, torch.from_numpy(X).cuda())
         torch.cuda.synchronize()
-        assert qb.query_status() == 0 and qb.last_path() == "gemv"
-        assert_close(out.cpu().numpy(), oracle.moe_forward(X, arr, 2), TOL_GEMV)
+        path = expected_path(arr, 33)
+        assert qb.query_status() == 0 and qb.last_path() == path
+        assert_close(out.cpu().numpy(), oracle.moe_forward(X, arr, 2), TOL_TC if path == "gemm_tc" else TOL_GEMV)
+
+
+def test_q6k_down_tensor_cores_large(oracle):
+    """Q6_K down weights on the tensor-core path at T = 4096 (every expert cut
+    into token chunks, many work items per SM), sampled rows, and the same
+    layer through the GEMV kernels (threshold raised) on one row."""
+    arr, lay = layer("q4k", "q6k")
+    run(oracle, arr, lay, 4096, 31, rows=np.array([0, 1, 2047, 4095]))
+    old = qb.get_gemm_threshold()
+    qb.set_gemm_threshold(1 << 20)
+    try:
+        run(oracle, arr, lay, 6, 32)
+    finally:
+        qb.set_gemm_threshold(old)
 
 
 def test_q6k_field_extremes(oracle):
     """Q6_K down blocks at the field extremes: every quant 63 or 0 (all low
     nibbles and high parts set, or none), scales +127 and -128, fp16 d at its
-    largest normal; the result is checked on sampled rows."""
+    largest normal; on the GEMV kernels (T = 2) and the tensor-core kernels
+    (T = 37, sampled rows)."""
     arr, _ = layer("q4k", "q6k")
     arr = dict(arr)
     Wd = arr["Wd"].copy()
@@ -111,6 +134,7 @@ def test_q6k_field_extremes(oracle):
     arr["Sd"] = Sd
     lay = qb.MoeLayer.from_arrays(arr, K)
     run(oracle, arr, lay, 2, 21)
+    run(oracle, arr, lay, 37, 23, rows=np.array([0, 18, 36]))  # the tensor-core path
 
 
 def test_mxfp4_every_code_and_scale(oracle):
