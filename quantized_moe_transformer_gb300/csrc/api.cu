@@ -575,10 +575,11 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     return QMOE_OK;
   }
   const bool small = P <= 2048;
-  // the tensor-core kernels take Q4_K/Q5_K weights, and Q6_K down weights
-  // (whole rows by bulk copies) with F up to 512
+  // the tensor-core kernels take Q4_K/Q5_K weights, and Q6_K or MXFP4 down
+  // weights (whole rows by bulk copies) with F up to 512
   const bool tc_formats = d->gate_type <= QMOE_Q5K &&
-                          (d->down_type <= QMOE_Q5K || (d->down_type == QMOE_Q6K && F <= 512));
+                          (d->down_type <= QMOE_Q5K ||
+                           ((d->down_type == QMOE_Q6K || d->down_type == QMOE_MXFP4) && F <= 512));
   const bool use_tc = tc_formats && T > g_gemm_threshold.load();
   // on the tensor-core path at large T the permutation scan also builds the
   // token-chunk list

@@ -80,14 +80,14 @@ constexpr int TC_N_MIN = 64;                  // the smaller chunk cap (bounds t
 // the 512 TMEM columns and the A stages (128 columns each: K = 128 for both
 // matrices) the rest, so a cap of 64 rows buys 3 A stages instead of 2; it is
 // chosen when experts get few rows (T * k / E <= 32).
-// Q6_K weights (down pass only): a 210-byte super-block is only 2-byte
-// aligned, so neither a tensor-map box nor a bulk copy can take one
-// super-block column. An item's 256 rows of the down matrix are contiguous
-// and 16-byte aligned instead (256 x 210 bytes is a multiple of 16): the
-// weight loader copies all of them (both super-blocks for K <= 512) into the
-// one raw stage with four bulk copies.
+// Q6_K and MXFP4 weights (down pass only): a 210- or 136-byte super-block is
+// only 2- or 8-byte aligned, so neither a tensor-map box nor a bulk copy can
+// take one super-block column. An item's 256 rows of the down matrix are
+// contiguous and 16-byte aligned instead (256 x 210 and 256 x 136 bytes are
+// multiples of 16): the weight loader copies all of them (every super-block
+// for K <= 512) into the one raw stage with four bulk copies.
 template <int QT>
-__host__ __device__ constexpr bool tc_rowcopy() { return QT == QMOE_Q6K; }
+__host__ __device__ constexpr bool tc_rowcopy() { return QT == QMOE_Q6K || QT == QMOE_MXFP4; }
 constexpr int TC_ROWCOPY_KB = 2;  // super-blocks along K that the raw stage holds
 
 template <int QT, int NMAX>
@@ -261,6 +261,39 @@ __device__ __forceinline__ void dequant_q6k_group(const uint8_t* blk, int g, uin
                                 __byte_perm(src, 0x3F000000u, 0x7044u | (bhi << 8)));
       const float2 wv = unpack2(ffma2(f2, a2, c2));
       o[4 * n + i] = tc::pack_bf16x2(wv.x, wv.y);
+    }
+  }
+}
+
+// MXFP4: 32 weights (group g of a 136-byte super-block at ``blk``, 8-byte
+// aligned in shared memory) into 16 bf16x2 words in kPerm8 order. Weight i is
+// E2M1(code_i) * 2^(e_{i/32} - 127): the codes' magnitudes 0, 0.5, 1, 1.5, 2,
+// 3, 4, 6 as q = 2 |v| (one byte permute from an 8-entry table picks four),
+// f = 0.5 + q/256 (a byte permute into a float's mantissa), w = f * 128 s -
+// 64 s = |v| s in one fp32 FMA, exact, and the code's sign bit moved into
+// each bf16 half by a shift and an exclusive or. The products of E2M1 values
+// and powers of two are exact in bf16 (up to overflow and the flush of fp32
+// subnormals to zero).
+__device__ __forceinline__ void dequant_mxfp4_group(const uint8_t* blk, int g, uint32_t* o) {
+  const uint32_t e = blk[g];
+  const float sc = __uint_as_float(e == 0u ? 0x00400000u : (e == 255u ? 0x7FC00000u : e << 23));
+  const uint64_t a2 = pack2(__float_as_uint(128.f * sc), __float_as_uint(128.f * sc));
+  const uint64_t c2 = pack2(__float_as_uint(-64.f * sc), __float_as_uint(-64.f * sc));
+  const uint2 c01 = *reinterpret_cast<const uint2*>(blk + 8 + 16 * g);
+  const uint2 c23 = *reinterpret_cast<const uint2*>(blk + 16 + 16 * g);
+  const uint32_t w[4] = {c01.x, c01.y, c23.x, c23.y};
+  constexpr uint32_t LUT0 = 0x03020100u, LUT1 = 0x0C080604u;  // q = 2 |v| of magnitude codes 0..7
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    const uint32_t sel = w[n] & 0x77777777u;       // the magnitude of code m (weight 8n + m) in nibble m
+    const uint32_t mlo = __byte_perm(LUT0, LUT1, sel);        // q of weights 8n .. 8n + 3
+    const uint32_t mhi = __byte_perm(LUT0, LUT1, sel >> 16);  // q of weights 8n + 4 .. 8n + 7
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t pi = 0x7044u | ((uint32_t)i << 8);
+      const float2 wv = unpack2(ffma2(pack2(__byte_perm(mlo, 0x3F000000u, pi), __byte_perm(mhi, 0x3F000000u, pi)), a2, c2));
+      // sign bits of weights 8n + i (bit 4i + 3) and 8n + i + 4 (bit 4i + 19) to bits 15 and 31
+      o[4 * n + i] = tc::pack_bf16x2(wv.x, wv.y) ^ ((w[n] << (12 - 4 * i)) & 0x80008000u);
     }
   }
 }
@@ -463,8 +496,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
     auto deq = [&](int u, int hh) {
       if constexpr (ROWCOPY) {
         const uint8_t* blk = my_row + (size_t)(u % KB) * BYTES;
-        dequant_q6k_group(blk, 4 * hh + 2 * sp, wa);
-        dequant_q6k_group(blk, 4 * hh + 2 * sp + 1, wb);
+        if constexpr (QT == QMOE_Q6K) {
+          dequant_q6k_group(blk, 4 * hh + 2 * sp, wa);
+          dequant_q6k_group(blk, 4 * hh + 2 * sp + 1, wb);
+        } else {
+          dequant_mxfp4_group(blk, 4 * hh + 2 * sp, wa);
+          dequant_mxfp4_group(blk, 4 * hh + 2 * sp + 1, wb);
+        }
         return;
       }
       const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
@@ -948,7 +986,7 @@ cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
   const uint32_t bytes = (uint32_t)qtype_bytes(p.qt);
   const uint64_t rb = (uint64_t)(p.F / QK) * bytes;
   TcMaps m;
-  if (p.qt == QMOE_Q6K) {
+  if (p.qt == QMOE_Q6K || p.qt == QMOE_MXFP4) {
     // whole rows by bulk copies (no weight tensor maps)
     if (p.F / QK > TC_ROWCOPY_KB || !encode_tokens(&m.tok, p.hin, (uint64_t)p.tok_rows, (uint64_t)p.F))
       return cudaErrorInvalidValue;
@@ -956,7 +994,8 @@ cudaError_t launch_down_tc(const GroupedTcArgs& p, cudaStream_t st) {
     memset(&m.s, 0, sizeof(m.s));
     memset(&m.w2, 0, sizeof(m.w2));
     memset(&m.s2, 0, sizeof(m.s2));
-    return tc_launch_t<false, QMOE_Q6K>(a, m, p.max_chunks * (p.H / 256), p.nmax, st);
+    return p.qt == QMOE_Q6K ? tc_launch_t<false, QMOE_Q6K>(a, m, p.max_chunks * (p.H / 256), p.nmax, st)
+                            : tc_launch_t<false, QMOE_MXFP4>(a, m, p.max_chunks * (p.H / 256), p.nmax, st);
   }
   if (!encode_rows(&m.w, p.W, (uint64_t)p.E * p.H, rb, bytes, 256) ||
       !encode_rows(&m.s, p.S, (uint64_t)p.H, rb, bytes, 256) ||

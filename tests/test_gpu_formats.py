@@ -7,9 +7,9 @@ tensors (typically the down projections) in Q6_K. "Distributed CPU: Zip Fusion
 Beyond Tensor Parallelism", "Decode vs Prefill: Same Weights, Different
 Bottlenecks": the model class it targets carries MXFP4-class weights. Layers
 with either format run on the grouped GEMV kernels (fp32 accumulation, the
-fp32 tolerance), except Q6_K down projections next to Q4_K gate/up above the
-tensor-core threshold: those take the tcgen05 kernels (whole weight rows by
-bulk copies, bf16 operands, the tensor-core tolerance).
+fp32 tolerance), except Q6_K or MXFP4 down projections next to Q4_K gate/up
+above the tensor-core threshold: those take the tcgen05 kernels (whole
+weight rows by bulk copies, bf16 operands, the tensor-core tolerance).
 """
 
 import numpy as np
@@ -48,7 +48,7 @@ def layer(gate, down, seed=3):
 
 
 def expected_path(arr, T):
-    tc = (arr["Wg"].shape[-1] == 144 and arr["Wd"].shape[-1] == 210 and T > qb.get_gemm_threshold())
+    tc = (arr["Wg"].shape[-1] == 144 and arr["Wd"].shape[-1] in (210, 136) and T > qb.get_gemm_threshold())
     return "gemm_tc" if tc else "gemv"
 
 
@@ -139,7 +139,8 @@ def test_q6k_field_extremes(oracle):
 
 def test_mxfp4_every_code_and_scale(oracle):
     """MXFP4 down blocks cycling through all 16 E2M1 codes (both zeros and the
-    negative half) with E8M0 scales 2^-12 .. 2^-1."""
+    negative half) with E8M0 scales 2^-12 .. 2^-1; GEMV kernels (T = 3) and
+    tensor-core kernels (T = 37, sampled rows)."""
     arr, _ = layer("q4k", "mxfp4")
     arr = dict(arr)
     Wd = arr["Wd"].copy()
@@ -149,3 +150,10 @@ def test_mxfp4_every_code_and_scale(oracle):
     arr["Wd"] = Wd
     lay = qb.MoeLayer.from_arrays(arr, K)
     run(oracle, arr, lay, 3, 22)
+    run(oracle, arr, lay, 37, 24, rows=np.array([0, 18, 36]))
+
+
+def test_mxfp4_down_tensor_cores_large(oracle):
+    """MXFP4 down weights on the tensor-core path at T = 4096, sampled rows."""
+    arr, lay = layer("q4k", "mxfp4")
+    run(oracle, arr, lay, 4096, 33, rows=np.array([0, 1, 2047, 4095]))
