@@ -388,6 +388,50 @@ __device__ void decode_route(const DecodeArgs& a, RouteState& S, float* lg, int 
     if (k <= 8) warp_topk<8>(lg + warp * E, E, k, lane, S.sel_e + warp * k, S.sel_l + warp * k);
     else warp_topk<16>(lg + warp * E, E, k, lane, S.sel_e + warp * k, S.sel_l + warp * k);
   }
+  if (T == 1) {
+    // one row: the k selected experts are the routed slots; warp 0 takes the
+    // weights (the same arithmetic as below), the slot of each expert (its
+    // rank by index among the selected) and the pair indices
+    if (warp == 0) {
+      __syncwarp();
+      const bool sel = lane < k;
+      const int e = sel ? S.sel_e[lane] : 0x7fffffff;
+      float w = 0.f;
+      if (lane == 0) {
+        const float l0 = S.sel_l[0];
+        float den = 0.f;
+        for (int r = 0; r < k; ++r) den += expf(S.sel_l[r] - l0);
+        w = den;
+      }
+      const float den = __shfl_sync(0xffffffffu, w, 0);
+      int rank = 0;
+      for (int j = 0; j < k; ++j) rank += __shfl_sync(0xffffffffu, e, j) < e;
+      const int hs = a.has_shared;
+      if (sel) {
+        const float ws = expf(S.sel_l[lane] - S.sel_l[0]) / den;
+        S.wts[lane] = ws;
+        if (write_ids) {
+          a.ids[lane] = e;
+          a.w[lane] = ws;
+        }
+        S.slot_e[hs + rank] = e;
+        S.pair_of[hs + rank][0] = lane;
+#pragma unroll
+        for (int t = 1; t < DX_MAXT; ++t) S.pair_of[hs + rank][t] = -1;
+      }
+      if (lane == 0) {
+        if (hs) {
+          S.slot_e[0] = E;
+          S.pair_of[0][0] = k;  // the shared expert's pair of row 0: T k + 0
+#pragma unroll
+          for (int t = 1; t < DX_MAXT; ++t) S.pair_of[0][t] = -1;
+        }
+        S.n_slots = k + hs;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   __syncthreads();
   int* mark = reinterpret_cast<int*>(lg + T * E);  // [E], after the logits
   for (int e = tid; e < E; e += nthreads) mark[e] = 0;
