@@ -583,7 +583,8 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
   const bool use_tc = tc_formats && T > g_gemm_threshold.load();
   // on the tensor-core path at large T the permutation scan also builds the
   // token-chunk list
-  const bool chunks_in_scan = use_tc && !small;
+  // (the permutation kernels also build the tensor-core path's token-chunk list)
+  const bool chunks_in_scan = use_tc;
   int2* tc_chunks = reinterpret_cast<int2*>(base + L.chunks);
   int32_t* tc_n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
   const int tc_cap = tc_chunk_cap(T, k, E);
@@ -598,7 +599,8 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
           cudaError_t e2 = launch_topk(part, L.nsplit, T, E, k, ws_ids, ws_w, st);
           if (e2 != cudaSuccess) return e2;
           return launch_route_small(nullptr, 0, ws_ids, T, E, k, has_shared, ws_ids, ws_w, offsets, perm,
-                                    active, n_active, status, st);
+                                    active, n_active, status, st, tc_cap, chunks_in_scan ? tc_chunks : nullptr,
+                                    tc_n_chunks);
         });
       } else {
         e = staged(QMOE_STAGE_ROUTE, 4, st, [&] {
@@ -614,7 +616,8 @@ int qmoe_moe_forward(const qmoe_moe_desc* d, const float* X, const float* R, con
     if (small)
       e = staged(QMOE_STAGE_ROUTE, 1, st, [&] {
         return launch_route_small(nullptr, 0, ids, T, E, k, has_shared, ws_ids, ws_w, offsets,
-                                  perm, active, n_active, status, st);
+                                  perm, active, n_active, status, st, tc_cap,
+                                  chunks_in_scan ? tc_chunks : nullptr, tc_n_chunks);
       });
     else
       e = staged(QMOE_STAGE_ROUTE, 3, st, [&] {

@@ -29,10 +29,13 @@ cudaError_t launch_router_tc(const float* X, const float* Wr, float* part, int T
 cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k, int32_t* ids, float* w,
                         cudaStream_t st);
 size_t route_small_smem(int T, int E, int k);
+// with ``chunks`` set, also the tensor-core path's token-chunk list (cap 64
+// or 128 rows)
 cudaError_t launch_route_small(const float* part, int nsplit, const int32_t* ids_in, int T, int E,
                                int k, int has_shared, int32_t* ids, float* w, int32_t* offsets,
                                int32_t* perm, int32_t* active, int32_t* n_active, int* status,
-                               cudaStream_t st);
+                               cudaStream_t st, int cap = 0, int2* chunks = nullptr,
+                               int32_t* n_tok_chunks = nullptr);
 int perm_chunks(int P);
 // with ``chunks`` set, also the tensor-core path's token-chunk list (cap 64
 // or 128 rows), as launch_build_chunks would build it

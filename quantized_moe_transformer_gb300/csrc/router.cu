@@ -339,8 +339,9 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
 
 // ---------------------------------------------------------------------------
 // Permutation for small T (one CTA): optional top-k, histogram, exclusive scan,
-// stable scatter in (t, slot) order, active-expert list. Expert index E is the
-// shared expert, which takes every row (pairs T*k + t).
+// stable scatter in (t, slot) order, active-expert list, and (with ``chunks``)
+// the tensor-core path's token-chunk list. Expert index E is the shared
+// expert, which takes every row (pairs T*k + t).
 // Workspace outputs: offsets[E+2], perm[T*k+T], active[E+1], n_active[1].
 // ---------------------------------------------------------------------------
 template <int EPL>
@@ -348,8 +349,10 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     const float* __restrict__ part, int nsplit, const int32_t* __restrict__ ids_in, int T, int E,
     int k, int has_shared, int32_t* __restrict__ ids, float* __restrict__ w,
     int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ active,
-    int32_t* __restrict__ n_active, int* status) {
+    int32_t* __restrict__ n_active, int* status, int cap, int2* __restrict__ chunks,
+    int32_t* __restrict__ n_tok_chunks) {
   extern __shared__ int32_t sm[];
+  __shared__ int32_t cstart[1025 + 32];
   int32_t* cnt = sm;                 // [E+1]
   int32_t* cur = sm + (E + 1);       // [E+1] running cursor / scan scratch
   int32_t* sid = sm + 2 * (E + 1);   // [T*k] ids of this batch
@@ -376,35 +379,55 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
   // exclusive scan over E+1 counts, and the compacted active list (serial in
   // one warp: E+1 <= 1025 entries, 33 steps of a warp scan)
   if (warp == 0) {
-    int run = 0, arun = 0;
+    int run = 0, arun = 0, crun = 0;
     for (int base = 0; base <= E; base += 32) {
       int e = base + lane;
       int c = (e <= E) ? cnt[e] : 0;
       int a = (c > 0) ? 1 : 0;
-      int incl = c, aincl = a;
+      int nc = chunks ? (c + cap - 1) / cap : 0;
+      int incl = c, aincl = a, cincl = nc;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         int o = __shfl_up_sync(0xffffffffu, incl, off);
         int oa = __shfl_up_sync(0xffffffffu, aincl, off);
+        int oc = __shfl_up_sync(0xffffffffu, cincl, off);
         if (lane >= off) {
           incl += o;
           aincl += oa;
+          cincl += oc;
         }
       }
       if (e <= E) {
         offsets[e] = run + incl - c;
         cur[e] = run + incl - c;
+        cstart[e] = crun + cincl - nc;
         if (a) active[arun + aincl - 1] = e;
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
       arun += __shfl_sync(0xffffffffu, aincl, 31);
+      crun += __shfl_sync(0xffffffffu, cincl, 31);
     }
     if (lane == 0) {
       offsets[E + 1] = run;
       n_active[0] = arun;
+      if (chunks) n_tok_chunks[0] = crun;
     }
   }
   __syncthreads();
+  if (chunks) {
+    // each expert with rows (the shared expert last) cut into ceil(rows / cap)
+    // chunks of near-equal size (first row below 2^24, packed with the count)
+    for (int e = tid; e <= E; e += blockDim.x) {
+      const int Me = cnt[e];
+      if (Me <= 0) continue;
+      const int nc = (Me + cap - 1) / cap;
+      for (int i = 0; i < nc; ++i) {
+        const int c0 = (int)((long long)i * Me / nc);
+        const int c1 = (int)((long long)(i + 1) * Me / nc);
+        chunks[cstart[e] + i] = make_int2(e, c0 | ((c1 - c0 - 1) << 24));
+      }
+    }
+  }
   // stable scatter: one warp walks the pairs in order, 32 at a time
   if (warp == 0) {
     for (int base = 0; base < P; base += 32) {
@@ -662,20 +685,23 @@ template <int EPL>
 static cudaError_t route_small_dispatch(const float* part, int nsplit, const int32_t* ids_in, int T,
                                         int E, int k, int has_shared, int32_t* ids, float* w,
                                         int32_t* offsets, int32_t* perm, int32_t* active,
-                                        int32_t* n_active, int* status, cudaStream_t st) {
+                                        int32_t* n_active, int* status, cudaStream_t st, int cap,
+                                        int2* chunks, int32_t* n_tok_chunks) {
   size_t smem = route_small_smem(T, E, k);
   route_small_kernel<EPL><<<1, 1024, smem, st>>>(part, nsplit, ids_in, T, E, k, has_shared, ids, w,
-                                                 offsets, perm, active, n_active, status);
+                                                 offsets, perm, active, n_active, status, cap, chunks,
+                                                 n_tok_chunks);
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_small(const float* part, int nsplit, const int32_t* ids_in, int T, int E,
                                int k, int has_shared, int32_t* ids, float* w, int32_t* offsets,
                                int32_t* perm, int32_t* active, int32_t* n_active, int* status,
-                               cudaStream_t st) {
+                               cudaStream_t st, int cap, int2* chunks, int32_t* n_tok_chunks) {
+  if (E > 1024 || (chunks != nullptr && cap != 64 && cap != 128)) return cudaErrorInvalidValue;
 #define QMOE_RS(EPL) \
   route_small_dispatch<EPL>(part, nsplit, ids_in, T, E, k, has_shared, ids, w, offsets, perm, \
-                            active, n_active, status, st)
+                            active, n_active, status, st, cap, chunks, n_tok_chunks)
   if (E <= 32) return QMOE_RS(1);
   if (E <= 64) return QMOE_RS(2);
   if (E <= 128) return QMOE_RS(4);
