@@ -236,7 +236,7 @@ int qmoe_moe_forward_noalloc(const qmoe_moe_desc *d, const float *X, const float
 /*
  * Test-only fault injection (the pages have no counterpart: this exists so
  * that the library's bounded device waits can be exercised without faulting
- * a GPU). While a site is set, every qmoe_moe_forward that reaches that site
+ * a GPU). While a site is set, every call that reaches that site
  * withholds one copy or arrival, so that one wait can never complete; the
  * waiting CTA gives up after ``wait_us`` microseconds (0: the normal limit of
  * 2 s), records QMOE_ERR_TIMEOUT in the status word and returns with nothing
@@ -246,11 +246,14 @@ int qmoe_moe_forward_noalloc(const qmoe_moe_desc *d, const float *X, const float
  *                          weights of its last down unit;
  *   QMOE_FAULT_TC_ARRIVE   tensor-core path, gate/up kernel: the first CTA's
  *                          producers never mark the last stage of their last
- *                          work item stored.
+ *                          work item stored;
+ *   QMOE_FAULT_ATTN_FINAL  block prefill attention (T > 16): the first CTA's
+ *                          P V issuer never marks its output final, so its
+ *                          softmax warps' last wait runs out.
  * Returns QMOE_ERR_ARG for an unknown site or a negative wait. Not for use
  * outside tests; set QMOE_FAULT_NONE afterwards.
  */
-enum { QMOE_FAULT_NONE = 0, QMOE_FAULT_DECODE_COPY = 1, QMOE_FAULT_TC_ARRIVE = 2 };
+enum { QMOE_FAULT_NONE = 0, QMOE_FAULT_DECODE_COPY = 1, QMOE_FAULT_TC_ARRIVE = 2, QMOE_FAULT_ATTN_FINAL = 3 };
 int qmoe_test_inject(int site, int wait_us);
 
 /* Number of kernels this library has enqueued since it was loaded (a CUDA

@@ -187,11 +187,11 @@ def moe_forward(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = None,
     return out
 
 
-FAULT_SITES = {"none": 0, "decode_copy": 1, "tc_arrive": 2}
+FAULT_SITES = {"none": 0, "decode_copy": 1, "tc_arrive": 2, "attn_final": 3}
 
 
 def test_inject(site: str, wait_us: int = 0):
-    """Test-only: make the next forwards withhold one copy or arrival at
+    """Test-only: make the next calls withhold one copy, arrival or signal at
     ``site`` so that one bounded device wait runs out after ``wait_us``."""
     _check(lib().qmoe_test_inject(FAULT_SITES[site], int(wait_us)))
 

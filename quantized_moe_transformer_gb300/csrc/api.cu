@@ -333,7 +333,8 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
     g_launches.fetch_add(1);
   }
   if (e == cudaSuccess) {
-    e = launch_attention(q, kcb, vcb, part, o, T, pos0, nh, nkv, hd, L.chunked, status, wait_limit_ns(), st);
+    e = launch_attention(q, kcb, vcb, part, o, T, pos0, nh, nkv, hd, L.chunked, status, wait_limit_ns(),
+                         g_fault_site.load() == QMOE_FAULT_ATTN_FINAL ? 1 : 0, st);
     g_launches.fetch_add(L.chunked ? 2 : 1);
   }
   float* proj_out = R ? rr : out;  // rr is free once Q, K, V exist
@@ -755,7 +756,7 @@ int qmoe_moe_forward_host(const qmoe_moe_desc* d, const float* X_host, const flo
 long long qmoe_launch_count(void) { return g_launches.load(); }
 
 int qmoe_test_inject(int site, int wait_us) {
-  if (site < 0 || site > QMOE_FAULT_TC_ARRIVE || wait_us < 0) return QMOE_ERR_ARG;
+  if (site < 0 || site > QMOE_FAULT_ATTN_FINAL || wait_us < 0) return QMOE_ERR_ARG;
   g_fault_wait_us.store(wait_us);
   g_fault_site.store(site);
   return QMOE_OK;

@@ -122,8 +122,8 @@ __device__ __forceinline__ uint64_t at_mn_sw128_desc(uint32_t smem_addr, uint32_
 // pos0 + t and sees keys 0 .. pos0 + t.
 __global__ void __launch_bounds__(AT_THREADS, 1)
     attn_prefill_tc_kernel(const float* __restrict__ q, float* __restrict__ o, int T, int pos0, int nh, int nkv,
-                           int* status, unsigned long long wait_ns, const __grid_constant__ CUtensorMap kmap,
-                           const __grid_constant__ CUtensorMap vmap) {
+                           int* status, unsigned long long wait_ns, int fault,
+                           const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ uint8_t at_smem_raw[];
   const uint32_t s0 = tc::smem_u32(at_smem_raw);
   uint8_t* smem = at_smem_raw + (((s0 + 1023u) & ~1023u) - s0);
@@ -417,7 +417,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         tc::mma_commit(&p_free[b]);
         tc::mma_commit(&v_empty[b]);
       }
-      if (ok) tc::mma_commit(o_final);
+      // test-only fault: the first CTA never marks O final, so the softmax
+      // warps' wait for it runs out (every MMA of the CTA has been issued and
+      // is drained below)
+      if (ok && !(fault == 1 && blockIdx.x == 0 && blockIdx.y == 0)) tc::mma_commit(o_final);
       tc::mma_commit(&drain[1]);
       volatile int never = 0;
       tc::mbar_wait(&drain[1], 0, &never, lim);
@@ -468,7 +471,7 @@ static bool at_encode_cache(CUtensorMap* m, const void* base, int nkv, int rows)
 
 cudaError_t launch_attention_prefill_tc(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
                                         int T, int pos0, int nh, int nkv, int* status, unsigned long long wait_ns,
-                                        cudaStream_t st) {
+                                        int fault, cudaStream_t st) {
   if (T < 1 || nkv < 1 || nh % nkv != 0) return cudaErrorInvalidValue;
   CUtensorMap km, vm;
   if (!at_encode_cache(&km, kc, nkv, pos0 + T) || !at_encode_cache(&vm, vc, nkv, pos0 + T))
@@ -476,7 +479,7 @@ cudaError_t launch_attention_prefill_tc(const float* q, const __nv_bfloat16* kc,
   cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(attn_prefill_tc_kernel), AT_SMEM);
   if (e != cudaSuccess) return e;
   attn_prefill_tc_kernel<<<dim3((T + AT_BQ - 1) / AT_BQ, nh), AT_THREADS, AT_SMEM, st>>>(
-      q, o, T, pos0, nh, nkv, status, wait_ns ? wait_ns : tc::kWaitLimitNs, km, vm);
+      q, o, T, pos0, nh, nkv, status, wait_ns ? wait_ns : tc::kWaitLimitNs, fault, km, vm);
   return cudaGetLastError();
 }
 

@@ -106,15 +106,16 @@ cudaError_t launch_rope_cache(float* q, const float* k, const float* v, __nv_bfl
 int attn_nchunks(int T, int pos0);
 cudaError_t launch_attention(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* part, float* o,
                              int T, int pos0, int nh, int nkv, int hd, bool chunked, int* status,
-                             unsigned long long wait_ns, cudaStream_t st);
+                             unsigned long long wait_ns, int fault, cudaStream_t st);
 cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaStream_t st);
 
 // attn_prefill.cu: causal attention for many query rows (head_dim 128) on the
 // tcgen05 tensor cores (S and O in tensor memory); bounded waits record
 // QMOE_ERR_TIMEOUT in *status.
+// ``fault`` (test-only): 1 = CTA 0's P V issuer never marks its output final.
 cudaError_t launch_attention_prefill_tc(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
                                         int T, int pos0, int nh, int nkv, int* status, unsigned long long wait_ns,
-                                        cudaStream_t st);
+                                        int fault, cudaStream_t st);
 
 // moe_decode.cu: the decode path for T <= 4 (router kernel + one persistent
 // expert kernel, programmatic dependent launch).

@@ -4,10 +4,11 @@
 bounded time and reports the failure instead of hanging. Here every device
 wait of the library (a copy's mbarrier, a counter another CTA advances) gives
 up after a time limit and records QMOE_ERR_TIMEOUT. The test-only entry point
-qmoe_test_inject makes the next calls withhold one copy (decode path) or one
-producer arrival (tensor-core gate/up kernel) with a short limit; the call
-must return, report the time-out through qmoe_query_status, and the next
-normal call must be clean and correct.
+qmoe_test_inject makes the next calls withhold one copy (decode path), one
+producer arrival (tensor-core gate/up kernel) or the prefill attention's
+final-output signal with a short limit; the call must return, report the
+time-out through qmoe_query_status, and the next normal call must be clean
+and correct.
 """
 
 import time
@@ -72,6 +73,41 @@ def test_tensor_core_arrival_withheld_times_out_then_recovers(layer, T):
     assert st == -7, st
     assert dt < 5.0
     again = qb.moe_forward(layer, X, X)
+    torch.cuda.synchronize()
+    assert qb.query_status() == 0
+    assert torch.equal(again, ref)
+
+
+@pytest.mark.parametrize("T", [17, 300])
+def test_attention_final_withheld_times_out_then_recovers(T):
+    """The first attention CTA's P V issuer never marks its output final: its
+    softmax warps give up, every MMA is drained, TMEM is freed, the call
+    reports the time-out, and the next call gives the same bits as before."""
+    from quantized_moe_transformer_gb300 import build
+    build.build()
+    arr = inputs.block(3, ctx=1024)
+    blk = qb.Block.from_arrays(arr, 8)
+    X = torch.from_numpy(inputs.hidden(80 + T, T, 2048)).cuda()
+
+    def run():
+        kd = qb.cache_from_bits(arr["k_cache"])
+        vd = qb.cache_from_bits(arr["v_cache"])
+        return qb.attn_forward(blk, X, None, kd, vd, 40)
+
+    ref = run()
+    torch.cuda.synchronize()
+    assert qb.query_status() == 0
+    qb.test_inject("attn_final", 20000)
+    try:
+        t0 = time.perf_counter()
+        run()
+        st = qb.query_status()
+        dt = time.perf_counter() - t0
+    finally:
+        qb.test_inject("none")
+    assert st == -7, st
+    assert dt < 5.0
+    again = run()
     torch.cuda.synchronize()
     assert qb.query_status() == 0
     assert torch.equal(again, ref)
