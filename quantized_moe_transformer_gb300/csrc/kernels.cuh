@@ -29,16 +29,16 @@ cudaError_t launch_router_tc(const float* X, const float* Wr, float* part, int T
 cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k, int32_t* ids, float* w,
                         cudaStream_t st);
 size_t route_small_smem(int T, int E, int k);
-// with ``chunks`` set, also the tensor-core path's token-chunk list (cap 64
-// or 128 rows)
+// with ``chunks`` set, also the tensor-core path's token-chunk list (cap 64,
+// 128 or 192 rows)
 cudaError_t launch_route_small(const float* part, int nsplit, const int32_t* ids_in, int T, int E,
                                int k, int has_shared, int32_t* ids, float* w, int32_t* offsets,
                                int32_t* perm, int32_t* active, int32_t* n_active, int* status,
                                cudaStream_t st, int cap = 0, int2* chunks = nullptr,
                                int32_t* n_tok_chunks = nullptr);
 int perm_chunks(int P);
-// with ``chunks`` set, also the tensor-core path's token-chunk list (cap 64
-// or 128 rows), as launch_build_chunks would build it
+// with ``chunks`` set, also the tensor-core path's token-chunk list (cap 64,
+// 128 or 192 rows), as launch_build_chunks would build it
 cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_shared,
                               int32_t* chunk_cnt, int32_t* offsets, int32_t* perm,
                               int32_t* active, int32_t* n_active, int* status, cudaStream_t st,
@@ -77,7 +77,7 @@ struct GroupedTcArgs {
   __nv_bfloat16* yout;
   float* yout_f32;  // down pass: write fp32 instead of bf16 when not null
   int tok_rows;     // rows of the token matrix (xb for gate/up, hin for down)
-  int nmax;         // chunk cap the chunk list was built with (64 or 128)
+  int nmax;         // chunk cap the chunk list was built with (64, 128 or 192)
   int T, k, E, H, F;
   int* status;
   unsigned long long wait_ns;  // bound on a device wait (0: the default 2 s)

@@ -4,7 +4,7 @@
 // One Matrix-Work Scheduler": with many rows per weight region each packed
 // weight is reused across the rows and the region becomes GEMM-bound. Here the
 // rows routed to one expert (contiguous in permutation order) are cut into
-// chunks of at most 128 tokens; per work item one expert's packed Q4_K/Q5_K
+// chunks of at most 64, 128 or 192 tokens; per work item one expert's packed
 // rows are dequantised to bf16 and multiplied with the chunk's activations on
 // the tensor cores, fp32 accumulation in tensor memory ("What PR #382 Now
 // Splits" in "CKE Zip: From Splitting Tokens To Splitting Qwen3.5 Weights":
@@ -19,7 +19,7 @@
 //
 // A work item is (token chunk, weight block). A weight block is two 128-row
 // matrices A0, A1 with accumulators D0, D1 (TMEM columns [0, NMAX) and
-// [NMAX, 2 NMAX), NMAX = the chunk cap, 64 or 128):
+// [NMAX, 2 NMAX), NMAX = the chunk cap, 64, 128 or 192):
 // gate rows and the matching up rows (gate/up pass: SwiGLU pairs lane f of D0
 // with lane f of D1 in one thread), or two consecutive 128-row blocks of the
 // down matrix. One persistent CTA per SM walks the items; warp roles (896
@@ -30,18 +30,18 @@
 //               the y store (down), leaving through a small shared-memory
 //               transpose in 16-byte stores;
 //   warps 4-19  producers: warp 4 + pw covers lane quarter pw % 4 of A0
-//               (pw / 4 even) or A1, and sub-blocks 2 (pw / 8), 2 (pw / 8) + 1
-//               of each k-tile's four (k-tile = K 128, half a super-block); a
-//               thread dequantises 64 weights of its row per k-tile in bf16x2
-//               arithmetic from the packed super-block ring and stores them
-//               into the k-tile's A stage in TMEM (columns 2 NMAX + 128 s ..);
+//               (pw / 4 even) or A1, and half of each k-tile's sub-blocks
+//               (k-tile = K 128, half a super-block, or K 64 at NMAX 192); a
+//               thread dequantises 64 (or 32) weights of its row per k-tile
+//               from the packed super-block ring and stores them into the
+//               k-tile's A stage in TMEM (columns 2 NMAX + BK s ..);
 //   warps 20,23 issue the MMAs of D0 and D1 (one lane each); warp 20 also
 //               allocates the 512 TMEM columns;
 //   warp 21     copies each k-tile's token rows into the stage's
 //               shared-memory tile (one lane, 2-D tensor copies);
 //   warp 22     copies the packed weight rows into the super-block ring (one
 //               lane, 2-D tensor copies).
-// Two A stages in TMEM (three when NMAX is 64), three or five token stages
+// Two A stages in TMEM (three when NMAX is 64), three to five token stages
 // and two or three packed super-block stages in shared memory, each ring with
 // its own full/empty barriers, decouple the roles.
 // Every wait is bounded: on time-out the CTA records QMOE_ERR_TIMEOUT, drains
@@ -58,7 +58,6 @@
 
 namespace qmoe {
 
-constexpr int TC_BK = 128;      // K per stage: half a super-block
 constexpr int TC_PRODUCER_WARPS = 16;
 constexpr int TC_MMA_WARP = 4 + TC_PRODUCER_WARPS;  // 20
 constexpr int TC_LOAD_WARP = TC_MMA_WARP + 1;       // 21: token tiles
@@ -68,8 +67,11 @@ constexpr int TC_EPI_WARP2 = TC_MMA_WARP2 + 1;      // 24-27: second epilogue wa
 constexpr int TC_EPI_WARPS = 8;
 constexpr int TC_THREADS = 32 * (TC_EPI_WARP2 + 4); // 896
 constexpr int TC_EPI_BYTES = 2048;            // per epilogue warp: 16 tokens x 32 values x 4 B
-constexpr uint32_t TC_A_STAGE_COLS = TC_BK;  // two matrices x TC_BK / 2 columns
-constexpr int TC_N_MIN = 64;                  // the smaller chunk cap (bounds the chunk count)
+constexpr int TC_N_MIN = 64;                  // the smallest chunk cap (bounds the chunk count)
+// experts' mean rows (T k / E) above which the chunk cap is 192
+#ifndef TC_CAP192_MIN_ROWS
+#define TC_CAP192_MIN_ROWS 120
+#endif
 
 // Packed weights are staged per super-block: RS ring stages of 256 rows (A0
 // rows, then A1 rows), each filled by one or two 2-D tensor copies.
@@ -77,9 +79,12 @@ constexpr int TC_N_MIN = 64;                  // the smaller chunk cap (bounds t
 // so that their loads run ahead of the MMAs instead of inside the A ring's
 // round trip.
 // NMAX is the chunk cap (largest MMA N): the two accumulators take 2 NMAX of
-// the 512 TMEM columns and the A stages (128 columns each: K = 128 for both
-// matrices) the rest, so a cap of 64 rows buys 3 A stages instead of 2; it is
-// chosen when experts get few rows (T * k / E <= 32).
+// the 512 TMEM columns and the A stages (BK columns each: K = BK for both
+// matrices) the rest. A cap of 64 rows buys 3 A stages of K 128 (chosen when
+// experts get few rows, T * k / E <= 32); a cap of 192 leaves 128 columns,
+// two A stages of K 64 (chosen when experts get many rows: an expert's rows
+// are then one chunk, its weights dequantised once, where a cap of 128 cuts
+// about half of them in two).
 // Q6_K and MXFP4 weights (down pass only): a 210- or 136-byte super-block is
 // only 2- or 8-byte aligned, so neither a tensor-map box nor a bulk copy can
 // take one super-block column. An item's 256 rows of the down matrix are
@@ -93,13 +98,17 @@ constexpr int TC_ROWCOPY_KB = 2;  // super-blocks along K that the raw stage hol
 template <int QT, int NMAX>
 struct TcCfg {
   static constexpr int BYTES = qtype_size(QT);
-  static constexpr int S = (512 - 2 * NMAX) / (int)TC_A_STAGE_COLS;  // A stages in TMEM
+  static constexpr int BK = NMAX > 128 ? 64 : 128;                  // K per stage (k-tile)
+  static constexpr uint32_t A_STAGE_COLS = BK;                      // two matrices x BK / 2 columns
+  static constexpr int S = (512 - 2 * NMAX) / BK;                   // A stages in TMEM
   static constexpr uint32_t D1_COL = NMAX;                          // D0 at column 0
-  static constexpr uint32_t A_COL = 2 * NMAX;                       // A stage s at A_COL + 128 s
+  static constexpr uint32_t A_COL = 2 * NMAX;                       // A stage s at A_COL + BK s
   static constexpr int B_HALF = NMAX * 128;                         // K 64 x NMAX rows, one swizzle atom row each
-  static constexpr int B_BYTES = 2 * B_HALF;                        // token tile per stage: two K halves
-  static constexpr int RS = tc_rowcopy<QT>() ? 1 : ((QT == QMOE_Q5K && NMAX == 128) ? 2 : 3);
-  static constexpr int TS = NMAX == 64 ? (QT == QMOE_Q5K ? 4 : 5) : 3;
+  static constexpr int B_BYTES = (BK / 64) * B_HALF;                // token tile per stage: one or two K halves
+  static constexpr int RS = tc_rowcopy<QT>() ? 1 : ((QT == QMOE_Q5K && NMAX >= 128) ? 2 : 3);
+  static constexpr int TS = NMAX == 64 ? (QT == QMOE_Q5K ? 4 : 5)
+                          : NMAX == 128 ? 3
+                                        : ((QT == QMOE_Q4K || QT == QMOE_Q6K) ? 4 : 5);
   static constexpr int RAW_STAGE = tc_rowcopy<QT>() ? 256 * TC_ROWCOPY_KB * BYTES : 256 * BYTES;
   static constexpr int SMEM = TS * B_BYTES + RS * RAW_STAGE + TC_EPI_WARPS * TC_EPI_BYTES + 1024 /*align*/ +
                               512 /*barriers*/;
@@ -139,7 +148,7 @@ struct Chunk {
 };
 __device__ __forceinline__ Chunk chunk_at(const int2* chunks, int i) {
   const int2 c = chunks[i];
-  return {c.x, c.y & 0xFFFFFF, (c.y >> 24) + 1};
+  return {c.x, c.y & 0xFFFFFF, (int)((uint32_t)c.y >> 24) + 1};
 }
 
 // K order inside every group of 8 consecutive K values of the tensor-core
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   const uint32_t s0 = tc::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((s0 + 1023u) & ~1023u) - s0);
   using Cfg = TcCfg<QT, NMAX>;
-  constexpr int S = Cfg::S, RS = Cfg::RS, TS = Cfg::TS, BYTES = Cfg::BYTES;
+  constexpr int S = Cfg::S, RS = Cfg::RS, TS = Cfg::TS, BYTES = Cfg::BYTES, BK = Cfg::BK;
   constexpr int TC_B_BYTES = Cfg::B_BYTES, TC_B_HALF = Cfg::B_HALF;
   constexpr uint32_t TC_D1_COL = Cfg::D1_COL, TC_A_COL = Cfg::A_COL;
   uint8_t* sB = smem;                                         // [TS][NMAX][128 B] token tiles
@@ -343,8 +352,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = g.wait_ns;
   const int NB = GATEUP ? g.F / 128 : g.H / 256;      // weight blocks per chunk
-  const int KT = GATEUP ? g.H / TC_BK : g.F / TC_BK;  // k-tiles
-  const int KB = KT / 2;                              // super-blocks along K
+  const int KT = GATEUP ? g.H / BK : g.F / BK;        // k-tiles
+  const int KB = KT / (256 / BK);                     // super-blocks along K
   const int total = g.n_chunks[0] * NB;
   const int n_mine = (int)blockIdx.x < total ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
 
@@ -455,8 +464,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
   } else if (warp < 4 + TC_PRODUCER_WARPS) {
     // ------------------------------------------------------------ producers
     // Warp 4 + pw covers TMEM lane quarter pw % 4 of matrix (pw / 4) % 2 and
-    // sub-blocks 2 sp, 2 sp + 1 (sp = pw / 8) of each k-tile's four: thread =
-    // one weight row, 64 weights per k-tile. A k-tile is stored and its stage
+    // sub-blocks 2 sp, 2 sp + 1 (sp = pw / 8) of each k-tile's four (BK 128),
+    // or sub-block sp of its two (BK 64): thread = one weight row, 64 or 32
+    // weights per k-tile. A k-tile is stored and its stage
     // released before the next one is dequantised, so that the stage round
     // trip (MMA commit -> producers -> MMA) stays short.
     // (sp is a compile-time constant in each of the two copies of the body, so
@@ -467,8 +477,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       constexpr int sp = decltype(sp_c)::value;
       const int mat = (pw >> 2) & 1;
       const int r = 32 * (pw & 3) + lane;
+      constexpr int HPS = 256 / BK;  // k-tiles per super-block
+      constexpr int SUBS = BK / 64;  // sub-blocks per thread and k-tile
       const uint32_t ta0 =
-          tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * (TC_BK / 2) + sp * 32);
+          tmem + ((uint32_t)(32 * (pw & 3)) << 16) + TC_A_COL + (uint32_t)(mat * (BK / 2) + sp * (BK / 4));
       // (whole rows: the item's rows, every super-block, in one stage)
       constexpr bool ROWCOPY = tc_rowcopy<QT>();
       const size_t row_pitch = ROWCOPY ? (size_t)KB * BYTES : (size_t)BYTES;
@@ -492,33 +504,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         }
         return true;
     };
-    // sub-blocks 4 hh + 2 sp and + 1 of super-block u
-    auto deq = [&](int u, int hh) {
+    // sub-blocks j0 .. j0 + SUBS - 1 of super-block u, k-tile hh, into o0 (and o1)
+    auto deq = [&](int u, int hh, uint32_t* o0, uint32_t* o1) {
+      const int j0 = (BK / 32) * hh + SUBS * sp;
       if constexpr (ROWCOPY) {
         const uint8_t* blk = my_row + (size_t)(u % KB) * BYTES;
         if constexpr (QT == QMOE_Q6K) {
-          dequant_q6k_group(blk, 4 * hh + 2 * sp, wa);
-          dequant_q6k_group(blk, 4 * hh + 2 * sp + 1, wb);
+          dequant_q6k_group(blk, j0, o0);
+          if (SUBS == 2) dequant_q6k_group(blk, j0 + 1, o1);
         } else {
-          dequant_mxfp4_group(blk, 4 * hh + 2 * sp, wa);
-          dequant_mxfp4_group(blk, 4 * hh + 2 * sp + 1, wb);
+          dequant_mxfp4_group(blk, j0, o0);
+          if (SUBS == 2) dequant_mxfp4_group(blk, j0 + 1, o1);
         }
         return;
       }
       const uint4* rp = reinterpret_cast<const uint4*>(my_row + (size_t)(u % RS) * Cfg::RAW_STAGE);
-      const int j0 = 4 * hh + 2 * sp;
+      const uint4 hq = (j0 >> 2) ? hq1 : hq0;  // high bits of sub-blocks 4 (j0 / 4) .. + 3
       const uint4 q0 = rp[(QT == QMOE_Q5K ? 3 : 1) + j0];
-      const uint4 q1 = rp[(QT == QMOE_Q5K ? 3 : 1) + j0 + 1];
-      const uint4 hq = hh ? hq1 : hq0;  // high bits of sub-blocks 4 hh .. 4 hh + 3
-      dequant_sub<QT>(hdr, q0, QT == QMOE_Q5K ? pick_word(hq, 2 * sp) : 0u, j0, wa);
-      dequant_sub<QT>(hdr, q1, QT == QMOE_Q5K ? pick_word(hq, 2 * sp + 1) : 0u, j0 + 1, wb);
+      dequant_sub<QT>(hdr, q0, QT == QMOE_Q5K ? pick_word(hq, j0 & 3) : 0u, j0, o0);
+      if (SUBS == 2) {
+        const uint4 q1 = rp[(QT == QMOE_Q5K ? 3 : 1) + j0 + 1];
+        dequant_sub<QT>(hdr, q1, QT == QMOE_Q5K ? pick_word(hq, (j0 + 1) & 3) : 0u, j0 + 1, o1);
+      }
     };
     bool ok = NU > 0 && open_sb(0);
-    if (ok) deq(0, 0);
+    if (ok) deq(0, 0, wa, wb);
     int kg = 0;
     for (int u = 0; u < NU && ok; ++u) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      for (int hh = 0; hh < HPS; ++hh) {
         const int stage = kg % S;
         // warp-uniform outcome: the TMEM stores below are warp-collective
         if (!__all_sync(0xffffffffu, tc::mbar_wait(&empty[stage], ((kg / S) & 1) ^ 1, abort_flag, lim))) {
@@ -531,21 +545,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
         if (pw == 0 && lane == 0 && kg >= S) tc::mbar_arrive(&tok_empty[(kg - S) % TS]);
         // store and release the stage first: this is the path the MMAs wait on
         tc::tc_fence_after();
-        const uint32_t ta = ta0 + (uint32_t)stage * TC_A_STAGE_COLS;
+        const uint32_t ta = ta0 + (uint32_t)stage * Cfg::A_STAGE_COLS;
         tc::tmem_st16(ta, wa);
-        tc::tmem_st16(ta + 16, wb);
+        if (SUBS == 2) tc::tmem_st16(ta + 16, wb);
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
         // test-only fault: the first CTA's first producer warp never marks the
         // last k-tile of its last item stored, so the MMA warps' wait on it
         // runs out (every copy of the CTA has landed by then)
-        const bool withhold = GATEUP && g.fault == 1 && blockIdx.x == 0 && pw == 0 && u == NU - 1 && hh == 1;
+        const bool withhold = GATEUP && g.fault == 1 && blockIdx.x == 0 && pw == 0 && u == NU - 1 && hh == HPS - 1;
         if (lane == 0 && !withhold) tc::mbar_arrive(&full[stage]);
         ++kg;
         // then dequantise the next k-tile while the MMAs run
-        if (hh == 0) {
-          deq(u, 1);
+        if (hh < HPS - 1) {
+          deq(u, hh + 1, wa, wb);
         } else {
           // every read of slot u is done: release it to the weight loader
           // (whole rows: after the item's last super-block)
@@ -556,7 +570,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
           }
           if (u + 1 < NU) {
             if (!open_sb(u + 1)) ok = false;
-            else deq(u + 1, 0);
+            else deq(u + 1, 0, wa, wb);
           }
         }
         if (!ok) break;
@@ -639,11 +653,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
             break;
           }
           uint8_t* b_st = sB + stage * TC_B_BYTES;
-          tc::mbar_expect_tx(&tok_full[stage], (uint32_t)n32 * 2 * 32 * 128);
-          for (int half = 0; half < 2; ++half)
+          tc::mbar_expect_tx(&tok_full[stage], (uint32_t)n32 * (BK / 64) * 32 * 128);
+          for (int half = 0; half < BK / 64; ++half)
             for (int i = 0; i < n32; ++i)
-              tc::tma_load_2d(b_st + half * TC_B_HALF + i * 4096, &maps.tok, kt * TC_BK + 64 * half, pos0 + 32 * i,
-                          &tok_full[stage]);
+              tc::tma_load_2d(b_st + half * TC_B_HALF + i * 4096, &maps.tok, kt * BK + 64 * half, pos0 + 32 * i,
+                              &tok_full[stage]);
         }
       }
     }
@@ -675,12 +689,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a = tmem + TC_A_COL + (uint32_t)stage * TC_A_STAGE_COLS + (uint32_t)which * (TC_BK / 2);
+          const uint32_t a = tmem + TC_A_COL + (uint32_t)stage * Cfg::A_STAGE_COLS + (uint32_t)which * (BK / 2);
           // the descriptor's start address (16-byte units, low bits) advances by
           // 32 bytes per K step of 16 within a K half, by TC_B_HALF per half
           const uint64_t bd = bdesc0 + (uint64_t)(ts * (TC_B_BYTES >> 4));
 #pragma unroll
-          for (int kk = 0; kk < TC_BK / 16; ++kk)
+          for (int kk = 0; kk < BK / 16; ++kk)
             tc::mma_bf16_ts(d_tmem, a + 8 * kk, bd + (uint64_t)((kk >> 2) * (TC_B_HALF >> 4) + 2 * (kk & 3)), idesc,
                             (kt | kk) != 0);
           tc::mma_commit(&empty[stage]);
@@ -705,8 +719,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
 }
 
 // Builds the token-chunk list: every expert with rows (the shared expert
-// last) is cut into ceil(rows / 128) chunks of near-equal size (first row
-// below 2^24, packed with the row count). One CTA; the scan of chunk counts
+// last) is cut into ceil(rows / cap) chunks of near-equal size (first row
+// below 2^24, packed with the row count - 1 in the top 8 bits). One CTA; the scan of chunk counts
 // runs in warp 0.
 __global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __restrict__ offsets, int E, int cap,
                                                             int2* __restrict__ chunks,
@@ -738,10 +752,10 @@ __global__ void __launch_bounds__(1024) build_chunks_kernel(const int32_t* __res
     if (Me <= 0) continue;
     const int nc = (Me + cap - 1) / cap;
     for (int i = 0; i < nc; ++i) {
-      // rows [i*Me/nc, (i+1)*Me/nc): between 1 and 128 of them
+      // rows [i*Me/nc, (i+1)*Me/nc): between 1 and cap of them
       const int c0 = (int)((long long)i * Me / nc);
       const int c1 = (int)((long long)(i + 1) * Me / nc);
-      chunks[start[e] + i] = make_int2(e, c0 | ((c1 - c0 - 1) << 24));
+      chunks[start[e] + i] = make_int2(e, (int)((uint32_t)c0 | ((uint32_t)(c1 - c0 - 1) << 24)));
     }
   }
 }
@@ -838,11 +852,14 @@ int tc_max_chunks(int T, int k, int E, int has_shared) {
   return (P + (has_shared ? T : 0)) / TC_N_MIN + E + 1;
 }
 
-int tc_chunk_cap(int T, int k, int E) { return (long long)T * k <= 32LL * E ? 64 : 128; }
+int tc_chunk_cap(int T, int k, int E) {
+  const long long P = (long long)T * k;
+  return P <= 32LL * E ? 64 : (P <= (long long)TC_CAP192_MIN_ROWS * E ? 128 : 192);
+}
 
 cudaError_t launch_build_chunks(const int32_t* offsets, int E, int cap, int2* chunks, int32_t* n_chunks,
                                 cudaStream_t st) {
-  if (cap != 64 && cap != 128) return cudaErrorInvalidValue;
+  if (cap != 64 && cap != 128 && cap != 192) return cudaErrorInvalidValue;
   build_chunks_kernel<<<1, 1024, sizeof(int32_t) * (E + 1), st>>>(offsets, E, cap, chunks, n_chunks);
   return cudaGetLastError();
 }
@@ -907,6 +924,8 @@ static bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_
 
 template <bool GATEUP, int QT, int NMAX>
 static cudaError_t tc_launch_n(const TcArgs& a, const TcMaps& maps, int max_items, cudaStream_t st) {
+  static_assert(TcCfg<QT, NMAX>::SMEM <= 227 * 1024, "shared memory per CTA");
+  static_assert(TcCfg<QT, NMAX>::S >= 2 && TcCfg<QT, NMAX>::TS >= TcCfg<QT, NMAX>::S, "ring depths");
   cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(moe_tc_kernel<GATEUP, QT, NMAX>),
                                      TcCfg<QT, NMAX>::SMEM);
   if (e != cudaSuccess) return e;
@@ -919,8 +938,9 @@ static cudaError_t tc_launch_n(const TcArgs& a, const TcMaps& maps, int max_item
 
 template <bool GATEUP, int QT>
 static cudaError_t tc_launch_t(const TcArgs& a, const TcMaps& maps, int max_items, int nmax, cudaStream_t st) {
-  return nmax == 64 ? tc_launch_n<GATEUP, QT, 64>(a, maps, max_items, st)
-                    : tc_launch_n<GATEUP, QT, 128>(a, maps, max_items, st);
+  return nmax == 64    ? tc_launch_n<GATEUP, QT, 64>(a, maps, max_items, st)
+         : nmax == 128 ? tc_launch_n<GATEUP, QT, 128>(a, maps, max_items, st)
+                       : tc_launch_n<GATEUP, QT, 192>(a, maps, max_items, st);
 }
 
 static TcArgs tc_args(const GroupedTcArgs& p) {

@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
       for (int i = 0; i < nc; ++i) {
         const int c0 = (int)((long long)i * Me / nc);
         const int c1 = (int)((long long)(i + 1) * Me / nc);
-        chunks[cstart[e] + i] = make_int2(e, c0 | ((c1 - c0 - 1) << 24));
+        chunks[cstart[e] + i] = make_int2(e, (int)((uint32_t)c0 | ((uint32_t)(c1 - c0 - 1) << 24)));
       }
     }
   }
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
         // rows [i Me / nc, (i + 1) Me / nc)
         const int c0 = (int)((long long)i * Me / nc);
         const int c1 = (int)((long long)(i + 1) * Me / nc);
-        chunks[cstart[e] + i] = make_int2(e, c0 | ((c1 - c0 - 1) << 24));
+        chunks[cstart[e] + i] = make_int2(e, (int)((uint32_t)c0 | ((uint32_t)(c1 - c0 - 1) << 24)));
       }
     }
   }
@@ -698,7 +698,7 @@ cudaError_t launch_route_small(const float* part, int nsplit, const int32_t* ids
                                int k, int has_shared, int32_t* ids, float* w, int32_t* offsets,
                                int32_t* perm, int32_t* active, int32_t* n_active, int* status,
                                cudaStream_t st, int cap, int2* chunks, int32_t* n_tok_chunks) {
-  if (E > 1024 || (chunks != nullptr && cap != 64 && cap != 128)) return cudaErrorInvalidValue;
+  if (E > 1024 || (chunks != nullptr && cap != 64 && cap != 128 && cap != 192)) return cudaErrorInvalidValue;
 #define QMOE_RS(EPL) \
   route_small_dispatch<EPL>(part, nsplit, ids_in, T, E, k, has_shared, ids, w, offsets, perm, \
                             active, n_active, status, st, cap, chunks, n_tok_chunks)
@@ -717,7 +717,7 @@ cudaError_t launch_perm_large(const int32_t* ids, int T, int E, int k, int has_s
                               int32_t* chunk_cnt, int32_t* offsets, int32_t* perm,
                               int32_t* active, int32_t* n_active, int* status, cudaStream_t st, int cap,
                               int2* chunks, int32_t* n_tok_chunks) {
-  if (E > 1024 || (chunks != nullptr && cap != 64 && cap != 128)) return cudaErrorInvalidValue;
+  if (E > 1024 || (chunks != nullptr && cap != 64 && cap != 128 && cap != 192)) return cudaErrorInvalidValue;
   const int P = T * k, nc = perm_chunks(P);
   perm_count_kernel<<<nc, 256, sizeof(int32_t) * E, st>>>(ids, P, E, chunk_cnt, status);
   // the scan stages every chunk count in shared memory when they fit
