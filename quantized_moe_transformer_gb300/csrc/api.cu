@@ -248,11 +248,18 @@ cudaError_t dense_prep(const float* x, int T, int K, char* base, const AttnWs& L
   return launch_to_bf16(x, xb, T, K, nullptr, T, 1, nullptr, st);
 }
 
+// The projection runs on the tensor cores when T is above the threshold and N
+// is a multiple of 256 (the grouped kernel's 256-row weight blocks), else on
+// the fp32 GEMV, which reads x itself.
+bool dense_tc(int T, int N) { return dense_uses_tc(T) && N % 256 == 0; }
+
+// With ``res`` (tensor-core path only), y = res + x . W^T, the residual added
+// in the kernel's epilogue (y may be res).
 cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int N, float* y, char* base,
-                       const AttnWs& L, int* status, cudaStream_t st) {
+                       const AttnWs& L, int* status, cudaStream_t st, const float* res = nullptr) {
   int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
   int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
-  if (dense_uses_tc(T) && N % 256 == 0) {
+  if (dense_tc(T, N)) {
     GroupedTcArgs p{};
     p.W = static_cast<const uint8_t*>(W);
     p.qt = qt;
@@ -265,6 +272,7 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
     p.tok_rows = T;
     p.nmax = 128;
     p.yout_f32 = y;
+    p.yres = res;
     p.T = T;
     p.k = 1;
     p.E = 1;
@@ -274,6 +282,7 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
     g_launches.fetch_add(1);
     return launch_down_tc(p, st);
   }
+  if (res != nullptr) return cudaErrorInvalidValue;  // (the GEMV path has no residual)
   GroupedArgs g{};
   g.W = static_cast<const uint8_t*>(W);
   g.S = nullptr;
@@ -317,8 +326,10 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
   __nv_bfloat16* kcb = reinterpret_cast<__nv_bfloat16*>(kc);
   __nv_bfloat16* vcb = reinterpret_cast<__nv_bfloat16*>(vc);
   cudaError_t e;
-  if (dense_uses_tc(T)) {
-    // RMSNorm fused into the bf16 token operand of the Q, K, V projections
+  // RMSNorm fused into the bf16 token operand when every one of the Q, K, V
+  // projections runs on the tensor cores (a GEMV projection reads the fp32
+  // normed rows)
+  if (dense_tc(T, nh * hd) && dense_tc(T, nkv * hd)) {
     e = dense_prep_norm(X, b->g1, b->eps, T, H, base, L, st);
   } else {
     e = launch_rmsnorm(X, b->g1, b->eps, rr, T, H, st);
@@ -332,17 +343,36 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
     e = launch_rope_cache(q, k, v, kcb, vcb, T, pos0, nh, nkv, hd, (double)b->rope_theta, st);
     g_launches.fetch_add(1);
   }
+  // O projection on the tensor cores: the prefill attention writes its bf16
+  // token operand itself, and the residual is added in the projection's
+  // epilogue
+  const bool o_tc = dense_tc(T, H);
+  __nv_bfloat16* ob = (o_tc && !L.chunked) ? reinterpret_cast<__nv_bfloat16*>(base + L.xb) : nullptr;
   if (e == cudaSuccess) {
-    e = launch_attention(q, kcb, vcb, part, o, T, pos0, nh, nkv, hd, L.chunked, status, wait_limit_ns(),
+    e = launch_attention(q, kcb, vcb, part, o, ob, T, pos0, nh, nkv, hd, L.chunked, status, wait_limit_ns(),
                          g_fault_site.load() == QMOE_FAULT_ATTN_FINAL ? 1 : 0, st);
     g_launches.fetch_add(L.chunked ? 2 : 1);
   }
-  float* proj_out = R ? rr : out;  // rr is free once Q, K, V exist
-  if (e == cudaSuccess) e = dense_prep(o, T, nh * hd, base, L, st);
-  if (e == cudaSuccess) e = dense_proj(o, T, nh * hd, b->Wo, QMOE_Q4K, H, proj_out, base, L, status, st);
-  if (e == cudaSuccess && R) {
-    e = launch_add(R, proj_out, out, (size_t)T * H, st);
-    g_launches.fetch_add(1);
+  if (o_tc) {
+    // the dense route and chunk list are the Q, K, V projections' (the same
+    // rows) when those ran on the tensor cores
+    if (e == cudaSuccess) {
+      if (!dense_tc(T, nh * hd)) e = dense_prep(o, T, nh * hd, base, L, st);
+      else if (ob == nullptr) {
+        e = launch_to_bf16(o, reinterpret_cast<__nv_bfloat16*>(base + L.xb), T, nh * hd, nullptr, T, 1, nullptr,
+                           st);
+        g_launches.fetch_add(1);
+      }
+    }
+    if (e == cudaSuccess) e = dense_proj(o, T, nh * hd, b->Wo, QMOE_Q4K, H, out, base, L, status, st, R);
+  } else {
+    float* proj_out = R ? rr : out;  // rr is free once Q, K, V exist
+    if (e == cudaSuccess) e = dense_prep(o, T, nh * hd, base, L, st);
+    if (e == cudaSuccess) e = dense_proj(o, T, nh * hd, b->Wo, QMOE_Q4K, H, proj_out, base, L, status, st);
+    if (e == cudaSuccess && R) {
+      e = launch_add(R, proj_out, out, (size_t)T * H, st);
+      g_launches.fetch_add(1);
+    }
   }
   return launch_status(e);
 }

@@ -121,7 +121,8 @@ __device__ __forceinline__ uint64_t at_mn_sw128_desc(uint32_t smem_addr, uint32_
 // (positions [0, pos0 + T)), o [T][nh][128] fp32; query t sits at position
 // pos0 + t and sees keys 0 .. pos0 + t.
 __global__ void __launch_bounds__(AT_THREADS, 1)
-    attn_prefill_tc_kernel(const float* __restrict__ q, float* __restrict__ o, int T, int pos0, int nh, int nkv,
+    attn_prefill_tc_kernel(const float* __restrict__ q, float* __restrict__ o, __nv_bfloat16* __restrict__ ob,
+                           int T, int pos0, int nh, int nkv,
                            int* status, unsigned long long wait_ns, int fault,
                            const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ uint8_t at_smem_raw[];
@@ -328,12 +329,25 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (ok && __all_sync(0xffffffffu, tc::mbar_wait(o_final, 0, abort_flag, lim))) {
       tc::tc_fence_after();
       const float il = 1.f / l;
-      float* orow = o + ((size_t)(t < T ? t : 0) * nh + h) * AT_HD + col;
+      const size_t row0 = ((size_t)(t < T ? t : 0) * nh + h) * AT_HD + col;
       uint32_t v[32];
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         at_tmem_ld32(tq + AT_O_COL + col + 32 * c, v);
-        if (t < T) {
+        if (t < T && ob != nullptr) {
+          // bf16 (nearest even) in the tensor-core operand order: word i of
+          // a group of 8 head dims holds dims i and i + 4
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint4 w;
+            w.x = tc::pack_bf16x2(__uint_as_float(v[8 * m + 0]) * il, __uint_as_float(v[8 * m + 4]) * il);
+            w.y = tc::pack_bf16x2(__uint_as_float(v[8 * m + 1]) * il, __uint_as_float(v[8 * m + 5]) * il);
+            w.z = tc::pack_bf16x2(__uint_as_float(v[8 * m + 2]) * il, __uint_as_float(v[8 * m + 6]) * il);
+            w.w = tc::pack_bf16x2(__uint_as_float(v[8 * m + 3]) * il, __uint_as_float(v[8 * m + 7]) * il);
+            *reinterpret_cast<uint4*>(ob + row0 + 32 * c + 8 * m) = w;
+          }
+        } else if (t < T) {
+          float* orow = o + row0;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             *reinterpret_cast<float4*>(orow + 32 * c + 4 * i) =
@@ -470,8 +484,8 @@ static bool at_encode_cache(CUtensorMap* m, const void* base, int nkv, int rows)
 }
 
 cudaError_t launch_attention_prefill_tc(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
-                                        int T, int pos0, int nh, int nkv, int* status, unsigned long long wait_ns,
-                                        int fault, cudaStream_t st) {
+                                        __nv_bfloat16* ob, int T, int pos0, int nh, int nkv, int* status,
+                                        unsigned long long wait_ns, int fault, cudaStream_t st) {
   if (T < 1 || nkv < 1 || nh % nkv != 0) return cudaErrorInvalidValue;
   CUtensorMap km, vm;
   if (!at_encode_cache(&km, kc, nkv, pos0 + T) || !at_encode_cache(&vm, vc, nkv, pos0 + T))
@@ -479,7 +493,7 @@ cudaError_t launch_attention_prefill_tc(const float* q, const __nv_bfloat16* kc,
   cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(attn_prefill_tc_kernel), AT_SMEM);
   if (e != cudaSuccess) return e;
   attn_prefill_tc_kernel<<<dim3((T + AT_BQ - 1) / AT_BQ, nh), AT_THREADS, AT_SMEM, st>>>(
-      q, o, T, pos0, nh, nkv, status, wait_ns ? wait_ns : tc::kWaitLimitNs, fault, km, vm);
+      q, o, ob, T, pos0, nh, nkv, status, wait_ns ? wait_ns : tc::kWaitLimitNs, fault, km, vm);
   return cudaGetLastError();
 }
 

@@ -283,9 +283,10 @@ cudaError_t launch_rope_cache(float* q, const float* k, const float* v, __nv_bfl
 int attn_nchunks(int T, int pos0) { return (pos0 + T + ATT_CHUNK - 1) / ATT_CHUNK; }
 
 cudaError_t launch_attention(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* part, float* o,
-                             int T, int pos0, int nh, int nkv, int hd, bool chunked, int* status,
+                             __nv_bfloat16* ob, int T, int pos0, int nh, int nkv, int hd, bool chunked, int* status,
                              unsigned long long wait_ns, int fault, cudaStream_t st) {
   if (chunked) {
+    if (ob != nullptr) return cudaErrorInvalidValue;
     const int nc = attn_nchunks(T, pos0);
     attn_chunk_kernel<<<dim3(T * nh, nc), 256, sizeof(float) * (hd + ATT_CHUNK), st>>>(q, kc, vc, part, pos0, nh,
                                                                                           nkv, hd, nc);
@@ -295,7 +296,7 @@ cudaError_t launch_attention(const float* q, const __nv_bfloat16* kc, const __nv
     return cudaGetLastError();
   }
   if (hd != 128) return cudaErrorInvalidValue;
-  return launch_attention_prefill_tc(q, kc, vc, o, T, pos0, nh, nkv, status, wait_ns, fault, st);
+  return launch_attention_prefill_tc(q, kc, vc, o, ob, T, pos0, nh, nkv, status, wait_ns, fault, st);
 }
 
 cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaStream_t st) {

@@ -75,7 +75,8 @@ struct GroupedTcArgs {
   const __nv_bfloat16* hin;
   __nv_bfloat16* hout;
   __nv_bfloat16* yout;
-  float* yout_f32;  // down pass: write fp32 instead of bf16 when not null
+  float* yout_f32;    // down pass: write fp32 instead of bf16 when not null
+  const float* yres;  // with yout_f32: residual added in the epilogue (may alias yout_f32)
   int tok_rows;     // rows of the token matrix (xb for gate/up, hin for down)
   int nmax;         // chunk cap the chunk list was built with (64, 128 or 192)
   int T, k, E, H, F;
@@ -104,8 +105,10 @@ cudaError_t launch_dense_route(int32_t* offsets, int32_t* perm, int32_t* active,
 cudaError_t launch_rope_cache(float* q, const float* k, const float* v, __nv_bfloat16* kc, __nv_bfloat16* vc, int T,
                               int pos0, int nh, int nkv, int hd, double theta, cudaStream_t st);
 int attn_nchunks(int T, int pos0);
+// With ``ob`` (prefill only), the output rows go there as bf16 in the
+// tensor-core operand order (kPerm8 inside each group of 8) instead of to ``o``.
 cudaError_t launch_attention(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* part, float* o,
-                             int T, int pos0, int nh, int nkv, int hd, bool chunked, int* status,
+                             __nv_bfloat16* ob, int T, int pos0, int nh, int nkv, int hd, bool chunked, int* status,
                              unsigned long long wait_ns, int fault, cudaStream_t st);
 cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaStream_t st);
 
@@ -114,8 +117,8 @@ cudaError_t launch_add(const float* a, const float* b, float* y, size_t n, cudaS
 // QMOE_ERR_TIMEOUT in *status.
 // ``fault`` (test-only): 1 = CTA 0's P V issuer never marks its output final.
 cudaError_t launch_attention_prefill_tc(const float* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, float* o,
-                                        int T, int pos0, int nh, int nkv, int* status, unsigned long long wait_ns,
-                                        int fault, cudaStream_t st);
+                                        __nv_bfloat16* ob, int T, int pos0, int nh, int nkv, int* status,
+                                        unsigned long long wait_ns, int fault, cudaStream_t st);
 
 // moe_decode.cu: the decode path for T <= 4 (router kernel + one persistent
 // expert kernel, programmatic dependent launch).
