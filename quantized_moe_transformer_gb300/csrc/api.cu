@@ -165,7 +165,8 @@ int launch_status(cudaError_t e) {
 
 // ---------------------------------------------------------------- block
 struct AttnWs {
-  size_t r, q, k, v, o, part, offsets, perm, active, n_active, chunks, n_chunks, xb, total;
+  size_t r, q, k, v, o, part, offsets, perm, active, n_active, chunks, n_chunks, xb, offsets2, chunks2, n_chunks2,
+      total;
   bool chunked;
 };
 
@@ -190,6 +191,11 @@ AttnWs attn_ws_layout(const qmoe_block_desc* b, int T, int pos0) {
   L.chunks = o;   o += up256(sizeof(int2) * (size_t)tc_max_chunks(T, 1, 1, 0));
   L.n_chunks = o; o += 256;
   L.xb = o;       o += up256(sizeof(uint16_t) * T * (Q > (size_t)H ? Q : (size_t)H));
+  // the K and V projections as one launch (V as the shared expert of a
+  // two-expert chunk list; its output rows follow K's, L.v == L.k + T KV)
+  L.offsets2 = o; o += 256;
+  L.chunks2 = o;  o += up256(sizeof(int2) * (size_t)tc_max_chunks(T, 1, 1, 1));
+  L.n_chunks2 = o; o += 256;
   L.total = o;
   return L;
 }
@@ -216,20 +222,58 @@ bool dense_uses_tc(int T) { return T > g_gemm_threshold.load(); }
 
 // dense_prep of RMSNorm(x; gamma) on the tensor-core path: the norm is written
 // straight into the bf16 token operand (no fp32 normed copy).
+// (``kv_pair``: also the two-expert chunk list of the fused K and V launch)
 cudaError_t dense_prep_norm(const float* x, const float* gamma, float eps, int T, int K, char* base,
-                            const AttnWs& L, cudaStream_t st) {
+                            const AttnWs& L, bool kv_pair, cudaStream_t st) {
   int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
   int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
   int32_t* active = reinterpret_cast<int32_t*>(base + L.active);
   int32_t* n_active = reinterpret_cast<int32_t*>(base + L.n_active);
-  cudaError_t e = launch_dense_route(offsets, perm, active, n_active, T, st);
+  int32_t* offsets2 = reinterpret_cast<int32_t*>(base + L.offsets2);
+  cudaError_t e = launch_dense_route(offsets, perm, active, n_active, T, st, kv_pair ? offsets2 : nullptr);
   if (e != cudaSuccess) return e;
   int2* chunks = reinterpret_cast<int2*>(base + L.chunks);
   int32_t* n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks);
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
   if ((e = launch_build_chunks(offsets, 1, 128, chunks, n_chunks, st)) != cudaSuccess) return e;
+  if (kv_pair) {
+    e = launch_build_chunks(offsets2, 1, 128, reinterpret_cast<int2*>(base + L.chunks2),
+                            reinterpret_cast<int32_t*>(base + L.n_chunks2), st);
+    if (e != cudaSuccess) return e;
+    g_launches.fetch_add(1);
+  }
   g_launches.fetch_add(3);
   return launch_rmsnorm_bf16(x, gamma, eps, xb, T, K, st);
+}
+
+// The K and V projections of the bf16 normed rows as one tensor-core launch:
+// K is expert 0 and V the shared expert of the two-expert chunk list, so V's
+// output rows land right after K's (kv = [K rows; V rows]) and its token rows
+// are read T rows back.
+cudaError_t dense_proj_kv(int T, int K, const void* Wk, const void* Wv, int N, float* kv, char* base,
+                          const AttnWs& L, int* status, cudaStream_t st) {
+  GroupedTcArgs p{};
+  p.W = static_cast<const uint8_t*>(Wk);
+  p.S = static_cast<const uint8_t*>(Wv);
+  p.qt = QMOE_Q4K;
+  p.offsets = reinterpret_cast<int32_t*>(base + L.offsets2);
+  p.perm = reinterpret_cast<int32_t*>(base + L.perm);
+  p.chunks = reinterpret_cast<int2*>(base + L.chunks2);
+  p.n_chunks = reinterpret_cast<int32_t*>(base + L.n_chunks2);
+  p.max_chunks = tc_max_chunks(T, 1, 1, 1);
+  p.hin = reinterpret_cast<__nv_bfloat16*>(base + L.xb);
+  p.tok_rows = T;
+  p.tok_shift = T;
+  p.nmax = 128;
+  p.yout_f32 = kv;
+  p.T = T;
+  p.k = 1;
+  p.E = 1;
+  p.H = N;
+  p.F = K;
+  p.status = status;
+  g_launches.fetch_add(1);
+  return launch_down_tc(p, st);
 }
 
 cudaError_t dense_prep(const float* x, int T, int K, char* base, const AttnWs& L, cudaStream_t st) {
@@ -328,17 +372,24 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
   cudaError_t e;
   // RMSNorm fused into the bf16 token operand when every one of the Q, K, V
   // projections runs on the tensor cores (a GEMV projection reads the fp32
-  // normed rows)
-  if (dense_tc(T, nh * hd) && dense_tc(T, nkv * hd)) {
-    e = dense_prep_norm(X, b->g1, b->eps, T, H, base, L, st);
+  // normed rows); then the K and V projections run as one launch (V's rows
+  // follow K's in the workspace)
+  const bool qkv_tc = dense_tc(T, nh * hd) && dense_tc(T, nkv * hd);
+  const bool kv_pair = qkv_tc && L.v == L.k + sizeof(float) * (size_t)T * nkv * hd;
+  if (qkv_tc) {
+    e = dense_prep_norm(X, b->g1, b->eps, T, H, base, L, kv_pair, st);
   } else {
     e = launch_rmsnorm(X, b->g1, b->eps, rr, T, H, st);
     g_launches.fetch_add(1);
     if (e == cudaSuccess) e = dense_prep(rr, T, H, base, L, st);
   }
   if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wq, QMOE_Q4K, nh * hd, q, base, L, status, st);
-  if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wk, QMOE_Q4K, nkv * hd, k, base, L, status, st);
-  if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wv, QMOE_Q4K, nkv * hd, v, base, L, status, st);
+  if (kv_pair) {
+    if (e == cudaSuccess) e = dense_proj_kv(T, H, b->Wk, b->Wv, nkv * hd, k, base, L, status, st);
+  } else {
+    if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wk, QMOE_Q4K, nkv * hd, k, base, L, status, st);
+    if (e == cudaSuccess) e = dense_proj(rr, T, H, b->Wv, QMOE_Q4K, nkv * hd, v, base, L, status, st);
+  }
   if (e == cudaSuccess) {
     e = launch_rope_cache(q, k, v, kcb, vcb, T, pos0, nh, nkv, hd, (double)b->rope_theta, st);
     g_launches.fetch_add(1);

@@ -76,8 +76,11 @@ cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, float eps, _
   return cudaGetLastError();
 }
 
-// Routing of a dense projection seen as one expert (index 0) holding all rows.
-__global__ void dense_route_kernel(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T) {
+// Routing of a dense projection seen as one expert (index 0) holding all rows;
+// with ``offsets2``, also the offsets of a pair of projections of the same rows
+// run as one launch (the first as expert 0, the second as the shared expert).
+__global__ void dense_route_kernel(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T,
+                                   int32_t* offsets2) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T; i += gridDim.x * blockDim.x) perm[i] = i;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     offsets[0] = 0;
@@ -85,6 +88,11 @@ __global__ void dense_route_kernel(int32_t* offsets, int32_t* perm, int32_t* act
     offsets[2] = T;
     active[0] = 0;
     n_active[0] = 1;
+    if (offsets2 != nullptr) {
+      offsets2[0] = 0;
+      offsets2[1] = T;
+      offsets2[2] = 2 * T;
+    }
   }
 }
 
@@ -264,10 +272,10 @@ cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, float*
 }
 
 cudaError_t launch_dense_route(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T,
-                               cudaStream_t st) {
+                               cudaStream_t st, int32_t* offsets2) {
   int blocks = (T + 255) / 256;
   if (blocks > 64) blocks = 64;
-  dense_route_kernel<<<blocks, 256, 0, st>>>(offsets, perm, active, n_active, T);
+  dense_route_kernel<<<blocks, 256, 0, st>>>(offsets, perm, active, n_active, T, offsets2);
   return cudaGetLastError();
 }
 

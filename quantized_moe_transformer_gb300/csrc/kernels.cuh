@@ -77,6 +77,7 @@ struct GroupedTcArgs {
   __nv_bfloat16* yout;
   float* yout_f32;    // down pass: write fp32 instead of bf16 when not null
   const float* yres;  // with yout_f32: residual added in the epilogue (may alias yout_f32)
+  int tok_shift;      // down pass: the shared expert's token rows start this many rows before its output rows
   int tok_rows;     // rows of the token matrix (xb for gate/up, hin for down)
   int nmax;         // chunk cap the chunk list was built with (64, 128 or 192)
   int T, k, E, H, F;
@@ -101,7 +102,7 @@ cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, float*
 cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, float eps, __nv_bfloat16* y, int T, int H,
                                 cudaStream_t st);
 cudaError_t launch_dense_route(int32_t* offsets, int32_t* perm, int32_t* active, int32_t* n_active, int T,
-                               cudaStream_t st);
+                               cudaStream_t st, int32_t* offsets2 = nullptr);
 cudaError_t launch_rope_cache(float* q, const float* k, const float* v, __nv_bfloat16* kc, __nv_bfloat16* vc, int T,
                               int pos0, int nh, int nkv, int hd, double theta, cudaStream_t st);
 int attn_nchunks(int T, int pos0);

@@ -129,6 +129,7 @@ struct TcArgs {
   __nv_bfloat16* yout;          // down output, [P+T][H] bf16, rows in permutation order
   float* yout_f32;              // down output in fp32 instead, when not null
   const float* yres;            // with yout_f32: added to it in the epilogue (may alias it)
+  int tok_shift;                // the shared expert's token rows start this many rows before its output rows
   int T, k, E, H, F;
   int* status;
   unsigned long long wait_ns;   // a bounded wait gives up after this long
@@ -652,7 +653,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
       for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x) {
         const Chunk ch = chunk_at(g.chunks, wi / NB);
         const int n32 = (ch.n + 31) >> 5;  // NMAX is a multiple of 32
-        const int pos0 = g.offsets[ch.e] + ch.c0;
+        const int pos0 = g.offsets[ch.e] + ch.c0 - (ch.e == g.E ? g.tok_shift : 0);
         for (int kt = 0; kt < KT; ++kt, ++kg) {
           const int stage = kg % TS;
           if (!tc::mbar_wait(&tok_empty[stage], ((kg / TS) & 1) ^ 1, abort_flag, lim)) {
@@ -956,6 +957,7 @@ static TcArgs tc_args(const GroupedTcArgs& p) {
   a.offsets = p.offsets; a.perm = p.perm; a.chunks = p.chunks; a.n_chunks = p.n_chunks;
   a.xb = p.xb; a.hin = p.hin; a.hout = p.hout; a.yout = p.yout; a.yout_f32 = p.yout_f32;
   a.yres = p.yres;
+  a.tok_shift = p.tok_shift;
   a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
   a.wait_ns = p.wait_ns ? p.wait_ns : tc::kWaitLimitNs;
   a.fault = p.fault;
