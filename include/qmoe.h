@@ -198,6 +198,12 @@ int qmoe_moe_workspace_layout(const qmoe_moe_desc *d, int T, qmoe_moe_ws_layout 
  * out_host are [T][H] fp32 host arrays (pinned memory makes the copies
  * asynchronous DMA; pageable memory works too). ws is a DEVICE workspace of
  * qmoe_moe_forward_host_workspace_bytes(d, T) bytes. Routing is internal.
+ * A call that repeats the arguments (descriptor contents, buffers, T, ws,
+ * stream, device, path thresholds) of an earlier one replays a CUDA graph of
+ * the copies and the kernels, captured on its second occurrence (the first
+ * runs directly); calls with pageable buffers, on a stream that is already
+ * capturing, or while a test fault site or stage profiling is set always run
+ * directly. Same results either way.
  */
 size_t qmoe_moe_forward_host_workspace_bytes(const qmoe_moe_desc *d, int T);
 int qmoe_moe_forward_host(const qmoe_moe_desc *d, const float *X_host, const float *R_host,

@@ -2,6 +2,8 @@
 // The operations are defined in include/qmoe.h.
 #include <atomic>
 #include <climits>
+#include <cstring>
+#include <mutex>
 #include <cstdio>
 
 #include "kernels.cuh"
@@ -804,6 +806,74 @@ size_t qmoe_moe_forward_host_workspace_bytes(const qmoe_moe_desc* d, int T) {
   return base + 3 * up256(sizeof(float) * (size_t)T * d->H);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Copies in, the layer, copies out: the work of one host-buffer call, enqueued
+// on ``st`` (no wait).
+int host_forward_enqueue(const qmoe_moe_desc* d, const float* X_host, const float* R_host, float* out_host, int T,
+                         void* ws, cudaStream_t st) {
+  const size_t base = qmoe_moe_workspace_bytes(d, T);
+  const size_t rows = up256(sizeof(float) * (size_t)T * d->H);
+  char* p = static_cast<char*>(ws);
+  float* Xd = reinterpret_cast<float*>(p + base);
+  float* Rd = R_host ? reinterpret_cast<float*>(p + base + rows) : nullptr;
+  float* Od = reinterpret_cast<float*>(p + base + 2 * rows);
+  const size_t nbytes = sizeof(float) * (size_t)T * d->H;
+  if (cudaMemcpyAsync(Xd, X_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return QMOE_ERR_CUDA;
+  if (R_host && cudaMemcpyAsync(Rd, R_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return QMOE_ERR_CUDA;
+  int r = qmoe_moe_forward(d, Xd, Rd, nullptr, nullptr, Od, T, ws, base, reinterpret_cast<qmoe_stream_t>(st));
+  if (r != QMOE_OK) return r;
+  if (cudaMemcpyAsync(out_host, Od, nbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return QMOE_ERR_CUDA;
+  return QMOE_OK;
+}
+
+// Host-buffer calls that repeat their arguments replay a CUDA graph of the
+// copies and the layer's kernels (one launch instead of one per copy and
+// kernel). A key is the descriptor, the buffers, T, the stream, the device and
+// the path threshold; its first call runs directly (every lazy setup happens
+// then), its second captures and replays, later ones replay. Calls made while
+// a test fault site or stage profiling is set, on a stream that is already
+// capturing, or with pageable host buffers always run directly.
+struct HostGraph {
+  qmoe_moe_desc d;
+  const float *x, *r;
+  float* out;
+  int T, device, threshold, decode_rows;
+  void* ws;
+  cudaStream_t st;
+  int calls;       // calls seen with this key
+  bool direct;     // never replayed (capture failed or pageable buffers)
+  cudaGraphExec_t exec;
+  long long launches;
+  int path;
+};
+constexpr int kHostGraphs = 64;
+std::mutex g_hg_mu;
+HostGraph g_hg[kHostGraphs];
+int g_hg_n = 0, g_hg_next = 0;
+
+bool host_pinned(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+bool same_key(const HostGraph& g, const qmoe_moe_desc* d, const float* x, const float* r, float* out, int T,
+              void* ws, cudaStream_t st, int device, int threshold, int decode_rows) {
+  return g.x == x && g.r == r && g.out == out && g.T == T && g.ws == ws && g.st == st && g.device == device &&
+         g.threshold == threshold && g.decode_rows == decode_rows && memcmp(&g.d, d, sizeof(*d)) == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
 int qmoe_moe_forward_host(const qmoe_moe_desc* d, const float* X_host, const float* R_host,
                           float* out_host, int T, void* ws, size_t ws_bytes,
                           qmoe_stream_t stream) {
@@ -816,20 +886,71 @@ int qmoe_moe_forward_host(const qmoe_moe_desc* d, const float* X_host, const flo
   const size_t base = qmoe_moe_workspace_bytes(d, T);
   const size_t rows = up256(sizeof(float) * (size_t)T * d->H);
   if (ws_bytes < base + 3 * rows) return QMOE_ERR_WORKSPACE;
-  char* p = static_cast<char*>(ws);
-  float* Xd = reinterpret_cast<float*>(p + base);
-  float* Rd = R_host ? reinterpret_cast<float*>(p + base + rows) : nullptr;
-  float* Od = reinterpret_cast<float*>(p + base + 2 * rows);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t nbytes = sizeof(float) * (size_t)T * d->H;
-  if (cudaMemcpyAsync(Xd, X_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return QMOE_ERR_CUDA;
-  if (R_host && cudaMemcpyAsync(Rd, R_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return QMOE_ERR_CUDA;
-  r = qmoe_moe_forward(d, Xd, Rd, nullptr, nullptr, Od, T, ws, base, stream);
+
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  int device = 0;
+  const bool graphs_ok = g_fault_site.load() == 0 && g_prof.stage == 0 &&
+                         cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone &&
+                         cudaGetDevice(&device) == cudaSuccess;
+  if (graphs_ok) {
+    std::lock_guard<std::mutex> lock(g_hg_mu);
+    const int threshold = g_gemm_threshold.load(), decode_rows = g_decode_max_rows.load();
+    HostGraph* g = nullptr;
+    for (int i = 0; i < g_hg_n && !g; ++i)
+      if (same_key(g_hg[i], d, X_host, R_host, out_host, T, ws, st, device, threshold, decode_rows)) g = &g_hg[i];
+    if (g == nullptr) {
+      // a new key (replacing the oldest when the table is full): this call runs directly
+      g = &g_hg[g_hg_next];
+      if (g_hg_n < kHostGraphs) ++g_hg_n;
+      g_hg_next = (g_hg_next + 1) % kHostGraphs;
+      if (g->exec) cudaGraphExecDestroy(g->exec);
+      *g = HostGraph{};
+      g->d = *d;
+      g->x = X_host;
+      g->r = R_host;
+      g->out = out_host;
+      g->T = T;
+      g->device = device;
+      g->threshold = threshold;
+      g->decode_rows = decode_rows;
+      g->ws = ws;
+      g->st = st;
+      g->direct = !host_pinned(X_host) || !host_pinned(out_host) || (R_host && !host_pinned(R_host));
+    } else if (!g->direct) {
+      if (g->exec == nullptr) {
+        // second call: capture the copies and kernels once
+        cudaGraph_t graph = nullptr;
+        const long long l0 = g_launches.load();
+        bool ok = cudaStreamBeginCapture(st, cudaStreamCaptureModeRelaxed) == cudaSuccess;
+        int rr = ok ? host_forward_enqueue(d, X_host, R_host, out_host, T, ws, st) : QMOE_ERR_CUDA;
+        if (ok) ok = cudaStreamEndCapture(st, &graph) == cudaSuccess && rr == QMOE_OK;
+        if (ok) ok = cudaGraphInstantiate(&g->exec, graph, 0) == cudaSuccess;
+        if (graph) cudaGraphDestroy(graph);
+        if (!ok) {
+          cudaGetLastError();
+          if (g->exec) cudaGraphExecDestroy(g->exec);
+          g->exec = nullptr;
+          g->direct = true;
+          if (rr != QMOE_OK && rr != QMOE_ERR_CUDA) return rr;
+        } else {
+          g->launches = g_launches.load() - l0;
+          g->path = g_last_path;
+        }
+      }
+      if (g->exec) {
+        if (cudaGraphLaunch(g->exec, st) != cudaSuccess) return QMOE_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return QMOE_ERR_CUDA;
+        g_launches.fetch_add(g->launches);
+        g_last_path = g->path;
+        ++g->calls;
+        return QMOE_OK;
+      }
+    }
+    ++g->calls;
+  }
+  r = host_forward_enqueue(d, X_host, R_host, out_host, T, ws, st);
   if (r != QMOE_OK) return r;
-  if (cudaMemcpyAsync(out_host, Od, nbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return QMOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return QMOE_ERR_CUDA;
   return QMOE_OK;
 }
