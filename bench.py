@@ -570,13 +570,16 @@ def ours_main(args, rank, world, local_rank):
         Oh = torch.empty_like(Xh).pin_memory()
         hws = torch.empty(qb.host_workspace_bytes(layers[0], T), dtype=torch.uint8, device=device)
         n_e2e = min(args.steps, 400)
+        calls = [(layers[i], Xh[i], Oh[i]) for i in range(NL)]  # each layer instance's own buffers
         # warm-up: every layer's host call twice (the second captures the graph
         # that later calls with the same arguments replay)
         for i in range(2 * NL + 1):
-            qb.moe_forward_host(layers[i % NL], Xh[i % NL], out=Oh[i % NL], ws=hws, stream=stream)
+            lay, xi, oi = calls[i % NL]
+            qb.moe_forward_host(lay, xi, out=oi, ws=hws, stream=stream)
         t0 = time.perf_counter()
         for i in range(n_e2e):
-            qb.moe_forward_host(layers[i % NL], Xh[i % NL], out=Oh[i % NL], ws=hws, stream=stream)
+            lay, xi, oi = calls[i % NL]
+            qb.moe_forward_host(lay, xi, out=oi, ws=hws, stream=stream)
         dt = time.perf_counter() - t0
         e2e = {"value": T * n_e2e * world / dt, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 4,
                "d2h_bytes_per_step": T * H * 4, "steps": n_e2e,

@@ -236,6 +236,9 @@ def moe_forward_host(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = 
     if ws is None:
         n = int(lib().qmoe_moe_forward_host_workspace_bytes(ctypes.byref(layer.desc), T))
         ws = torch.empty(max(n, 256), dtype=torch.uint8, device=layer.Wr.device)
+    for t in (X, R, out):
+        if t is not None and (t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32):
+            raise QmoeError("moe_forward_host takes contiguous fp32 host tensors")
     hp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     _check(lib().qmoe_moe_forward_host(ctypes.byref(layer.desc), hp(X), hp(R), hp(out), T,
                                        _ptr(ws), ws.numel(), _stream(stream)))
