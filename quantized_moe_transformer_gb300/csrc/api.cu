@@ -299,10 +299,8 @@ cudaError_t dense_prep(const float* x, int T, int K, char* base, const AttnWs& L
 // the fp32 GEMV, which reads x itself.
 bool dense_tc(int T, int N) { return dense_uses_tc(T) && N % 256 == 0; }
 
-// With ``res`` (tensor-core path only), y = res + x . W^T, the residual added
-// in the kernel's epilogue (y may be res).
 cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int N, float* y, char* base,
-                       const AttnWs& L, int* status, cudaStream_t st, const float* res = nullptr) {
+                       const AttnWs& L, int* status, cudaStream_t st) {
   int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
   int32_t* perm = reinterpret_cast<int32_t*>(base + L.perm);
   if (dense_tc(T, N)) {
@@ -318,7 +316,6 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
     p.tok_rows = T;
     p.nmax = 128;
     p.yout_f32 = y;
-    p.yres = res;
     p.T = T;
     p.k = 1;
     p.E = 1;
@@ -328,7 +325,6 @@ cudaError_t dense_proj(const float* x, int T, int K, const void* W, int qt, int 
     g_launches.fetch_add(1);
     return launch_down_tc(p, st);
   }
-  if (res != nullptr) return cudaErrorInvalidValue;  // (the GEMV path has no residual)
   GroupedArgs g{};
   g.W = static_cast<const uint8_t*>(W);
   g.S = nullptr;
@@ -397,9 +393,9 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
     g_launches.fetch_add(1);
   }
   // O projection on the tensor cores: the prefill attention writes its bf16
-  // token operand itself, and the residual is added in the projection's
-  // epilogue
-  const bool o_tc = dense_tc(T, H);
+  // token operand itself
+  // (with the route and chunk list of these rows from the Q, K, V projections)
+  const bool o_tc = dense_tc(T, H) && qkv_tc;
   __nv_bfloat16* ob = (o_tc && !L.chunked) ? reinterpret_cast<__nv_bfloat16*>(base + L.xb) : nullptr;
   if (e == cudaSuccess) {
     e = launch_attention(q, kcb, vcb, part, o, ob, T, pos0, nh, nkv, hd, L.chunked, status, wait_limit_ns(),
@@ -407,25 +403,21 @@ int attn_impl(const qmoe_block_desc* b, const float* X, const float* R, float* o
     g_launches.fetch_add(L.chunked ? 2 : 1);
   }
   if (o_tc) {
-    // the dense route and chunk list are the Q, K, V projections' (the same
-    // rows) when those ran on the tensor cores
-    if (e == cudaSuccess) {
-      if (!dense_tc(T, nh * hd)) e = dense_prep(o, T, nh * hd, base, L, st);
-      else if (ob == nullptr) {
-        e = launch_to_bf16(o, reinterpret_cast<__nv_bfloat16*>(base + L.xb), T, nh * hd, nullptr, T, 1, nullptr,
-                           st);
-        g_launches.fetch_add(1);
-      }
-    }
-    if (e == cudaSuccess) e = dense_proj(o, T, nh * hd, b->Wo, QMOE_Q4K, H, out, base, L, status, st, R);
-  } else {
-    float* proj_out = R ? rr : out;  // rr is free once Q, K, V exist
-    if (e == cudaSuccess) e = dense_prep(o, T, nh * hd, base, L, st);
-    if (e == cudaSuccess) e = dense_proj(o, T, nh * hd, b->Wo, QMOE_Q4K, H, proj_out, base, L, status, st);
-    if (e == cudaSuccess && R) {
-      e = launch_add(R, proj_out, out, (size_t)T * H, st);
+    // the dense route and chunk list are the Q, K, V projections' (the same rows)
+    if (e == cudaSuccess && ob == nullptr) {
+      e = launch_to_bf16(o, reinterpret_cast<__nv_bfloat16*>(base + L.xb), T, nh * hd, nullptr, T, 1, nullptr, st);
       g_launches.fetch_add(1);
     }
+  } else if (e == cudaSuccess) {
+    e = dense_prep(o, T, nh * hd, base, L, st);
+  }
+  // (the residual as its own pass: added in the projection's epilogue, the
+  // loads of R held up each 16-token group, 75 against 42 + 20 us at T=4096)
+  float* proj_out = R ? rr : out;  // rr is free once Q, K, V exist
+  if (e == cudaSuccess) e = dense_proj(o, T, nh * hd, b->Wo, QMOE_Q4K, H, proj_out, base, L, status, st);
+  if (e == cudaSuccess && R) {
+    e = launch_add(R, proj_out, out, (size_t)T * H, st);
+    g_launches.fetch_add(1);
   }
   return launch_status(e);
 }

@@ -76,7 +76,6 @@ struct GroupedTcArgs {
   __nv_bfloat16* hout;
   __nv_bfloat16* yout;
   float* yout_f32;    // down pass: write fp32 instead of bf16 when not null
-  const float* yres;  // with yout_f32: residual added in the epilogue (may alias yout_f32)
   int tok_shift;      // down pass: the shared expert's token rows start this many rows before its output rows
   int tok_rows;     // rows of the token matrix (xb for gate/up, hin for down)
   int nmax;         // chunk cap the chunk list was built with (64, 128 or 192)

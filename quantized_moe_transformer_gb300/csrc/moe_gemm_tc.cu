@@ -128,7 +128,6 @@ struct TcArgs {
   __nv_bfloat16* hout;          // gate/up output, [P+T][F] bf16
   __nv_bfloat16* yout;          // down output, [P+T][H] bf16, rows in permutation order
   float* yout_f32;              // down output in fp32 instead, when not null
-  const float* yres;            // with yout_f32: added to it in the epilogue (may alias it)
   int tok_shift;                // the shared expert's token rows start this many rows before its output rows
   int T, k, E, H, F;
   int* status;
@@ -437,15 +436,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) moe_tc_kernel(const TcArgs g, c
               for (int j = 0; j < 4; ++j) {
                 const int id = lane + 32 * j, i = id >> 3, part = id & 7;
                 const int t = c + i;
-                if (t < ch.n) {
-                  const size_t yi = (size_t)(pos0 + t) * g.H + col0 + 4 * part;
-                  float4 v4 = reinterpret_cast<const float4*>(stg)[id];
-                  if (g.yres != nullptr) {
-                    const float4 r4 = *reinterpret_cast<const float4*>(g.yres + yi);
-                    v4 = make_float4(r4.x + v4.x, r4.y + v4.y, r4.z + v4.z, r4.w + v4.w);
-                  }
-                  *reinterpret_cast<float4*>(g.yout_f32 + yi) = v4;
-                }
+                if (t < ch.n)
+                  *reinterpret_cast<uint4*>(g.yout_f32 + (size_t)(pos0 + t) * g.H + col0 + 4 * part) =
+                      reinterpret_cast<const uint4*>(stg)[id];
               }
             } else {
               __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
@@ -956,7 +949,6 @@ static TcArgs tc_args(const GroupedTcArgs& p) {
   a.W = p.W; a.W2 = p.W2; a.S = p.S; a.S2 = p.S2;
   a.offsets = p.offsets; a.perm = p.perm; a.chunks = p.chunks; a.n_chunks = p.n_chunks;
   a.xb = p.xb; a.hin = p.hin; a.hout = p.hout; a.yout = p.yout; a.yout_f32 = p.yout_f32;
-  a.yres = p.yres;
   a.tok_shift = p.tok_shift;
   a.T = p.T; a.k = p.k; a.E = p.E; a.H = p.H; a.F = p.F; a.status = p.status;
   a.wait_ns = p.wait_ns ? p.wait_ns : tc::kWaitLimitNs;

@@ -102,9 +102,8 @@ def test_prefill_attention_one_kv_head_mixed_paths(blk_pair):
     projections (1024 and 2048 outputs) run on the tensor cores, the K and V
     projections (128 outputs, not a whole 256-row weight block) on the fp32
     kernels, which read the fp32 RMSNorm rows. The K/V cache rows the call
-    writes must be the bits the all-fp32 projections write, and the residual
-    added in the O projection's epilogue must give the bits of X + the
-    sub-layer without it. (Against the oracle, bf16 queries move this slice's
+    writes must be the bits the all-fp32 projections write, and the call with
+    a residual must give the bits of X + the sub-layer without it. (Against the oracle, bf16 queries move this slice's
     large synthetic attention scores beyond the tensor-core bound; the
     all-tensor-core block is checked against the oracle in test_gpu_block.)"""
     arr, _ = blk_pair
