@@ -813,34 +813,53 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* 
 // operand K order (kPerm8 inside each group of 8): the token operand of the
 // tensor-core path. row(i) = i, or with ``perm`` the token of permutation
 // position i (pairs t*k + s, then the shared expert's rows t); then also
-// inv[perm[i]] = i, the position of each pair.
+// inv[perm[i]] = i, the position of each pair. One warp per row: the row's
+// source is looked up once, and each lane has K/256 groups of 8 values (two
+// 16-byte loads each) in flight at once.
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y,
                                                       int rows, int K, const int32_t* __restrict__ perm, int T,
                                                       int k, int32_t* __restrict__ inv) {
+  const int lane = threadIdx.x & 31;
   const int K8 = K / 8;
-  const size_t n8 = (size_t)rows * K8;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const int r = (int)(i / K8), c = (int)(i % K8);
+  const int wpb = blockDim.x >> 5;
+  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows; r += gridDim.x * wpb) {
     const int pr = perm ? perm[r] : r;
     const int src = perm ? tc_pair_row(pr, T, k) : r;
-    if (inv != nullptr && c == 0) inv[pr] = r;
-    const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)src * K) + 2 * c;
-    const float4 a = x4[0];
-    const float4 b = x4[1];
-    // group (0..7) = a.x a.y a.z a.w b.x b.y b.z b.w -> order 0,4,1,5,2,6,3,7
-    uint4 o;
-    o.x = tc::pack_bf16x2(a.x, b.x);
-    o.y = tc::pack_bf16x2(a.y, b.y);
-    o.z = tc::pack_bf16x2(a.z, b.z);
-    o.w = tc::pack_bf16x2(a.w, b.w);
-    reinterpret_cast<uint4*>(y)[i] = o;
+    if (inv != nullptr && lane == 0) inv[pr] = r;
+    const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)src * K);
+    uint4* y4 = reinterpret_cast<uint4*>(y + (size_t)r * K);
+    constexpr int G = 8;  // groups a lane converts per pass (K = 2048: the whole row)
+    for (int c0 = 0; c0 < K8; c0 += 32 * G) {
+      float4 a[G], b[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const int c = c0 + 32 * j + lane;
+        if (c < K8) {
+          a[j] = __ldg(x4 + 2 * c);
+          b[j] = __ldg(x4 + 2 * c + 1);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const int c = c0 + 32 * j + lane;
+        if (c < K8) {
+          // group (0..7) = a.x a.y a.z a.w b.x b.y b.z b.w -> order 0,4,1,5,2,6,3,7
+          uint4 o;
+          o.x = tc::pack_bf16x2(a[j].x, b[j].x);
+          o.y = tc::pack_bf16x2(a[j].y, b[j].y);
+          o.z = tc::pack_bf16x2(a[j].z, b[j].z);
+          o.w = tc::pack_bf16x2(a[j].w, b[j].w);
+          y4[c] = o;
+        }
+      }
+    }
   }
 }
 
 cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, int rows, int K, const int32_t* perm, int T, int k,
                            int32_t* inv, cudaStream_t st) {
-  const size_t n8 = (size_t)rows * (K / 8);
-  int blocks = (int)((n8 + 255) / 256);
+  // 8 rows (warps) a block, up to 8 blocks per SM
+  int blocks = (rows + 7) / 8;
   if (blocks > 152 * 8) blocks = 152 * 8;
   if (blocks < 1) blocks = 1;
   to_bf16_kernel<<<blocks, 256, 0, st>>>(x, y, rows, K, perm, T, k, inv);
