@@ -553,15 +553,7 @@ def ours_main(args, rank, world, local_rank):
         rec, clk, step, ws, outs = measure_layer(torch, qb, layers, T, routing, args.steps, args.warmup, stream,
                                                  world, device, peaks, rank, clocks=True)
         path = rec["path"]
-        traffic = None
-        tf = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-        kernel_sha = source_sha(KERNEL_SOURCES[path])
-        if os.path.exists(tf):
-            r = json.load(open(tf)).get(f"{path}:{args.workload}")
-            if r and r.get("source_sha") == kernel_sha:
-                traffic = r["dram_bytes_per_launch"]
-        rec["roofline"]["traffic"] = traffic
-        rec["roofline"]["kernel_source_sha"] = kernel_sha
+        attach_traffic(rec, args.workload)
 
         # end to end through the C ABI on host buffers (pinned), copies inside
         Xh = torch.randn((NL, T, H), generator=torch.Generator().manual_seed(11)).pin_memory()
@@ -596,6 +588,7 @@ def ours_main(args, rank, world, local_rank):
             r, _, _, _, _ = measure_layer(torch, qb, layers, Tx, routing, st, 3 * NL // 2, stream, world, device,
                                           peaks, rank)
             r["tokens_per_s"] *= world
+            attach_traffic(r, {"decode_t64": "decode64", "prefill_t4096": "prefill4096"}[key])
             extras[key] = r
         torch.cuda.empty_cache()
 
@@ -684,6 +677,22 @@ TRAFFIC_KERNELS = {
     "gemm_tc": ("moe_tc_kernel<1,", ("moe_tc_kernel<1,",)),
     "gemv": ("gateup_gemv_kernel", ("gateup_gemv_kernel",)),
 }
+
+
+def attach_traffic(rec, workload):
+    """rec["roofline"]["traffic"]: the dominant kernel's DRAM bytes per launch
+    recorded in profiles/ncu_traffic.json for this path and workload, when the
+    record was taken on the current kernel sources (else None)."""
+    path = rec["path"]
+    kernel_sha = source_sha(KERNEL_SOURCES[path])
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if os.path.exists(tf):
+        r = json.load(open(tf)).get(f"{path}:{workload}")
+        if r and r.get("source_sha") == kernel_sha:
+            traffic = r["dram_bytes_per_launch"]
+    rec["roofline"]["traffic"] = traffic
+    rec["roofline"]["kernel_source_sha"] = kernel_sha
 
 
 def record_traffic(args):
