@@ -76,3 +76,32 @@ def test_reference_arm_json_line():
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_traffic_record_attaches_only_on_current_sources(tmp_path, monkeypatch):
+    """A DRAM-traffic record is attached to a roofline only when it was taken on
+    the kernel sources as they are now (same source hash), for the same path
+    and workload."""
+    import json
+
+    sha = bench.source_sha(bench.KERNEL_SOURCES["gemm_tc"])
+    (tmp_path / "profiles").mkdir()
+    rec_file = tmp_path / "profiles" / "ncu_traffic.json"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_sha", lambda paths: sha)
+
+    def attached(records, workload="prefill4096"):
+        rec_file.write_text(json.dumps(records))
+        r = {"path": "gemm_tc", "roofline": {}}
+        bench.attach_traffic(r, workload)
+        return r["roofline"]["traffic"], r["roofline"]["kernel_source_sha"]
+
+    good = {"gemm_tc:prefill4096": {"dram_bytes_per_launch": 123.0, "source_sha": sha}}
+    assert attached(good) == (123.0, sha)
+    stale = {"gemm_tc:prefill4096": {"dram_bytes_per_launch": 123.0, "source_sha": "0" * 16}}
+    assert attached(stale) == (None, sha)
+    assert attached(good, workload="decode64") == (None, sha)
+    rec_file.unlink()
+    r = {"path": "gemm_tc", "roofline": {}}
+    bench.attach_traffic(r, "prefill4096")
+    assert r["roofline"]["traffic"] is None
