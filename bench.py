@@ -82,6 +82,10 @@ def parse():
                    help="rows above which the tensor-core path is taken (library default if unset)")
     p.add_argument("--cpu-seconds", type=float, default=24.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--stage-split", action="store_true",
+                   help="add each stage's time per layer step inside graph replays (router, route, gateup, "
+                        "down, combine, decode: event-record nodes around each stage's launches, which add a "
+                        "few us each) to the line as stages_in_graph_us")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the T=64 and T=4096 points the default decode run adds to its line")
     p.add_argument("--cpu-sample", type=str, default=None, help=argparse.SUPPRESS)
@@ -413,13 +417,19 @@ def gateup_in_graph_us(torch, qb, step, NL, stream, replays=3):
     library brackets each gate/up launch with events, which stream capture turns
     into event-record nodes of the graph; after each replay the times of that
     replay's launches are read back."""
+    return stage_in_graph_us(torch, qb, step, NL, stream, "gateup", replays)
+
+
+def stage_in_graph_us(torch, qb, step, NL, stream, stage, replays=3):
+    """(Average time per bracketed launch group of ``stage`` inside graph
+    replays of NL layer steps, number of groups read.)"""
     with torch.cuda.stream(stream):
-        qb.profile_start("gateup")          # events created outside the capture
+        qb.profile_start(stage)             # events created outside the capture
         for i in range(NL):
             step(i, stream)
         qb.profile_stop()
         torch.cuda.synchronize()
-        qb.profile_start("gateup")
+        qb.profile_start(stage)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(NL):
@@ -432,7 +442,17 @@ def gateup_in_graph_us(torch, qb, step, NL, stream, replays=3):
         tot += ms
         n += k
     qb.profile_stop()
-    return 1e3 * tot / n, n
+    return (1e3 * tot / n if n else 0.0), n
+
+
+def stages_per_step_us(torch, qb, step, NL, stream, replays=3):
+    """Each stage's time per layer step inside graph replays (a stage with no
+    launches on the path reads 0)."""
+    out = {}
+    for stage in ("router", "route", "gateup", "down", "combine", "decode"):
+        us, n = stage_in_graph_us(torch, qb, step, NL, stream, stage, replays)
+        out[stage] = round(us * n / (replays * NL), 2)
+    return out
 
 
 def distinct_experts(torch, qb, layers, step, ws, ws_off, T, NL, stream):
@@ -554,6 +574,8 @@ def ours_main(args, rank, world, local_rank):
                                                  world, device, peaks, rank, clocks=True)
         path = rec["path"]
         attach_traffic(rec, args.workload)
+        if args.stage_split:
+            rec["stages_in_graph_us"] = stages_per_step_us(torch, qb, step, len(layers), stream)
 
         # end to end through the C ABI on host buffers (pinned), copies inside
         Xh = torch.randn((NL, T, H), generator=torch.Generator().manual_seed(11)).pin_memory()
@@ -613,6 +635,8 @@ def ours_main(args, rank, world, local_rank):
                 "layer_hbm": rec.get("layer_hbm"), "layer_tflops": rec.get("layer_tflops"),
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": rec["launches_per_step"] * args.steps,
                 "launches_per_step": rec["launches_per_step"], "clocks": clk, "parity": parity}
+        if "stages_in_graph_us" in rec:
+            line["stages_in_graph_us"] = rec["stages_in_graph_us"]
         line.update(extras)
         print(json.dumps(line))
 
