@@ -802,6 +802,23 @@ size_t qmoe_moe_forward_host_workspace_bytes(const qmoe_moe_desc* d, int T) {
 
 namespace {
 
+// The device-accessible address of pinned, mapped host memory ``p`` (nullptr
+// when it has none: pageable memory).
+const void* host_mapped(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Outputs up to this size are written by the layer's last kernel straight into
+// mapped host memory (and a residual of the same size is read from there): no
+// copy node, a few KB over the host link; larger ones go through the workspace
+// and one copy.
+constexpr size_t kDirectHostBytes = 1 << 20;
+
 // Copies in, the layer, copies out: the work of one host-buffer call, enqueued
 // on ``st`` (no wait).
 int host_forward_enqueue(const qmoe_moe_desc* d, const float* X_host, const float* R_host, float* out_host, int T,
@@ -813,12 +830,20 @@ int host_forward_enqueue(const qmoe_moe_desc* d, const float* X_host, const floa
   float* Rd = R_host ? reinterpret_cast<float*>(p + base + rows) : nullptr;
   float* Od = reinterpret_cast<float*>(p + base + 2 * rows);
   const size_t nbytes = sizeof(float) * (size_t)T * d->H;
+  float* out_dev = nullptr;
+  const float* res_dev = nullptr;
+  if (nbytes <= kDirectHostBytes) {
+    out_dev = static_cast<float*>(const_cast<void*>(host_mapped(out_host)));
+    if (R_host) res_dev = static_cast<const float*>(host_mapped(R_host));
+  }
   if (cudaMemcpyAsync(Xd, X_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return QMOE_ERR_CUDA;
-  if (R_host && cudaMemcpyAsync(Rd, R_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  if (R_host && !res_dev && cudaMemcpyAsync(Rd, R_host, nbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return QMOE_ERR_CUDA;
-  int r = qmoe_moe_forward(d, Xd, Rd, nullptr, nullptr, Od, T, ws, base, reinterpret_cast<qmoe_stream_t>(st));
+  int r = qmoe_moe_forward(d, Xd, res_dev ? res_dev : Rd, nullptr, nullptr, out_dev ? out_dev : Od, T, ws, base,
+                           reinterpret_cast<qmoe_stream_t>(st));
   if (r != QMOE_OK) return r;
-  if (cudaMemcpyAsync(out_host, Od, nbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return QMOE_ERR_CUDA;
+  if (!out_dev && cudaMemcpyAsync(out_host, Od, nbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return QMOE_ERR_CUDA;
   return QMOE_OK;
 }
 
