@@ -131,6 +131,7 @@ class MoeLayer:
         self._desc = MoeDesc(H, E, k, F, QTYPE[gate_type], QTYPE[down_type],
                              _ptr(Wr), _ptr(Wg), _ptr(Wu), _ptr(Wd),
                              _ptr(Sg), _ptr(Su), _ptr(Sd))
+        self._desc_ref = ctypes.byref(self._desc)
 
     @classmethod
     def from_arrays(cls, layer: dict, k: int, device="cuda"):
@@ -228,8 +229,6 @@ def moe_forward_host(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = 
                      stream=None) -> torch.Tensor:
     """The layer on HOST tensors (pinned for asynchronous copies): the library
     copies X (and R) in, runs the layer and copies the result back, then waits."""
-    if X.is_cuda:
-        raise QmoeError("moe_forward_host takes host tensors")
     T = X.shape[0]
     if out is None:
         out = torch.empty_like(X)
@@ -237,11 +236,15 @@ def moe_forward_host(layer: MoeLayer, X: torch.Tensor, R: torch.Tensor | None = 
         n = int(lib().qmoe_moe_forward_host_workspace_bytes(ctypes.byref(layer.desc), T))
         ws = torch.empty(max(n, 256), dtype=torch.uint8, device=layer.Wr.device)
     for t in (X, R, out):
-        if t is not None and (t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32):
+        if t is not None and (t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()):
             raise QmoeError("moe_forward_host takes contiguous fp32 host tensors")
-    hp = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
-    _check(lib().qmoe_moe_forward_host(ctypes.byref(layer.desc), hp(X), hp(R), hp(out), T,
-                                       _ptr(ws), ws.numel(), _stream(stream)))
+    if not ws.is_cuda:
+        raise QmoeError("the workspace must be on a CUDA device")
+    # (a per-call path: integer addresses and the layer's cached descriptor
+    # reference, converted by the argument types declared in lib())
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib().qmoe_moe_forward_host(layer._desc_ref, X.data_ptr(), None if R is None else R.data_ptr(),
+                                       out.data_ptr(), T, ws.data_ptr(), ws.numel(), s.cuda_stream))
     return out
 
 
