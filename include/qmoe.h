@@ -204,7 +204,7 @@ int qmoe_moe_workspace_layout(const qmoe_moe_desc *d, int T, qmoe_moe_ws_layout 
  * runs directly); calls with pageable buffers, on a stream that is already
  * capturing, or while a test fault site or stage profiling is set always run
  * directly. Same results either way. With pinned (mapped) host buffers of at
- * most 1 MiB, the layer's last kernel writes out_host itself and reads R_host
+ * most 4 MiB, the layer's last kernel writes out_host itself and reads R_host
  * itself (no copy for them); X_host is always copied in.
  */
 size_t qmoe_moe_forward_host_workspace_bytes(const qmoe_moe_desc *d, int T);
